@@ -1,0 +1,88 @@
+"""Seeded synthetic workloads for exact tiled attention.
+
+This module only draws inputs; it holds none of the attention arithmetic, so
+both the CUDA path and the fp64 CPU oracle can be fed from it without sharing
+any computation.
+
+Shapes follow the ``[B, heads, S, head_dim]`` activation layout of the
+"07-16 下午：分布式大模型训练与推理" notes (section 自回归语言模型推理, step 3 of
+the tensor walk-through), written here as ``[B, H, N, d]``. The five workloads
+are the GPT-2-small, ragged-tile, Llama and long-context shapes this library is
+measured on; the ragged one uses the context length 1028 with 64-wide tiles
+that the dcwnkz.com FlashAttention walk-through (CS336 tricks, "回到
+FlashAttention") uses as its example of tiling along N.
+
+Recipe: ``torch.Generator().manual_seed(seed)`` on the CPU, fp32 normal draws
+in the order q, k, v, dO, each multiplied by its standard deviation, then
+rounded to bf16 (round-to-nearest-even). Seeds are ``1000 + config index``.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: tuple  # the causal settings this workload is run with
+    directions: tuple  # ("fwd",) or ("fwd", "bwd")
+    q_std: float = 1.0
+    kv_std: float = 1.0
+    seed: int = 1000
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.d ** 0.5)
+
+    @property
+    def shape(self):
+        return (self.B, self.H, self.N, self.d)
+
+
+WORKLOADS = {
+    "c1": Workload("c1", 1, 1, 256, 64, (False,), ("fwd",), seed=1001),
+    "c2": Workload("c2", 8, 12, 1024, 64, (True,), ("fwd", "bwd"), seed=1002),
+    "c3": Workload("c3", 4, 12, 1028, 64, (False, True), ("fwd",), seed=1003),
+    "c4": Workload("c4", 2, 32, 8192, 128, (True,), ("fwd", "bwd"), seed=1004),
+    "c5": Workload("c5", 1, 16, 32768, 128, (True,), ("fwd",), q_std=4.0, seed=1005),
+}
+
+WORKLOAD_TITLES = {
+    "c1": "attention fwd B=1 H=1 N=256 d=64 non-causal",
+    "c2": "GPT-2-small-shaped attention fwd+bwd B=8 H=12 N=1024 d=64 causal",
+    "c3": "ragged-tile attention fwd B=4 H=12 N=1028 d=64 non-causal and causal",
+    "c4": "Llama-shaped attention fwd+bwd B=2 H=32 N=8192 d=128 causal",
+    "c5": "long-context attention fwd B=1 H=16 N=32768 d=128 causal, Q ~ N(0, 4^2)",
+}
+
+
+def make_inputs(B, H, N, d, seed, q_std=1.0, kv_std=1.0, do_std=1.0, with_do=True):
+    """Draw q, k, v (and dO) as bf16 CPU tensors of shape [B, H, N, d]."""
+    g = torch.Generator().manual_seed(int(seed))
+    shape = (B, H, N, d)
+    q = (torch.randn(shape, generator=g, dtype=torch.float32) * q_std).to(torch.bfloat16)
+    k = (torch.randn(shape, generator=g, dtype=torch.float32) * kv_std).to(torch.bfloat16)
+    v = (torch.randn(shape, generator=g, dtype=torch.float32) * kv_std).to(torch.bfloat16)
+    out = [q, k, v]
+    if with_do:
+        do = (torch.randn(shape, generator=g, dtype=torch.float32) * do_std).to(torch.bfloat16)
+        out.append(do)
+    return tuple(out)
+
+
+def workload_inputs(name: str, with_do=None):
+    w = WORKLOADS[name]
+    if with_do is None:
+        with_do = "bwd" in w.directions
+    return make_inputs(w.B, w.H, w.N, w.d, w.seed, q_std=w.q_std, kv_std=w.kv_std, with_do=with_do)
+
+
+def to_f64(t: torch.Tensor):
+    """bf16 tensor -> exact float64 numpy array (bf16 values are exact in fp64)."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
