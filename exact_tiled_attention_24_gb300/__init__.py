@@ -1,0 +1,182 @@
+"""Exact tiled attention (FlashAttention-style) for GB300 / sm_103a.
+
+Thin ctypes binding over ``libfa.so`` (C ABI in ``include/fa.h``): it only
+checks tensors, allocates outputs with torch on the current device, and
+passes raw pointers plus the current CUDA stream. Every step of the forward
+and backward runs in the library's CUDA kernels; there is no fallback path —
+if the library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "FAError",
+    "lib",
+    "lib_path",
+    "fwd",
+    "bwd",
+    "bwd_preprocess",
+    "bwd_main",
+    "bwd_dq_convert",
+    "bwd_workspace_bytes",
+    "last_device_error",
+    "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libfa.so")
+_lib = None
+
+FA_STATUS = {
+    0: "FA_OK",
+    1: "FA_ERR_INVALID_ARG",
+    2: "FA_ERR_UNSUPPORTED",
+    3: "FA_ERR_MISALIGNED",
+    4: "FA_ERR_CUDA",
+    5: "FA_ERR_TIMEOUT",
+    6: "FA_ERR_WORKSPACE",
+}
+
+EXPORTED_SYMBOLS = (
+    "fa_fwd",
+    "fa_bwd_workspace_bytes",
+    "fa_bwd",
+    "fa_bwd_preprocess",
+    "fa_bwd_main",
+    "fa_bwd_dq_convert",
+    "fa_last_device_error",
+    "fa_status_string",
+    "fa_version",
+)
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {FA_STATUS.get(status, status)}")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise FAError(-1, f"libfa.so not built at {_LIB_PATH}; run exact_tiled_attention_24_gb300.build.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd.restype = i
+        L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        L.fa_bwd_workspace_bytes.restype = sz
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
+        L.fa_bwd.restype = i
+        L.fa_bwd_preprocess.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.fa_bwd_preprocess.restype = i
+        L.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_main.restype = i
+        L.fa_bwd_dq_convert.argtypes = [vp, vp, i, i, i, i, f, vp]
+        L.fa_bwd_dq_convert.restype = i
+        L.fa_last_device_error.argtypes = [vp]
+        L.fa_last_device_error.restype = i
+        L.fa_status_string.argtypes = [i]
+        L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_version.argtypes = []
+        L.fa_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status, where):
+    if status != 0:
+        raise FAError(status, where)
+
+
+def _check_inputs(*ts):
+    ref = ts[0]
+    if ref.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if t.dtype != torch.bfloat16:
+            raise ValueError("tensors must be bfloat16")
+        if t.shape != ref.shape:
+            raise ValueError("q, k, v (and o, dO) must have the same shape")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if t.device != ref.device:
+            raise ValueError("tensors must be on one device")
+
+
+def _scale(d, scale):
+    return (1.0 / d ** 0.5) if scale is None else float(scale)
+
+
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None):
+    """o, lse = softmax(scale·q kᵀ [causal]) v and its per-row log-sum-exp."""
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, N, d,
+                        _scale(d, scale), int(bool(causal)), _stream(q.device)), "fa_fwd")
+    return o, lse_t
+
+
+def bwd_workspace_bytes(B, H, N, d) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None):
+    """dq, dk, dv of o = softmax(scale·q kᵀ [causal]) v for the output gradient do."""
+    _check_inputs(q, k, v, o, do)
+    B, H, N, d = q.shape
+    ws_bytes = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                        _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                        B, H, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)), "fa_bwd")
+    return dq, dk, dv
+
+
+def bwd_preprocess(o, do, Dvec, dq_acc):
+    B, H, N, d = o.shape
+    _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(Dvec), _ptr(dq_acc), B, H, N, d,
+                                   _stream(o.device)), "fa_bwd_preprocess")
+
+
+def bwd_main(q, k, v, do, lse, Dvec, dq_acc, dk, dv, causal=False, scale=None):
+    B, H, N, d = q.shape
+    _check(lib().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec),
+                             _ptr(dq_acc), _ptr(dk), _ptr(dv), B, H, N, d, _scale(d, scale),
+                             int(bool(causal)), _stream(q.device)), "fa_bwd_main")
+
+
+def bwd_dq_convert(dq_acc, dq, scale=None):
+    B, H, N, d = dq.shape
+    _check(lib().fa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, H, N, d, _scale(d, scale),
+                                   _stream(dq.device)), "fa_bwd_dq_convert")
+
+
+def last_device_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device error status."""
+    dev = torch.device("cuda") if device is None else device
+    return int(lib().fa_last_device_error(_stream(dev)))

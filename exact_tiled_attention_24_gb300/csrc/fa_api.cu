@@ -1,0 +1,156 @@
+// C ABI of the exact tiled attention library: argument checks, TMA
+// descriptor construction and kernel dispatch. Declarations and the full
+// contract are in include/fa.h.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/fa.h"
+#include "fa_common.h"
+#include "fa_tmap.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared size/scale checks. Returns FA_OK or the status to report.
+int check_sizes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  // Grid sizes and row indices are 32-bit: BH * N rows must fit in int32.
+  if (bh * N > INT_MAX) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int check_scale(float scale) {
+  if (!std::isfinite(scale) || scale <= 0.f) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+size_t dq_acc_bytes(int B, int H, int N, int d) {
+  return static_cast<size_t>(B) * H * N * d * sizeof(float);
+}
+size_t dvec_offset(int B, int H, int N, int d) {
+  return (dq_acc_bytes(B, H, N, d) + 255) & ~static_cast<size_t>(255);
+}
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_version(void) { return "0.1.0"; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if (!fa::make_tmap_bf16(&tq, q, BH, N, d, 128) || !fa::make_tmap_bf16(&tk, k, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tv, v, BH, N, d, 128) || !fa::make_tmap_bf16(&to, o, BH, N, d, 128))
+    return FA_ERR_CUDA;
+  return map_cuda(fa::launch_fwd(tq, tk, tv, to, lse, BH, N, d, scale, causal != 0,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d) != FA_OK) return 0;
+  return dvec_offset(B, H, N, d) + static_cast<size_t>(B) * H * N * sizeof(float);
+}
+
+int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H,
+                      int N, int d, void* stream) {
+  if (!o || !dO || !Dvec || !dq_acc) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(Dvec) || !aligned16(dq_acc))
+    return FA_ERR_MISALIGNED;
+  return map_cuda(fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o),
+                                            static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc,
+                                            B * H, N, d, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                const float* Dvec, float* dq_acc, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, void* stream) {
+  if (!q || !k || !v || !dO || !lse || !Dvec || !dq_acc || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(Dvec) || !aligned16(dq_acc) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (!fa::make_tmap_bf16(&tq, q, BH, N, d, 128) || !fa::make_tmap_bf16(&tk, k, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tv, v, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tdo, dO, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tdk, dk, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tdv, dv, BH, N, d, 128))
+    return FA_ERR_CUDA;
+  return map_cuda(fa::launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, d,
+                                      scale, causal != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale,
+                      void* stream) {
+  if (!dq_acc || !dq) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(dq_acc) || !aligned16(dq)) return FA_ERR_MISALIGNED;
+  return map_cuda(fa::launch_bwd_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), B * H, N, d,
+                                            scale, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+           int B, int H, int N, int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!workspace || ws_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_WORKSPACE;
+  if (!aligned16(workspace) || !aligned16(o) || !aligned16(dq)) return FA_ERR_MISALIGNED;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* Dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + dvec_offset(B, H, N, d));
+  st = fa_bwd_preprocess(o, dO, Dvec, dq_acc, B, H, N, d, stream);
+  if (st != FA_OK) return st;
+  st = fa_bwd_main(q, k, v, dO, lse, Dvec, dq_acc, dk, dv, B, H, N, d, scale, causal, stream);
+  if (st != FA_OK) return st;
+  return fa_bwd_dq_convert(dq_acc, dq, B, H, N, d, scale, stream);
+}
+
+int fa_last_device_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t ef = 0, eb = 0;
+  if (fa::read_and_clear_fwd_error(&ef, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::read_and_clear_bwd_error(&eb, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (ef || eb) return FA_ERR_TIMEOUT;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+/*
+ * fa.h — C ABI of the exact tiled attention library (libfa.so, sm_103a).
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale · Q Kᵀ) V        (row-wise softmax, optional causal mask)
+ *
+ * tile by tile with online softmax, so the N×N score matrix S and the
+ * probability matrix P never reach device memory, and its gradient by
+ * recomputing each P tile from the saved per-row log-sum-exp.
+ *
+ * Where the operation is defined:
+ *   - attention itself: dcwnkz.com GPU-tricks article (CS336 tricks),
+ *     FlashAttention section, "先简要回顾注意力机制" (scores are q·k dot
+ *     products; softmax makes each row sum to 1; output = weighted sum of V);
+ *   - tiling + online softmax + recomputation: CMU 10-423 L17–L18 notes
+ *     (quidproquo.cc), sections 前置二：online softmax and FlashAttention 本身;
+ *   - the six-score block-by-block rescaling walk-through: dcwnkz.com
+ *     article, FlashAttention section;
+ *   - the [B, heads, S, head_dim] layout and the causal mask:
+ *     "07-16 下午：分布式大模型训练与推理" (docs.bfyes.cn), section
+ *     自回归语言模型推理.
+ * The 1/sqrt(d) factor is not printed on those pages; callers pass `scale`.
+ *
+ * Conventions shared by every entry point
+ *   Tensors   q, k, v, o, dO, dq, dk, dv: bf16, contiguous, row-major
+ *             [B][H][N][d]; d must be 64 or 128. lse, D: fp32 [B][H][N].
+ *   Pointers  device pointers, each 16-byte aligned. The caller owns every
+ *             buffer; the library allocates no memory, never synchronises
+ *             the stream (except fa_last_device_error), and launches on
+ *             `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *             stream). Calls are asynchronous: a 0 return means the work was
+ *             enqueued.
+ *   Outputs   fully overwritten, never accumulated into.
+ *   Errors    arguments are checked before anything is launched; on error
+ *             nothing is launched and a non-zero fa_status is returned.
+ *             Device-side failures (a pipeline wait that exceeded its time
+ *             limit) are reported by fa_last_device_error.
+ *   Threads   entry points may be called from several host threads; each
+ *             call works on its own descriptors.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, B/H/N < 1, scale not finite or <= 0 */
+  FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or sizes past 2^31 elements */
+  FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch error) */
+  FA_ERR_TIMEOUT = 5,     /* device pipeline wait exceeded its limit */
+  FA_ERR_WORKSPACE = 6    /* workspace pointer null or smaller than required */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   q, k, v  [B][H][N][d] bf16 inputs.
+ *   o        [B][H][N][d] bf16 output: softmax(scale·q kᵀ [+ causal mask]) v.
+ *   lse      [B][H][N] fp32 output: per-row log-sum-exp of the scaled,
+ *            masked scores, natural log: lse_i = ln Σ_j exp(scale·q_i·k_j).
+ *   causal   non-zero: query i attends to keys j <= i (top-left aligned).
+ * Returns an fa_status.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
+ * [B][H][N][d] followed by the fp32 row vector D [B][H][N]
+ * (D_i = Σ_c dO_ic · O_ic). Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass: gradients of o = softmax(scale·q kᵀ) v with respect to q,
+ * k, v for the output gradient dO. P is rebuilt tile by tile from q, k and
+ * the forward's lse (recomputation), never read from memory.
+ *   q, k, v, o, dO  [B][H][N][d] bf16 (o and lse from fa_fwd on q, k, v).
+ *   dq, dk, dv      [B][H][N][d] bf16 outputs.
+ *   workspace       device buffer of at least fa_bwd_workspace_bytes(...)
+ *                   bytes, 16-byte aligned; contents on entry are ignored.
+ * Launches three kernels in order on `stream`: preprocess (D and zeroed dQ
+ * accumulator), the main dK/dV/dQ kernel, and the dQ conversion.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+           int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * The three backward stages as separate calls (fa_bwd runs all three).
+ * They share fa_bwd's argument rules; `Dvec` is fp32 [B][H][N] and `dq_acc`
+ * fp32 [B][H][N][d], both caller-owned device memory.
+ *   fa_bwd_preprocess : Dvec_i = Σ_c dO_ic·O_ic; dq_acc = 0.
+ *   fa_bwd_main       : dk, dv (bf16, final) and dq_acc += unscaled dS·K.
+ *   fa_bwd_dq_convert : dq = bf16(scale · dq_acc).
+ */
+int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H,
+                      int N, int d, void* stream);
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                const float* Dvec, float* dq_acc, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, void* stream);
+int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale,
+                      void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word set by
+ * any kernel of this library on the current device. Returns FA_OK,
+ * FA_ERR_TIMEOUT (a pipeline wait gave up; outputs of the calls since the
+ * last check are undefined) or FA_ERR_CUDA.
+ */
+int fa_last_device_error(void* stream);
+
+/* Human-readable name of an fa_status value (static string). */
+const char* fa_status_string(int status);
+
+/* Library version, e.g. "0.1.0". */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,105 @@
+"""Host-side checks of the C-ABI library: it loads, exports every entry point
+declared in include/fa.h, and rejects bad arguments before touching a GPU
+(no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_24_gb300 as fa
+from exact_tiled_attention_24_gb300 import build as fabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fabuild.build()
+    return fa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_binding_symbols():
+    assert declared_functions() == sorted(fa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert L.fa_status_string(0) == b"FA_OK"
+    assert L.fa_status_string(6) == b"FA_ERR_WORKSPACE"
+    assert L.fa_status_string(99) == b"FA_ERR_UNKNOWN"
+    assert re.match(rb"^\d+\.\d+\.\d+$", L.fa_version())
+
+
+FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: checks fail first
+MIS = ctypes.c_void_p(0x10002)
+NUL = ctypes.c_void_p(0)
+
+
+def fwd_call(L, q=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=16, d=64, scale=0.125, causal=0):
+    return L.fa_fwd(q, FAKE, FAKE, o, lse, B, H, N, d, scale, causal, NUL)
+
+
+def test_fwd_argument_errors(L):
+    assert fwd_call(L, q=NUL) == 1
+    assert fwd_call(L, lse=NUL) == 1
+    assert fwd_call(L, N=0) == 1
+    assert fwd_call(L, B=-1) == 1
+    assert fwd_call(L, scale=0.0) == 1
+    assert fwd_call(L, scale=float("nan")) == 1
+    assert fwd_call(L, scale=float("inf")) == 1
+    assert fwd_call(L, d=96) == 2
+    assert fwd_call(L, d=256) == 2
+    assert fwd_call(L, B=65536, H=65536, N=2) == 2  # more than 2^31 rows
+    assert fwd_call(L, q=MIS) == 3
+    assert fwd_call(L, o=MIS) == 3
+
+
+def test_bwd_workspace_size(L):
+    B, H, N, d = 2, 3, 100, 64
+    n = B * H * N
+    acc = n * d * 4
+    expect = ((acc + 255) // 256) * 256 + n * 4
+    assert L.fa_bwd_workspace_bytes(B, H, N, d) == expect
+    assert L.fa_bwd_workspace_bytes(B, H, 0, d) == 0
+    assert L.fa_bwd_workspace_bytes(B, H, N, 80) == 0
+
+
+def test_bwd_argument_errors(L):
+    ws = L.fa_bwd_workspace_bytes(1, 1, 16, 64)
+
+    def call(workspace=FAKE, ws_bytes=ws, dq=FAKE, d=64, scale=0.125):
+        return L.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dq, FAKE, FAKE, workspace, ws_bytes,
+                        1, 1, 16, d, scale, 1, NUL)
+
+    assert call(dq=NUL) == 1
+    assert call(scale=-1.0) == 1
+    assert call(d=32) == 2
+    assert call(workspace=NUL) == 6
+    assert call(ws_bytes=ws - 1) == 6
+    assert call(workspace=MIS) == 3
+    # stage entry points
+    assert L.fa_bwd_preprocess(FAKE, FAKE, FAKE, NUL, 1, 1, 16, 64, NUL) == 1
+    assert L.fa_bwd_main(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MIS, 1, 1, 16, 64,
+                         0.125, 0, NUL) == 3
+    assert L.fa_bwd_dq_convert(FAKE, FAKE, 1, 1, 16, 64, 0.0, NUL) == 1
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "exact_tiled_attention_24_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", text, flags=re.M), f
