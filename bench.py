@@ -1,0 +1,414 @@
+"""Throughput benchmark for exact tiled attention on GB300.
+
+One step = one forward + one backward pass (all stages of the hot path)
+over the Llama-shaped causal workload B=2 H=32 N=8192 d=128, bf16 inputs
+drawn from the seeded generator. Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload c4|c2|c5|c3|c1]
+
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(the path shards by independent heads; there is no data exchange), timing
+is max-over-ranks, and ``value`` is the whole-job FLOP rate.
+
+``--impl reference`` times the fp64 CPU oracle as it stands on the host
+cores, one bounded sample (one head's forward + backward) per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (fwd; fwd+bwd) on 1 GB300 and % of dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def flops(w, direction):
+    pairs = w.N * (w.N + 1) // 2 if True in w.causal else w.N * w.N
+    per_pair = {"fwd": 4 * w.d, "bwd": 10 * w.d}[direction]
+    return per_pair * w.B * w.H * pairs
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None, period_ms=100):
+        self.bus_id = bus_id
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = []
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.bus_id and parts[1].lower()[-12:] != self.bus_id.lower()[-12:]:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        smax = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        under_load = [s for s in sm if smax and s >= 0.3 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(under_load) if under_load else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
+
+
+# -------------------------------------------------------------- oracle leg
+
+def oracle_sample(w, q, k, v, do, heads):
+    """Time the fp64 oracle's forward + backward on the given heads.
+    Returns (seconds, algorithmic FLOPs of the sample)."""
+    from exact_tiled_attention_24_gb300.workloads import to_f64
+    from oracle import attention_bwd_head, attention_fwd_head
+    causal = True in w.causal
+    t0 = time.perf_counter()
+    for (b, h) in heads:
+        qq, kk, vv, dd = (to_f64(t[b, h]) for t in (q, k, v, do))
+        attention_fwd_head(qq, kk, vv, w.scale, causal)
+        if do is not None:
+            attention_bwd_head(qq, kk, vv, dd, w.scale, causal)
+    dt = time.perf_counter() - t0
+    per_head = (flops(w, "fwd") + (flops(w, "bwd") if do is not None else 0)) // (w.B * w.H)
+    return dt, per_head * len(heads)
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return None
+    from exact_tiled_attention_24_gb300.workloads import workload_inputs
+    q, k, v, *rest = workload_inputs(args.workload, with_do=True)
+    do = rest[0] if rest else None
+    heads = [(0, 0)]
+    oracle_sample(w, q, k, v, do, heads)  # one untimed call (BLAS thread start-up)
+    times, fl = [], 0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(w, q, k, v, do, heads)
+        times.append(dt)
+    total = sum(times)
+    value = fl * args.steps / total / 1e12
+    sample = f"one head (b=0,h=0) of {args.workload} forward+backward per step, fp64 NumPy oracle"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(args, w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def config_dict(args, w):
+    return {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} causal={True in w.causal} bf16",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True in w.causal,
+            "directions": list(w.directions),
+            "l2": "inputs larger than L2 (q,k,v,dO = %d MB vs 129 MB L2); no flush" % (
+                4 * w.B * w.H * w.N * w.d * 2 // 2**20),
+            "parallelism": f"replicas x{args.gpus} (independent heads per GPU, no collective)"}
+
+
+# -------------------------------------------------------------- GPU leg
+
+def traffic_for(kernel_key, sources):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    ent = data.get(kernel_key)
+    if not ent:
+        return None
+    h = hashlib.sha256()
+    for s in sources:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    if ent.get("source_sha256") != h.hexdigest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def run_ours(args, w, rank, world, dist):
+    import torch
+
+    import exact_tiled_attention_24_gb300 as fa
+    from exact_tiled_attention_24_gb300 import build as fabuild
+    from exact_tiled_attention_24_gb300.workloads import workload_inputs
+
+    fabuild.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    causal = True in w.causal
+    has_bwd = "bwd" in w.directions
+    q, k, v, *rest = workload_inputs(args.workload, with_do=has_bwd)
+    do = rest[0] if rest else None
+    host = [t.pin_memory() for t in (q, k, v) + ((do,) if do is not None else ())]
+    qg, kg, vg = (t.to(dev) for t in host[:3])
+    dog = host[3].to(dev) if has_bwd else None
+    B, H, N, d = w.shape
+    o = torch.empty_like(qg)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if has_bwd:
+        dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+        Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fwd(qg, kg, vg, causal=causal, out=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        if has_bwd:
+            fa.bwd_preprocess(o, dog, Dvec, acc)
+            if ev is not None:
+                ev[2].record(stream)
+            fa.bwd_main(qg, kg, vg, dog, lse, Dvec, acc, dk, dv, causal=causal)
+            if ev is not None:
+                ev[3].record(stream)
+            fa.bwd_dq_convert(acc, dq)
+            if ev is not None:
+                ev[4].record(stream)
+
+    launches_per_step = 4 if has_bwd else 1
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.last_device_error(dev) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        bus = None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(bus_id=bus) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if fa.last_device_error(dev) != 0:
+        raise RuntimeError("device error during the timed region")
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    if has_bwd:
+        pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+        conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+    F_fwd = flops(w, "fwd")
+    F_bwd = flops(w, "bwd") if has_bwd else 0
+    F_step = F_fwd + F_bwd
+    ms_per_step = elapsed_ms / args.steps
+    value = F_step * world / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+
+    # Dominant kernel: the one with the larger share of the step.
+    if has_bwd and main_ms >= fwd_ms:
+        dom, dom_ms, dom_flops = "bwd_main", main_ms, F_bwd
+        srcs = ["exact_tiled_attention_24_gb300/csrc/fa_bwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
+    else:
+        dom, dom_ms, dom_flops = "fwd", fwd_ms, F_fwd
+        srcs = ["exact_tiled_attention_24_gb300/csrc/fa_fwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} bf16_tflops_sustained (kernel timed inside a long step)",
+                "traffic": traffic_for(f"{dom}_{args.workload}", srcs)}
+
+    # End-to-end: host buffers in, results out, every step.
+    e2e_steps = max(3, args.steps // 4)
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse)]
+    if has_bwd:
+        outs += [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        qg.copy_(host[0], non_blocking=True)
+        kg.copy_(host[1], non_blocking=True)
+        vg.copy_(host[2], non_blocking=True)
+        if has_bwd:
+            dog.copy_(host[3], non_blocking=True)
+        step()
+        srcs_dev = [o, lse] + ([dq, dk, dv] if has_bwd else [])
+        for hst, dvc in zip(outs, srcs_dev):
+            hst.copy_(dvc, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = F_step * world / (e2e_ms * 1e-3) / 1e12
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(args, w),
+        "fwd_tflops": F_fwd / (fwd_ms * 1e-3) / 1e12,
+        "fwd_ms": fwd_ms,
+        "frac_of_peak": {"fwd_bwd": value / world / peak, "fwd": F_fwd / (fwd_ms * 1e-3) / 1e12 / peak,
+                         "peak_tflops": peak, "peak_source": peak_kind,
+                         "nominal_2250": value / world / 2250.0},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roofline,
+    }
+    if has_bwd:
+        result["bwd_ms"] = {"preprocess": pre_ms, "main": main_ms, "dq_convert": conv_ms}
+        result["bwd_tflops"] = F_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12
+        result["mfu_style_tflops"] = 3 * F_fwd * world / (ms_per_step * 1e-3) / 1e12
+    if rank == 0 and not args.no_cpu_baseline:
+        heads = [(0, 0)]
+        dt, fl = oracle_sample(w, q, k, v, do, heads)
+        reps = 1
+        while dt * reps < 10.0 and reps < 8:
+            dt2, _ = oracle_sample(w, q, k, v, do, [(0, reps % w.H)])
+            dt += dt2
+            reps += 1
+        result["cpu_baseline"] = {
+            "value": fl * reps / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"{reps} head(s) of {args.workload} forward{'+backward' if has_bwd else ''}, "
+                      f"fp64 NumPy oracle, {dt:.1f} s"}
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c4")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from exact_tiled_attention_24_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        res = run_reference(args, w, rank)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as tdist
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            tdist.init_process_group("nccl")
+            dist = tdist
+        res = run_ours(args, w, rank, world, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
