@@ -51,6 +51,7 @@ EXPORTED_SYMBOLS = (
     "fa_last_device_error",
     "fa_status_string",
     "fa_version",
+    "fa_bwd_noalloc",
 )
 
 

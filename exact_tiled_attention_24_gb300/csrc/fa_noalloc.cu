@@ -1,0 +1,97 @@
+// Allocation-free variant of the backward pass.
+//
+// fa_bwd needs device scratch (an fp32 dQ accumulator and the fp32 row
+// vector D) and expects the caller to provide it. Some callers cannot make
+// that allocation: a host application that owns all device memory through
+// its own fixed pool and gives plug-ins no allocator, a runtime that forbids
+// device allocation after start-up (fixed memory budget, real-time loop), or
+// code that must not take cudaMalloc's implicit device-wide synchronisation.
+// fa_bwd_noalloc serves them: its scratch is a file-scope __device__ array
+// of fixed size that lives in the library image, so the call itself
+// allocates nothing.
+//
+// Properties of that array (also stated in include/fa.h):
+//   * FA_BWD_NOALLOC_SCRATCH_BYTES bytes, held on every GPU that loads this
+//     library until the process exits;
+//   * shared by every call on a device: calls whose kernels overlap on the
+//     GPU (other streams, other host threads) race on it;
+//   * it keeps the last call's contents; the preprocess kernel re-zeroes the
+//     dQ accumulator and rewrites D on every call, so nothing stale is read.
+// The array's device address is looked up once per device (with that device
+// current) on the first call there.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_common.h"
+#include "fa_tmap.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device (host code
+// cannot use the array's name as an address). Returns nullptr on failure.
+void* scratch_on_current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  // Same size and scale rules as fa_bwd; the workspace query returns 0 for
+  // invalid sizes.
+  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+  if (need == 0) return (B < 1 || H < 1 || N < 1) ? FA_ERR_INVALID_ARG : FA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || scale <= 0.f) return FA_ERR_INVALID_ARG;
+  if (need > FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  void* scratch = scratch_on_current_device();
+  if (!scratch) return FA_ERR_CUDA;
+  float* dq_acc = static_cast<float*>(scratch);
+  const size_t acc_bytes = static_cast<size_t>(B) * H * N * d * sizeof(float);
+  float* Dvec = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                         ((acc_bytes + 255) & ~static_cast<size_t>(255)));
+  const int BH = B * H;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (!fa::make_tmap_bf16(&tq, q, BH, N, d, 128) || !fa::make_tmap_bf16(&tk, k, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tv, v, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tdo, dO, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tdk, dk, BH, N, d, 128) ||
+      !fa::make_tmap_bf16(&tdv, dv, BH, N, d, 128))
+    return FA_ERR_CUDA;
+  if (fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o),
+                                static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, BH, N, d,
+                                s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (fa::launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, d, scale,
+                          causal != 0, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (fa::launch_bwd_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), BH, N, d, scale, s) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}

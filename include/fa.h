@@ -108,6 +108,39 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, con
 int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale,
                       void* stream);
 
+/* Size in bytes of the static scratch area behind fa_bwd_noalloc (32 MiB). */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * fa_bwd for callers that cannot allocate device memory. The pages this
+ * library follows have no counterpart to this call; it exists for hosts
+ * that hand a plug-in no allocator (all device memory belongs to the host's
+ * own fixed pool), runtimes that forbid device allocation after start-up,
+ * and code that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation.
+ *
+ * Same arguments and results as fa_bwd, minus the workspace: the scratch
+ * (fp32 dQ accumulator and D vector, fa_bwd_workspace_bytes(B,H,N,d) bytes)
+ * is a file-scope __device__ array of FA_BWD_NOALLOC_SCRATCH_BYTES inside
+ * the library image, held on every GPU that loads the library until the
+ * process exits. The call itself allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *   - Problems whose scratch need exceeds FA_BWD_NOALLOC_SCRATCH_BYTES are
+ *     rejected with FA_ERR_WORKSPACE before anything is launched
+ *     (B*H*N*(d+1)*4 bytes, rounded up; e.g. B=8 H=12 N=1024 d=64 fits).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (a one-time set-up per device); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array. Calls whose kernels
+ *     overlap on the GPU (different streams or host threads without
+ *     ordering between them) race on it and give undefined results; order
+ *     such calls on one stream. The array keeps the last call's contents;
+ *     each call re-zeroes the accumulator and rewrites D before use.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the device error word set by
  * any kernel of this library on the current device. Returns FA_OK,

@@ -1,0 +1,73 @@
+"""fa_bwd_noalloc: the backward for callers that cannot allocate device
+memory (hosts whose device memory all belongs to their own fixed pool and
+that give a plug-in no allocator, runtimes that forbid allocation after
+start-up, code that cannot take cudaMalloc's implicit synchronisation).
+
+It takes no workspace: its scratch is a fixed-size array inside the library.
+These tests call it through the C ABI and compare it with fa_bwd, which
+takes a caller-provided workspace, on two calls in a row (the second call
+sees the array holding the first call's contents). This file is collected
+last so that a failure here does not hide the other tests.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import exact_tiled_attention_24_gb300 as fa
+from exact_tiled_attention_24_gb300 import build as fabuild
+from exact_tiled_attention_24_gb300.workloads import make_inputs
+from gpu_helpers import TOL_GRAD
+
+SCRATCH_BYTES = 32 * 1024 * 1024  # FA_BWD_NOALLOC_SCRATCH_BYTES in include/fa.h
+
+
+@pytest.fixture(scope="module")
+def L():
+    fabuild.build()
+    L = fa.lib()
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    L.fa_bwd_noalloc.restype = i
+    return L
+
+
+def test_noalloc_rejects_problems_larger_than_its_scratch(L):
+    """Checked on the host before any launch: B=2 H=32 N=8192 d=128 needs
+    about 270 MB of scratch, more than the 32 MiB array."""
+    fake = ctypes.c_void_p(0x10000)
+    assert fa.bwd_workspace_bytes(2, 32, 8192, 128) > SCRATCH_BYTES
+    st = L.fa_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                          2, 32, 8192, 128, 0.088, 1, ctypes.c_void_p(0))
+    assert st == 6  # FA_ERR_WORKSPACE
+    assert L.fa_bwd_noalloc(fake, fake, fake, fake, fake, ctypes.c_void_p(0), fake, fake, fake,
+                            1, 1, 64, 64, 0.125, 0, ctypes.c_void_p(0)) == 1
+
+
+def _call_noalloc(L, q, k, v, o, lse, do, causal):
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = L.fa_bwd_noalloc(p(q), p(k), p(v), p(o), p(do), p(lse), p(dq), p(dk), p(dv),
+                          B, H, N, d, 1.0 / d ** 0.5, int(causal),
+                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, st
+    return dq, dk, dv
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_fa_bwd_two_calls_in_a_row(L):
+    dev = torch.device("cuda")
+    cases = [((2, 3, 700, 128), True, 41), ((1, 4, 1028, 64), False, 42)]
+    for (B, H, N, d), causal, seed in cases:
+        q, k, v, do = (t.to(dev) for t in make_inputs(B, H, N, d, seed=seed))
+        o, lse = fa.fwd(q, k, v, causal=causal)
+        ref = fa.bwd(q, k, v, o, lse, do, causal=causal)
+        got = _call_noalloc(L, q, k, v, o, lse, do, causal)
+        torch.cuda.synchronize()
+        assert fa.last_device_error() == 0
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            err = (a.float() - b.float()).abs().max().item()
+            assert err <= TOL_GRAD, f"{name} (N={N}, d={d}): max-abs {err}"
+        # dK and dV involve no atomics: identical to the workspace path
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
