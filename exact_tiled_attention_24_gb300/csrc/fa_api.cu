@@ -10,7 +10,6 @@
 
 #include "../../include/fa.h"
 #include "fa_common.h"
-#include "fa_tmap.h"
 
 namespace {
 
@@ -67,12 +66,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
-  const int BH = B * H;
-  CUtensorMap tq, tk, tv, to;
-  if (!fa::make_tmap_bf16(&tq, q, BH, N, d, 128) || !fa::make_tmap_bf16(&tk, k, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tv, v, BH, N, d, 128) || !fa::make_tmap_bf16(&to, o, BH, N, d, 128))
-    return FA_ERR_CUDA;
-  return map_cuda(fa::launch_fwd(tq, tk, tv, to, lse, BH, N, d, scale, causal != 0,
+  return map_cuda(fa::launch_fwd(q, k, v, o, lse, B * H, N, d, scale, causal != 0,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -103,16 +97,8 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, con
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(Dvec) || !aligned16(dq_acc) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
-  const int BH = B * H;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!fa::make_tmap_bf16(&tq, q, BH, N, d, 128) || !fa::make_tmap_bf16(&tk, k, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tv, v, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tdo, dO, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tdk, dk, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tdv, dv, BH, N, d, 128))
-    return FA_ERR_CUDA;
-  return map_cuda(fa::launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, d,
-                                      scale, causal != 0, static_cast<cudaStream_t>(stream)));
+  return map_cuda(fa::launch_bwd_main(q, k, v, dO, dk, dv, lse, Dvec, dq_acc, B * H, N, d, scale,
+                                      causal != 0, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale,

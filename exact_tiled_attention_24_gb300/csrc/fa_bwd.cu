@@ -11,24 +11,30 @@
 //
 // Three kernels:
 //   preprocess  D = rowsum(dO ∘ O) and a zeroed fp32 dQ accumulator
-//   main        one CTA per (head, 128-key tile): K_j, V_j stay in shared
-//               memory, the CTA sweeps the 128-row query tiles (from the
-//               diagonal on when causal). Sᵀ = K Qᵢᵀ and dPᵀ = V dOᵢᵀ land in
-//               TMEM; the compute warps turn them into Pᵀ and dSᵀ (bf16,
-//               written back into TMEM and, for dS, into shared memory);
-//               dV += Pᵀ dOᵢ and dK += dSᵀ Qᵢ accumulate in TMEM for the
-//               whole sweep; dQᵢ = dS K goes through TMEM and is added to
-//               the fp32 accumulator with vector atomics.
+//   main        one CTA per (head, 128-key tile): K_j and V_j stay in shared
+//               memory while the CTA sweeps 64-row query tiles (from the
+//               diagonal on when causal). Per tile: Sᵀ = K Qᵢᵀ and
+//               dPᵀ = V dOᵢᵀ land in TMEM; the compute warps turn them into
+//               Pᵀ and dSᵀ (bf16, written back into TMEM, dSᵀ also into shared
+//               memory); dV += Pᵀ dOᵢ and dK += dSᵀ Qᵢ accumulate in TMEM over
+//               the whole sweep; dQᵢᵀ = Kᵀ dSᵢᵀ lands in TMEM with the head
+//               dimension on the lanes, so the dQ warps add it to the fp32
+//               accumulator with coalesced 128-byte reductions.
 //   dq_convert  dq = bf16(scale · dQ accumulator)
 //
-// Roles in the main kernel (192 threads): warp 0 TMA, warp 1 TMEM owner and
-// MMA issuer, warps 2..5 compute (one thread per key row = TMEM lane).
-// TMEM columns: dV 0.., dK 128.., S/P 256.., dP/dS 384..; dQᵢ reuses the S/P
-// columns once the dV MMA that read P has completed.
+// Roles in the main kernel (448 threads): warp 0 TMA, warp 1 TMEM owner and
+// MMA issuer, warps 2..9 compute (two warps per TMEM lane quarter, each
+// owning half of the 64 query columns; thread = key row), warps 10..13 read
+// dQᵀ out of TMEM. TMEM columns: dV 0.., dK 128.., two S buffers 256 and
+// 320 (Sᵀ_{i+1} is ready while tile i's gradient products run), dP 384,
+// dQᵀ 448. Products that reuse TMEM columns read by an earlier product are
+// issued after it on the same thread, and tcgen05 MMAs execute in issue
+// order.
 #include <cuda_bf16.h>
 
 #include "fa_common.h"
 #include "fa_ptx.cuh"
+#include "fa_tmap.h"
 
 namespace fa {
 
@@ -91,31 +97,41 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 
 // ------------------------------------------------------------ main kernel
 
-constexpr int BK = 128;  // keys per CTA
-constexpr int BQ = 128;  // query rows per tile
-constexpr int THREADS = 192;
-constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 384;
+constexpr int BK = 128;  // keys per CTA (M of the S, dP, dV, dK products)
+constexpr int BQ = 64;   // query rows per tile (N of S and dP, K of dV and dK)
+constexpr int QST = 3;   // Q / dO stages: tiles i, i+1 in use while i+2 lands
+constexpr int THREADS = 448;  // 14 warps
+// TMEM columns (fp32 words): accumulators for dV and dK, two S buffers, dP
+// and the dQᵀ tile.
+constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 384, COL_DQ = 448;
 
 template <int D>
 struct Smem {
   static constexpr int PANELS = D / 64;
-  static constexpr int STAGES = 2;
-  static constexpr int TILE = 128 * D * 2;
+  static constexpr int KV_TILE = BK * D * 2;       // one K or V tile
+  static constexpr int Q_TILE = BQ * D * 2;        // one Q or dO tile
+  static constexpr int KV_PANEL = BK * 128;        // 64 columns of a K/V tile
+  static constexpr int Q_PANEL = BQ * 128;         // 64 columns of a Q/dO tile
   static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = K_OFF + TILE;
-  static constexpr int Q_OFF = V_OFF + TILE;
-  static constexpr int DO_OFF = Q_OFF + STAGES * TILE;
-  static constexpr int DS_OFF = DO_OFF + STAGES * TILE;
-  static constexpr int DS_BYTES = BK * BQ * 2;
-  static constexpr int LSE_OFF = DS_OFF + DS_BYTES;   // 128 floats (log2 units)
-  static constexpr int DV_OFF = LSE_OFF + BQ * 4;     // 128 floats
-  static constexpr int BAR_OFF = DV_OFF + BQ * 4;
-  // kv_full, q_full[2], q_empty[2], sdp_full, ds_ready, mma2_done, dq_full, dq_free, final
-  static constexpr int NBARS = 1 + 2 * STAGES + 6;
+  static constexpr int V_OFF = K_OFF + KV_TILE;
+  static constexpr int Q_OFF = V_OFF + KV_TILE;
+  static constexpr int DO_OFF = Q_OFF + QST * Q_TILE;
+  static constexpr int DS_OFF = DO_OFF + QST * Q_TILE;
+  static constexpr int DS_TILE = BK * BQ * 2;      // dSᵀ tile: 128 key rows x 64 queries
+  static constexpr int STAT_OFF = DS_OFF + 2 * DS_TILE;
+  static constexpr int STAT_BYTES = 8 * 64 * 4;    // per compute warp: 32 lse + 32 D
+  static constexpr int BAR_OFF = STAT_OFF + STAT_BYTES;
+  // kv_full, q_full[QST], q_empty[QST], s_full[2], dp_full, ds_ready,
+  // dq_full, dq_free, dq_done[2], final
+  static constexpr int NBARS = 1 + 2 * QST + 2 + 1 + 1 + 1 + 1 + 2 + 1;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
-  static constexpr int ALLOC = BYTES + 1024;
+  static constexpr int ALLOC = (BYTES + 1024) > 118784 ? (BYTES + 1024) : 118784;
 };
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -134,42 +150,43 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sQ = smem + L::Q_OFF;
   uint8_t* sdO = smem + L::DO_OFF;
   uint8_t* sdS = smem + L::DS_OFF;
-  float* sLse = reinterpret_cast<float*>(smem + L::LSE_OFF);
-  float* sDv = reinterpret_cast<float*>(smem + L::DV_OFF);
+  float* sStat = reinterpret_cast<float*>(smem + L::STAT_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
-  uint64_t* q_empty = q_full + L::STAGES;
-  uint64_t* sdp_full = q_empty + L::STAGES;
-  uint64_t* ds_ready = sdp_full + 1;
-  uint64_t* mma2_done = ds_ready + 1;
-  uint64_t* dq_full = mma2_done + 1;
+  uint64_t* q_empty = q_full + QST;
+  uint64_t* s_full = q_empty + QST;
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* ds_ready = dp_full + 1;
+  uint64_t* dq_full = ds_ready + 1;
   uint64_t* dq_free = dq_full + 1;
-  uint64_t* final_bar = dq_free + 1;
+  uint64_t* dq_done = dq_free + 1;
+  uint64_t* final_bar = dq_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_kt = (N + BK - 1) / BK;
   const int n_qt = (N + BQ - 1) / BQ;
   const int kt = static_cast<int>(blockIdx.x) / BH;  // causal: heaviest key tile first
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int k0 = kt * BK;
-  const int qt_begin = CAUSAL ? kt : 0;  // BQ == BK
+  const int qt_begin = CAUSAL ? (k0 / BQ) : 0;  // first query tile with a visible pair
   const int n_it = n_qt - qt_begin;
-  (void)n_kt;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < L::STAGES; ++s) {
+    for (int s = 0; s < QST; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(ds_ready, 4);
-    mbar_init(mma2_done, 1);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_ready, 8);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);
+    mbar_init(&dq_done[0], 1);
+    mbar_init(&dq_done[1], 1);
     mbar_init(final_bar, 1);
     fence_mbar_init();
   }
@@ -190,241 +207,286 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
-      mbar_arrive_expect_tx(kv_full, 2 * L::TILE);
+      mbar_arrive_expect_tx(kv_full, 2 * L::KV_TILE);
       for (int p = 0; p < L::PANELS; ++p) {
-        tma_load_3d(sK + p * (BK * 128), &tk, kv_full, p * 64, k0, bh);
-        tma_load_3d(sV + p * (BK * 128), &tv, kv_full, p * 64, k0, bh);
+        tma_load_3d(sK + p * L::KV_PANEL, &tk, kv_full, p * 64, k0, bh);
+        tma_load_3d(sV + p * L::KV_PANEL, &tv, kv_full, p * 64, k0, bh);
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % L::STAGES;
-        if (!mbar_wait(&q_empty[s], ((it / L::STAGES) & 1) ^ 1, err)) break;
+        const int s = it % QST;
+        if (!mbar_wait(&q_empty[s], ((it / QST) & 1) ^ 1, err)) break;
         const int q0 = (qt_begin + it) * BQ;
-        mbar_arrive_expect_tx(&q_full[s], 2 * L::TILE);
+        mbar_arrive_expect_tx(&q_full[s], 2 * L::Q_TILE);
         for (int p = 0; p < L::PANELS; ++p) {
-          tma_load_3d(sQ + s * L::TILE + p * (BQ * 128), &tq, &q_full[s], p * 64, q0, bh);
-          tma_load_3d(sdO + s * L::TILE + p * (BQ * 128), &tdo, &q_full[s], p * 64, q0, bh);
+          tma_load_3d(sQ + s * L::Q_TILE + p * L::Q_PANEL, &tq, &q_full[s], p * 64, q0, bh);
+          tma_load_3d(sdO + s * L::Q_TILE + p * L::Q_PANEL, &tdo, &q_full[s], p * 64, q0, bh);
         }
         issued = it + 1;
       }
       mbar_wait(kv_full, 0, err);
-      for (int it = max(0, issued - L::STAGES); it < issued; ++it)
-        mbar_wait(&q_full[it % L::STAGES], (it / L::STAGES) & 1, err);
+      for (int it = max(0, issued - QST); it < issued; ++it)
+        mbar_wait(&q_full[it % QST], (it / QST) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(BK, BQ, false, false);  // Sᵀ, dPᵀ: 128x128, K = D
-      constexpr uint32_t id_g = idesc_bf16(BK, D, false, true);    // dV, dK: B MN-major
-      constexpr uint32_t id_q = idesc_bf16(BQ, D, true, true);     // dQ: A and B MN-major
-      bool ok = mbar_wait(kv_full, 0, err);
+      constexpr uint32_t id_s = idesc_bf16(BK, BQ, false, false);  // Sᵀ, dPᵀ: K-major both
+      constexpr uint32_t id_g = idesc_bf16(BK, D, false, true);    // dV, dK: A in TMEM, B MN-major
+      constexpr uint32_t id_q = idesc_bf16(128, BQ, true, true);   // dQᵀ = Kᵀ dSᵀ: both MN-major
       const uint32_t k_base = smem_u32(sK);
       const uint32_t v_base = smem_u32(sV);
-      const uint32_t ds_base = smem_u32(sdS);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it % L::STAGES;
-        const uint32_t q_base = smem_u32(sQ + s * L::TILE);
-        const uint32_t do_base = smem_u32(sdO + s * L::TILE);
-        ok = mbar_wait(&q_full[s], (it / L::STAGES) & 1, err);
-        if (ok && it > 0) ok = mbar_wait(dq_free, (it - 1) & 1, err);  // S/P columns free
-        if (!ok) break;
-        tc_fence_after();
+      // Sᵀ_i = K Q_iᵀ  (or dPᵀ_i = V dO_iᵀ): 128 keys x 64 queries, K = D.
+      auto issue_kq = [&](uint32_t a_base, uint32_t b_base, uint32_t d_col) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t poff = (ks / 4) * (128 * 128);
-          const uint32_t kin = (ks % 4) * 16;
-          mma_ss(tmem + COL_S, sdesc_kmajor(k_base + poff, kin), sdesc_kmajor(q_base + poff, kin),
-                 id_s, ks > 0);
+          mma_ss(tmem + d_col, sdesc_kmajor(a_base + (ks / 4) * L::KV_PANEL, (ks % 4) * 16),
+                 sdesc_kmajor(b_base + (ks / 4) * L::Q_PANEL, (ks % 4) * 16), id_s, ks > 0);
         }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t poff = (ks / 4) * (128 * 128);
-          const uint32_t kin = (ks % 4) * 16;
-          mma_ss(tmem + COL_DP, sdesc_kmajor(v_base + poff, kin),
-                 sdesc_kmajor(do_base + poff, kin), id_s, ks > 0);
+      };
+      bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(&q_full[0], 0, err);
+      if (ok) {
+        tc_fence_after();
+        issue_kq(k_base, smem_u32(sQ), COL_S);
+        tc_commit(&s_full[0]);
+        issue_kq(v_base, smem_u32(sdO), COL_DP);
+        tc_commit(dp_full);
+        if (n_it > 1) {
+          ok = mbar_wait(&q_full[1], 0, err);
+          if (ok) {
+            tc_fence_after();
+            issue_kq(k_base, smem_u32(sQ + L::Q_TILE), COL_S + BQ);
+            tc_commit(&s_full[1]);
+          }
         }
-        tc_commit(sdp_full);
-        ok = mbar_wait(ds_ready, it & 1, err);
+      }
+      for (int i = 0; i < n_it && ok; ++i) {
+        const int st = i % QST;
+        const int b = i & 1;
+        const uint32_t q_base = smem_u32(sQ + st * L::Q_TILE);
+        const uint32_t do_base = smem_u32(sdO + st * L::Q_TILE);
+        ok = mbar_wait(ds_ready, i & 1, err);
         if (!ok) break;
         tc_fence_after();
-        // dV += Pᵀ dOᵢ ; dK += dSᵀ Qᵢ   (A from TMEM, B MN-major in smem)
+        // dV += Pᵀ dO_i and dK += dSᵀ Q_i. Pᵀ / dSᵀ are bf16 in TMEM: the two
+        // 32-query halves sit at column offsets 0 and 32 of their buffers.
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks) {
-          mma_ts(tmem + COL_DV, tmem + COL_S + ks * 8, sdesc_mnmajor(do_base, ks * 16, BQ * 128),
-                 id_g, (it > 0 || ks > 0) ? 1u : 0u);
+          const uint32_t acol = (ks / 2) * 32 + (ks % 2) * 8;
+          mma_ts(tmem + COL_DV, tmem + COL_S + b * BQ + acol,
+                 sdesc_mnmajor(do_base, ks * 16, L::Q_PANEL), id_g, (i > 0 || ks > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks) {
-          mma_ts(tmem + COL_DK, tmem + COL_DP + ks * 8, sdesc_mnmajor(q_base, ks * 16, BQ * 128),
-                 id_g, (it > 0 || ks > 0) ? 1u : 0u);
+          const uint32_t acol = (ks / 2) * 32 + (ks % 2) * 8;
+          mma_ts(tmem + COL_DK, tmem + COL_DP + acol, sdesc_mnmajor(q_base, ks * 16, L::Q_PANEL),
+                 id_g, (i > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(mma2_done);
-        tc_commit(&q_empty[s]);
-        // dQᵢ overwrites the S/P columns: only after the dV MMA has read P.
-        ok = mbar_wait(mma2_done, it & 1, err);
-        if (!ok) break;
-        tc_fence_after();
+        // dQᵀ_i = Kᵀ dSᵀ_i (head dim on TMEM lanes; with D = 64 lanes 64..127
+        // hold unused products of the neighbouring V tile).
+        if (i > 0) {
+          ok = mbar_wait(dq_free, (i - 1) & 1, err);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t ds_base = smem_u32(sdS + b * L::DS_TILE);
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks) {
-          mma_ss(tmem + COL_S, sdesc_mnmajor(ds_base, ks * 16, BK * 128),
-                 sdesc_mnmajor(k_base, ks * 16, BK * 128), id_q, ks > 0);
+          mma_ss(tmem + COL_DQ, sdesc_mnmajor(k_base, ks * 16, L::KV_PANEL),
+                 sdesc_mnmajor(ds_base, ks * 16, L::KV_PANEL), id_q, ks > 0);
         }
         tc_commit(dq_full);
+        tc_commit(&dq_done[b]);
+        tc_commit(&q_empty[st]);
+        // Next tiles: dPᵀ_{i+1} reuses the dP columns after the dK product
+        // that read dSᵀ_i; Sᵀ_{i+2} reuses buffer b after the dV product that
+        // read Pᵀ_i (both issued above, executed in issue order).
+        if (i + 1 < n_it) {
+          issue_kq(v_base, smem_u32(sdO + ((i + 1) % QST) * L::Q_TILE), COL_DP);
+          tc_commit(dp_full);
+        }
+        if (i + 2 < n_it) {
+          const int s2 = (i + 2) % QST;
+          ok = mbar_wait(&q_full[s2], ((i + 2) / QST) & 1, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_kq(k_base, smem_u32(sQ + s2 * L::Q_TILE), COL_S + b * BQ);
+          tc_commit(&s_full[b]);
+        }
       }
       tc_commit(final_bar);
       mbar_wait(final_bar, 0, err);
     }
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ compute
+    // Warps 2..9: two warps per TMEM lane quarter, each owning 32 of the 64
+    // query columns of a tile. Thread = key row r (TMEM lane).
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // TMEM lane: key row (S, dP, dK, dV) or query row (dQ)
+    const int half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
     const int key = k0 + r;
     const bool key_ok = key < N;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float* lse_h = lse + static_cast<size_t>(bh) * N;
     const float* D_h = Dvec + static_cast<size_t>(bh) * N;
-    float* dq_h = dq_acc + static_cast<size_t>(bh) * N * D;
+    float* my_lse = sStat + (warp - 2) * 64;
+    float* my_D = my_lse + 32;
     constexpr float LOG2E = 1.4426950408889634f;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int qt = qt_begin + it;
-      const int q0 = qt * BQ;
-      // Stage this tile's lse (log2 units) and D; rows past N get lse=+inf (P = 0).
-      named_bar_sync(1, 128);
+    for (int i = 0; i < n_it; ++i) {
+      const int qt = qt_begin + i;
+      const int q0 = qt * BQ + half * 32;  // first query of this warp's half
+      const int b = i & 1;
       {
-        const int q = q0 + r;
-        sLse[r] = (q < N) ? lse_h[q] * LOG2E : INFINITY;
-        sDv[r] = (q < N) ? D_h[q] : 0.f;
+        const int q = q0 + lane;
+        my_lse[lane] = (q < N) ? lse_h[q] * LOG2E : INFINITY;
+        my_D[lane] = (q < N) ? D_h[q] : 0.f;
       }
-      named_bar_sync(1, 128);
-      ok = mbar_wait(sdp_full, it & 1, err);
+      __syncwarp();
+      ok = mbar_wait(&s_full[b], (i >> 1) & 1, err);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + COL_S;
-      const uint32_t dp_addr = tmem + lane_addr + COL_DP;
-      float p[BQ];
-      {
-        uint32_t raw[4][32];
-        tmem_ld32(s_addr + 0, raw[0]);
-        tmem_ld32(s_addr + 32, raw[1]);
-        tmem_ld32(s_addr + 64, raw[2]);
-        tmem_ld32(s_addr + 96, raw[3]);
-        tmem_ld_wait();
-        const bool diag = CAUSAL && (qt == kt);
+      const uint32_t s_addr = tmem + lane_addr + COL_S + b * BQ + half * 32;
+      const uint32_t dp_addr = tmem + lane_addr + COL_DP + half * 32;
+      uint32_t raw[32];
+      tmem_ld32(s_addr, raw);
+      tmem_ld_wait();
+      float p[32];
+      const bool need_mask = !key_ok || (CAUSAL && q0 < k0 + BK);
 #pragma unroll
-        for (int c = 0; c < BQ; ++c) {
-          float v = ex2(fmaf(__uint_as_float(raw[c / 32][c % 32]), scale_log2, -sLse[c]));
-          if (!key_ok || (diag && c < r)) v = 0.f;
-          p[c] = v;
-        }
+      for (int c = 0; c < 32; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(my_lse + c);
+        p[c + 0] = ex2(fmaf(__uint_as_float(raw[c + 0]), scale_log2, -l4.x));
+        p[c + 1] = ex2(fmaf(__uint_as_float(raw[c + 1]), scale_log2, -l4.y));
+        p[c + 2] = ex2(fmaf(__uint_as_float(raw[c + 2]), scale_log2, -l4.z));
+        p[c + 3] = ex2(fmaf(__uint_as_float(raw[c + 3]), scale_log2, -l4.w));
       }
-      {
-        uint32_t pk[16];
+      if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < BQ; c += 32) {
-#pragma unroll
-          for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(p[c + 2 * t], p[c + 2 * t + 1]);
-          tmem_st16(s_addr + c / 2, pk);
-        }
+        for (int c = 0; c < 32; ++c)
+          if (!key_ok || (CAUSAL && q0 + c < key)) p[c] = 0.f;
       }
-      // dSᵀ = Pᵀ ∘ (dPᵀ − D): into TMEM (for dK) and shared memory (for dQ).
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < BQ; c += 32) {
-        uint32_t raw[32];
-        tmem_ld32(dp_addr + c, raw);
-        tmem_ld_wait();
-        uint32_t pk[16];
+      for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(p[2 * t], p[2 * t + 1]);
+      tmem_st16(s_addr, pk);
+      // dSᵀ = Pᵀ ∘ (dPᵀ − D)
+      ok = mbar_wait(dp_full, i & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      tmem_ld32(dp_addr, raw);
+      tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float d0 = p[c + 2 * t] * (__uint_as_float(raw[2 * t]) - sDv[c + 2 * t]);
-          const float d1 = p[c + 2 * t + 1] * (__uint_as_float(raw[2 * t + 1]) - sDv[c + 2 * t + 1]);
-          pk[t] = pack_bf16x2(d0, d1);
-        }
-        tmem_st16(dp_addr + c / 2, pk);
+      for (int c = 0; c < 32; c += 4) {
+        const float4 d4 = *reinterpret_cast<const float4*>(my_D + c);
+        const float a0 = p[c + 0] * (__uint_as_float(raw[c + 0]) - d4.x);
+        const float a1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - d4.y);
+        const float a2 = p[c + 2] * (__uint_as_float(raw[c + 2]) - d4.z);
+        const float a3 = p[c + 3] * (__uint_as_float(raw[c + 3]) - d4.w);
+        pk[c / 2] = pack_bf16x2(a0, a1);
+        pk[c / 2 + 1] = pack_bf16x2(a2, a3);
+      }
+      tmem_st16(dp_addr, pk);
+      // dSᵀ into shared memory for the dQ product: row = key, 64 queries of
+      // 2 bytes = one 128-byte swizzled row; this half is chunks 4h..4h+3.
+      if (i >= 2) {
+        ok = mbar_wait(&dq_done[b], ((i - 2) >> 1) & 1, err);
+        if (!ok) break;
+      }
+      uint8_t* ds_row = sdS + b * L::DS_TILE + r * 128;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int col0 = c + ch * 8;
-          const int panel = col0 / 64;
-          const int chunk = (col0 % 64) / 8;
-          *reinterpret_cast<uint4*>(sdS + panel * (BK * 128) + r * 128 + ((chunk ^ (r & 7)) * 16)) =
-              make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        }
+      for (int ch = 0; ch < 4; ++ch) {
+        const int chunk = half * 4 + ch;
+        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
+            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
       }
       tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_ready);
-      // dQᵢ (unscaled) from TMEM, lane = query row, added into the accumulator.
-      ok = mbar_wait(dq_full, it & 1, err);
-      if (!ok) break;
-      tc_fence_after();
-      {
-        const int q = q0 + r;
-        float* dst = dq_h + static_cast<size_t>(q) * D;
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t raw[32];
-          tmem_ld32(s_addr + c, raw);
-          tmem_ld_wait();
-          if (q < N) {
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              atomicAdd(reinterpret_cast<float4*>(dst + c + 4 * t),
-                        make_float4(__uint_as_float(raw[4 * t]), __uint_as_float(raw[4 * t + 1]),
-                                    __uint_as_float(raw[4 * t + 2]),
-                                    __uint_as_float(raw[4 * t + 3])));
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
     }
     // -------------------------------------------------------------- epilogue
-    // The last dq_full implies every MMA of this CTA has completed; the Q/dO
-    // stage-0 buffers are free and serve as staging for dK and dV.
-    named_bar_sync(1, 128);
+    // The last dQ product's completion implies every MMA of this CTA is done;
+    // the Q and dO stage buffers then stage dK and dV for the TMA stores.
+    if (ok) ok = mbar_wait(&dq_done[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, err);
     if (ok) {
       tc_fence_after();
-      uint8_t* stage_dk = sQ;
-      uint8_t* stage_dv = sdO;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t a[32], b[32];
+      for (int cc = 0; cc < D / 2; cc += 32) {
+        const int c = half * (D / 2) + cc;
+        uint32_t a[32], bb[32];
         tmem_ld32(tmem + lane_addr + COL_DK + c, a);
-        tmem_ld32(tmem + lane_addr + COL_DV + c, b);
+        tmem_ld32(tmem + lane_addr + COL_DV + c, bb);
         tmem_ld_wait();
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int col0 = c + ch * 8;
           const int panel = col0 / 64;
           const int chunk = (col0 % 64) / 8;
-          const int off = panel * (BK * 128) + r * 128 + ((chunk ^ (r & 7)) * 16);
+          const int off = panel * L::KV_PANEL + r * 128 + ((chunk ^ (r & 7)) * 16);
           uint4 vk, vv;
           vk.x = pack_bf16x2(__uint_as_float(a[ch * 8 + 0]) * scale, __uint_as_float(a[ch * 8 + 1]) * scale);
           vk.y = pack_bf16x2(__uint_as_float(a[ch * 8 + 2]) * scale, __uint_as_float(a[ch * 8 + 3]) * scale);
           vk.z = pack_bf16x2(__uint_as_float(a[ch * 8 + 4]) * scale, __uint_as_float(a[ch * 8 + 5]) * scale);
           vk.w = pack_bf16x2(__uint_as_float(a[ch * 8 + 6]) * scale, __uint_as_float(a[ch * 8 + 7]) * scale);
-          vv.x = pack_bf16x2(__uint_as_float(b[ch * 8 + 0]), __uint_as_float(b[ch * 8 + 1]));
-          vv.y = pack_bf16x2(__uint_as_float(b[ch * 8 + 2]), __uint_as_float(b[ch * 8 + 3]));
-          vv.z = pack_bf16x2(__uint_as_float(b[ch * 8 + 4]), __uint_as_float(b[ch * 8 + 5]));
-          vv.w = pack_bf16x2(__uint_as_float(b[ch * 8 + 6]), __uint_as_float(b[ch * 8 + 7]));
-          *reinterpret_cast<uint4*>(stage_dk + off) = vk;
-          *reinterpret_cast<uint4*>(stage_dv + off) = vv;
+          vv.x = pack_bf16x2(__uint_as_float(bb[ch * 8 + 0]), __uint_as_float(bb[ch * 8 + 1]));
+          vv.y = pack_bf16x2(__uint_as_float(bb[ch * 8 + 2]), __uint_as_float(bb[ch * 8 + 3]));
+          vv.z = pack_bf16x2(__uint_as_float(bb[ch * 8 + 4]), __uint_as_float(bb[ch * 8 + 5]));
+          vv.w = pack_bf16x2(__uint_as_float(bb[ch * 8 + 6]), __uint_as_float(bb[ch * 8 + 7]));
+          *reinterpret_cast<uint4*>(sQ + off) = vk;
+          *reinterpret_cast<uint4*>(sdO + off) = vv;
         }
       }
       fence_async_smem();
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, 256);
     if (ok && warp == 2 && lane == 0) {
       for (int p = 0; p < L::PANELS; ++p) {
-        tma_store_3d(&tdk, sQ + p * (BK * 128), p * 64, k0, bh);
-        tma_store_3d(&tdv, sdO + p * (BK * 128), p * 64, k0, bh);
+        tma_store_3d(&tdk, sQ + p * L::KV_PANEL, p * 64, k0, bh);
+        tma_store_3d(&tdv, sdO + p * L::KV_PANEL, p * 64, k0, bh);
       }
       tma_store_commit();
       tma_store_wait_all();
+    }
+  } else {
+    // ------------------------------------------------------------ dQ warps
+    // Warps 10..13: read dQᵀ_i (lane = head-dim index, column = query) and
+    // add it to the fp32 accumulator; a warp writes 32 consecutive floats of
+    // one query row per instruction.
+    const int quarter = warp & 3;
+    const int dd = quarter * 32 + lane;
+    const uint32_t dq_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + COL_DQ;
+    float* acc_h = dq_acc + static_cast<size_t>(bh) * N * D;
+    const bool active = (D == 128) || (quarter < 2);
+    for (int i = 0; i < n_it; ++i) {
+      if (!mbar_wait(dq_full, i & 1, err)) break;
+      tc_fence_after();
+      if (active) {
+        const int q0 = (qt_begin + i) * BQ;
+        uint32_t v0[32], v1[32];
+        tmem_ld32(dq_addr, v0);
+        tmem_ld32(dq_addr + 32, v1);
+        tmem_ld_wait();
+        float* col = acc_h + static_cast<size_t>(q0) * D + dd;
+        const int nq = min(BQ, N - q0);
+        if (nq == BQ) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) red_add_f32(col + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
+#pragma unroll
+          for (int c = 0; c < 32; ++c) red_add_f32(col + static_cast<size_t>(c + 32) * D, __uint_as_float(v1[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < nq) red_add_f32(col + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c + 32 < nq) red_add_f32(col + static_cast<size_t>(c + 32) * D, __uint_as_float(v1[c]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
     }
   }
   tc_fence_before();
@@ -467,11 +529,15 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* d
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdk,
-                            const CUtensorMap& tdv, const float* lse, const float* Dvec,
+cudaError_t launch_bwd_main(const void* q, const void* k, const void* v, const void* dO,
+                            void* dk, void* dv, const float* lse, const float* Dvec,
                             float* dq_acc, int BH, int N, int d, float scale, bool causal,
                             cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (!make_tmap_bf16(&tq, q, BH, N, d, bwd::BQ) || !make_tmap_bf16(&tdo, dO, BH, N, d, bwd::BQ) ||
+      !make_tmap_bf16(&tk, k, BH, N, d, bwd::BK) || !make_tmap_bf16(&tv, v, BH, N, d, bwd::BK) ||
+      !make_tmap_bf16(&tdk, dk, BH, N, d, bwd::BK) || !make_tmap_bf16(&tdv, dv, BH, N, d, bwd::BK))
+    return cudaErrorInvalidValue;
   if (d == 64)
     return causal ? bwd::launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, scale, stream)
                   : bwd::launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, scale, stream);

@@ -9,18 +9,16 @@
 
 namespace fa {
 
-// Launch the forward kernel. Maps: q/k/v/o are [BH][N][d] bf16 with 64x128
-// boxes. lse is [BH][N] fp32. Returns the launch error.
-cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, float* lse, int BH, int N, int d, float scale,
-                       bool causal, cudaStream_t stream);
-
-// Backward stages (see fa_bwd.cu).
+// Kernel launchers. Pointers are device pointers to contiguous [BH][N][d]
+// bf16 tensors (lse, Dvec: [BH][N] fp32; dq_acc: [BH][N][d] fp32); each
+// launcher builds the TMA descriptors its kernel needs. Arguments are assumed
+// validated by the caller. Return the launch (or descriptor) error.
+cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
+                       int N, int d, float scale, bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dO, float* Dvec,
                                   float* dq_acc, int BH, int N, int d, cudaStream_t stream);
-cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdk,
-                            const CUtensorMap& tdv, const float* lse, const float* Dvec,
+cudaError_t launch_bwd_main(const void* q, const void* k, const void* v, const void* dO,
+                            void* dk, void* dv, const float* lse, const float* Dvec,
                             float* dq_acc, int BH, int N, int d, float scale, bool causal,
                             cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int BH, int N, int d,

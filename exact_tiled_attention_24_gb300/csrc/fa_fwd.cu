@@ -24,6 +24,7 @@
 
 #include "fa_common.h"
 #include "fa_ptx.cuh"
+#include "fa_tmap.h"
 
 namespace fa {
 
@@ -357,9 +358,12 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
 
 }  // namespace fwd
 
-cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, float* lse, int BH, int N, int d, float scale,
-                       bool causal, cudaStream_t stream) {
+cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
+                       int N, int d, float scale, bool causal, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_bf16(&tq, q, BH, N, d, fwd::BM) || !make_tmap_bf16(&tk, k, BH, N, d, fwd::BN) ||
+      !make_tmap_bf16(&tv, v, BH, N, d, fwd::BN) || !make_tmap_bf16(&to, o, BH, N, d, fwd::BM))
+    return cudaErrorInvalidValue;
   if (d == 64)
     return causal ? fwd::launch_t<64, true>(tq, tk, tv, to, lse, BH, N, scale, stream)
                   : fwd::launch_t<64, false>(tq, tk, tv, to, lse, BH, N, scale, stream);

@@ -27,7 +27,6 @@
 
 #include "../../include/fa.h"
 #include "fa_common.h"
-#include "fa_tmap.h"
 
 namespace {
 
@@ -76,19 +75,12 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                                          ((acc_bytes + 255) & ~static_cast<size_t>(255)));
   const int BH = B * H;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!fa::make_tmap_bf16(&tq, q, BH, N, d, 128) || !fa::make_tmap_bf16(&tk, k, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tv, v, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tdo, dO, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tdk, dk, BH, N, d, 128) ||
-      !fa::make_tmap_bf16(&tdv, dv, BH, N, d, 128))
-    return FA_ERR_CUDA;
   if (fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o),
                                 static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, BH, N, d,
                                 s) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (fa::launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, d, scale,
-                          causal != 0, s) != cudaSuccess)
+  if (fa::launch_bwd_main(q, k, v, dO, dk, dv, lse, Dvec, dq_acc, BH, N, d, scale, causal != 0,
+                          s) != cudaSuccess)
     return FA_ERR_CUDA;
   if (fa::launch_bwd_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), BH, N, d, scale, s) !=
       cudaSuccess)
