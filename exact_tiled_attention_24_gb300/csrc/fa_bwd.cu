@@ -18,8 +18,9 @@
 //               Pᵀ and dSᵀ (bf16, written back into TMEM, dSᵀ also into shared
 //               memory); dV += Pᵀ dOᵢ and dK += dSᵀ Qᵢ accumulate in TMEM over
 //               the whole sweep; dQᵢᵀ = Kᵀ dSᵢᵀ lands in TMEM with the head
-//               dimension on the lanes, so the dQ warps add it to the fp32
-//               accumulator with coalesced 128-byte reductions.
+//               dimension on the lanes; the dQ warps restage it as [query][d]
+//               rows in shared memory and add it to the fp32 accumulator with
+//               bulk reductions.
 //   dq_convert  dq = bf16(scale · dQ accumulator)
 //
 // Roles in the main kernel (448 threads): warp 0 TMA, warp 1 TMEM owner and
@@ -104,6 +105,7 @@ constexpr int THREADS = 448;  // 14 warps
 // TMEM columns (fp32 words): accumulators for dV and dK, two S buffers, dP
 // and the dQᵀ tile.
 constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 384, COL_DQ = 448;
+constexpr int HEAD_GROUP = 4;  // heads whose key tiles are scheduled together
 
 template <int D>
 struct Smem {
@@ -120,7 +122,9 @@ struct Smem {
   static constexpr int DS_TILE = BK * BQ * 2;      // dSᵀ tile: 128 key rows x 64 queries
   static constexpr int STAT_OFF = DS_OFF + 2 * DS_TILE;
   static constexpr int STAT_BYTES = 8 * 64 * 4;    // per compute warp: 32 lse + 32 D
-  static constexpr int BAR_OFF = STAT_OFF + STAT_BYTES;
+  static constexpr int DQ_STAGE_OFF = STAT_OFF + STAT_BYTES;
+  static constexpr int DQ_STAGE_BYTES = 32 * D * 4;  // 32 query rows of fp32 dQ
+  static constexpr int BAR_OFF = DQ_STAGE_OFF + DQ_STAGE_BYTES;
   // kv_full, q_full[QST], q_empty[QST], s_full[2], dp_full, ds_ready,
   // dq_full, dq_free, dq_done[2], final
   static constexpr int NBARS = 1 + 2 * QST + 2 + 1 + 1 + 1 + 1 + 2 + 1;
@@ -128,10 +132,6 @@ struct Smem {
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   static constexpr int ALLOC = (BYTES + 1024) > 118784 ? (BYTES + 1024) : 118784;
 };
-
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sdO = smem + L::DO_OFF;
   uint8_t* sdS = smem + L::DS_OFF;
   float* sStat = reinterpret_cast<float*>(smem + L::STAT_OFF);
+  float* sDqStage = reinterpret_cast<float*>(smem + L::DQ_STAGE_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
@@ -167,8 +168,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_qt = (N + BQ - 1) / BQ;
-  const int kt = static_cast<int>(blockIdx.x) / BH;  // causal: heaviest key tile first
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int n_kt = (N + BK - 1) / BK;
+  int kt, bh;  // causal: heaviest key tile (kt = 0) first within each head group
+  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_kt, HEAD_GROUP, &kt, &bh);
   const int k0 = kt * BK;
   const int qt_begin = CAUSAL ? (k0 / BQ) : 0;  // first query tile with a visible pair
   const int n_it = n_qt - qt_begin;
@@ -333,16 +335,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* my_D = my_lse + 32;
     constexpr float LOG2E = 1.4426950408889634f;
     bool ok = true;
+    // lse and D of the next tile are loaded one tile ahead (registers), so
+    // their global-memory latency is off the per-tile critical path.
+    float lse_nx = INFINITY, D_nx = 0.f;
+    {
+      const int q = qt_begin * BQ + half * 32 + lane;
+      if (q < N) {
+        lse_nx = lse_h[q] * LOG2E;
+        D_nx = D_h[q];
+      }
+    }
     for (int i = 0; i < n_it; ++i) {
       const int qt = qt_begin + i;
       const int q0 = qt * BQ + half * 32;  // first query of this warp's half
       const int b = i & 1;
-      {
-        const int q = q0 + lane;
-        my_lse[lane] = (q < N) ? lse_h[q] * LOG2E : INFINITY;
-        my_D[lane] = (q < N) ? D_h[q] : 0.f;
-      }
       __syncwarp();
+      my_lse[lane] = lse_nx;
+      my_D[lane] = D_nx;
+      __syncwarp();
+      {
+        const int q = q0 + BQ + lane;
+        lse_nx = INFINITY;
+        D_nx = 0.f;
+        if (i + 1 < n_it && q < N) {
+          lse_nx = lse_h[q] * LOG2E;
+          D_nx = D_h[q];
+        }
+      }
       ok = mbar_wait(&s_full[b], (i >> 1) & 1, err);
       if (!ok) break;
       tc_fence_after();
@@ -451,43 +470,50 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ warps
-    // Warps 10..13: read dQᵀ_i (lane = head-dim index, column = query) and
-    // add it to the fp32 accumulator; a warp writes 32 consecutive floats of
-    // one query row per instruction.
+    // Warps 10..13: read dQᵀ_i out of TMEM (lane = head-dim index, column =
+    // query), release the TMEM columns, then stage 32 query rows at a time in
+    // shared memory in the accumulator's [query][d] layout and add them to
+    // the fp32 accumulator with one bulk reduction (rows q0.. are contiguous).
     const int quarter = warp & 3;
     const int dd = quarter * 32 + lane;
     const uint32_t dq_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + COL_DQ;
     float* acc_h = dq_acc + static_cast<size_t>(bh) * N * D;
     const bool active = (D == 128) || (quarter < 2);
+    const bool issuer = (warp == 10 && lane == 0);
     for (int i = 0; i < n_it; ++i) {
-      if (!mbar_wait(dq_full, i & 1, err)) break;
+      const bool got = mbar_wait(dq_full, i & 1, err);
+      if (named_bar_any(2, 128, !got)) break;  // all four warps leave together
       tc_fence_after();
-      if (active) {
-        const int q0 = (qt_begin + i) * BQ;
-        uint32_t v0[32], v1[32];
-        tmem_ld32(dq_addr, v0);
-        tmem_ld32(dq_addr + 32, v1);
-        tmem_ld_wait();
-        float* col = acc_h + static_cast<size_t>(q0) * D + dd;
-        const int nq = min(BQ, N - q0);
-        if (nq == BQ) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) red_add_f32(col + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
-#pragma unroll
-          for (int c = 0; c < 32; ++c) red_add_f32(col + static_cast<size_t>(c + 32) * D, __uint_as_float(v1[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < nq) red_add_f32(col + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c + 32 < nq) red_add_f32(col + static_cast<size_t>(c + 32) * D, __uint_as_float(v1[c]));
-        }
-      }
+      uint32_t v[2][32];
+      tmem_ld32(dq_addr, v[0]);
+      tmem_ld32(dq_addr + 32, v[1]);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free);
+      const int q0 = (qt_begin + i) * BQ;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rows = min(32, N - (q0 + 32 * h));
+        // the previous bulk reduction must have finished reading the stage
+        if (issuer) bulk_wait_read_all();
+        named_bar_sync(2, 128);
+        if (rows > 0) {
+          if (active) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sDqStage[c * D + dd] = __uint_as_float(v[h][c]);
+          }
+          fence_async_smem();
+        }
+        named_bar_sync(2, 128);
+        if (issuer && rows > 0) {
+          bulk_reduce_add_f32(acc_h + static_cast<size_t>(q0 + 32 * h) * D, sDqStage,
+                              static_cast<uint32_t>(rows) * D * 4u);
+          tma_store_commit();
+        }
+      }
     }
+    if (issuer) tma_store_wait_all();
   }
   tc_fence_before();
   __syncthreads();

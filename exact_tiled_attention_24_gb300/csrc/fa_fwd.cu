@@ -37,6 +37,7 @@ constexpr int BN = 128;       // keys per tile
 constexpr int NSB = 3;        // S buffers in TMEM
 constexpr int THREADS = 192;  // 6 warps
 constexpr uint32_t O_COL = 384;
+constexpr int HEAD_GROUP = 8;
 
 template <int D>
 struct Smem {
@@ -84,10 +85,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Heaviest (causal) query tiles first, all heads interleaved.
+  // Heads in groups of HEAD_GROUP (their K/V stay in L2 while the group
+  // runs); within a group the heaviest (causal) query tiles go first.
   const int n_qt = (N + BM - 1) / BM;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  int t, bh;
+  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_qt, HEAD_GROUP, &t, &bh);
+  const int qt = n_qt - 1 - t;
   const int q0 = qt * BM;
   const int n_kt_all = (N + BN - 1) / BN;
   const int n_kt = CAUSAL ? min(n_kt_all, qt + 1) : n_kt_all;

@@ -120,14 +120,52 @@ __device__ __forceinline__ void tma_store_commit() {
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Bulk (non-tensor) reduction: global[dst .. dst+bytes) += shared[src ..]
+// element-wise in fp32. Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+      "r"(smem_u32(src)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async (TMA/MMA) proxy.
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// CTA order shared by the tile kernels: heads are taken in groups of
+// `group` so that the CTAs resident at one time touch few heads (their K/V or
+// Q/dO stay in L2); inside a group, tile index `t` runs slowest.
+__device__ __forceinline__ void grouped_tile_order(int x, int BH, int n_tiles, int group,
+                                                   int* t, int* bh) {
+  const int gi = x / (group * n_tiles);
+  const int base = gi * group;
+  const int g = min(group, BH - base);
+  const int idx = x - gi * group * n_tiles;
+  *t = idx / g;
+  *bh = base + idx % g;
+}
+
 // Named barrier over a subset of warps (id 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads, so
+// a group of warps takes the same branch (e.g. all leave a loop together).
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+      " bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
 }
 
 // ------------------------------------------------------------ tcgen05
