@@ -232,7 +232,6 @@ def run_ours(args, w, rank, world, dist):
     if has_bwd:
         dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
         Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
@@ -242,13 +241,13 @@ def run_ours(args, w, rank, world, dist):
         if ev is not None:
             ev[1].record(stream)
         if has_bwd:
-            fa.bwd_preprocess(o, dog, Dvec, acc)
+            fa.bwd_preprocess(o, dog, Dvec)
             if ev is not None:
                 ev[2].record(stream)
-            fa.bwd_main(qg, kg, vg, dog, lse, Dvec, acc, dk, dv, causal=causal)
+            fa.bwd_dkdv(qg, kg, vg, dog, lse, Dvec, dk, dv, causal=causal)
             if ev is not None:
                 ev[3].record(stream)
-            fa.bwd_dq_convert(acc, dq)
+            fa.bwd_dq(qg, kg, vg, dog, lse, Dvec, dq, causal=causal)
             if ev is not None:
                 ev[4].record(stream)
 
@@ -289,8 +288,8 @@ def run_ours(args, w, rank, world, dist):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     if has_bwd:
         pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-        main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-        conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+        dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+        dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
     F_fwd = flops(w, "fwd")
     F_bwd = flops(w, "bwd") if has_bwd else 0
     F_step = F_fwd + F_bwd
@@ -298,13 +297,15 @@ def run_ours(args, w, rank, world, dist):
     value = F_step * world / (ms_per_step * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
 
-    # Dominant kernel: the one with the larger share of the step.
-    if has_bwd and main_ms >= fwd_ms:
-        dom, dom_ms, dom_flops = "bwd_main", main_ms, F_bwd
-        srcs = ["exact_tiled_attention_24_gb300/csrc/fa_bwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
-    else:
-        dom, dom_ms, dom_flops = "fwd", fwd_ms, F_fwd
-        srcs = ["exact_tiled_attention_24_gb300/csrc/fa_fwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
+    # Dominant kernel: the one with the largest share of the step. Its
+    # algorithmic FLOPs: fwd 4·d per pair (QKᵀ, PV); dkdv 8·d (Sᵀ, dPᵀ, dV,
+    # dK); dq 6·d (S, dP, dQ) — the dq sweep recomputes S and dP.
+    bsrc = ["exact_tiled_attention_24_gb300/csrc/fa_bwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
+    fsrc = ["exact_tiled_attention_24_gb300/csrc/fa_fwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
+    cands = [("fwd", fwd_ms, F_fwd, fsrc)]
+    if has_bwd:
+        cands += [("bwd_dkdv", dkdv_ms, F_fwd * 2, bsrc), ("bwd_dq", dq_ms, F_fwd * 3 // 2, bsrc)]
+    dom, dom_ms, dom_flops, srcs = max(cands, key=lambda c: c[1])
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
@@ -359,8 +360,8 @@ def run_ours(args, w, rank, world, dist):
         "roofline": roofline,
     }
     if has_bwd:
-        result["bwd_ms"] = {"preprocess": pre_ms, "main": main_ms, "dq_convert": conv_ms}
-        result["bwd_tflops"] = F_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12
+        result["bwd_ms"] = {"preprocess": pre_ms, "dkdv": dkdv_ms, "dq": dq_ms}
+        result["bwd_tflops"] = F_bwd / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12
         result["mfu_style_tflops"] = 3 * F_fwd * world / (ms_per_step * 1e-3) / 1e12
     if rank == 0 and not args.no_cpu_baseline:
         heads = [(0, 0)]

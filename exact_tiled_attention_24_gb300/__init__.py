@@ -20,8 +20,8 @@ __all__ = [
     "fwd",
     "bwd",
     "bwd_preprocess",
-    "bwd_main",
-    "bwd_dq_convert",
+    "bwd_dkdv",
+    "bwd_dq",
     "bwd_workspace_bytes",
     "last_device_error",
     "EXPORTED_SYMBOLS",
@@ -46,8 +46,8 @@ EXPORTED_SYMBOLS = (
     "fa_bwd_workspace_bytes",
     "fa_bwd",
     "fa_bwd_preprocess",
-    "fa_bwd_main",
-    "fa_bwd_dq_convert",
+    "fa_bwd_dkdv",
+    "fa_bwd_dq",
     "fa_last_device_error",
     "fa_status_string",
     "fa_version",
@@ -79,12 +79,14 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = i
-        L.fa_bwd_preprocess.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
         L.fa_bwd_preprocess.restype = i
-        L.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
-        L.fa_bwd_main.restype = i
-        L.fa_bwd_dq_convert.argtypes = [vp, vp, i, i, i, i, f, vp]
-        L.fa_bwd_dq_convert.restype = i
+        L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_dkdv.restype = i
+        L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_dq.restype = i
+        L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_noalloc.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
         L.fa_status_string.argtypes = [i]
@@ -158,23 +160,27 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None):
     return dq, dk, dv
 
 
-def bwd_preprocess(o, do, Dvec, dq_acc):
+def bwd_preprocess(o, do, Dvec):
+    """Dvec = rowsum(do * o) (fp32 [B, H, N])."""
     B, H, N, d = o.shape
-    _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(Dvec), _ptr(dq_acc), B, H, N, d,
-                                   _stream(o.device)), "fa_bwd_preprocess")
+    _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(Dvec), B, H, N, d, _stream(o.device)),
+           "fa_bwd_preprocess")
 
 
-def bwd_main(q, k, v, do, lse, Dvec, dq_acc, dk, dv, causal=False, scale=None):
+def bwd_dkdv(q, k, v, do, lse, Dvec, dk, dv, causal=False, scale=None):
+    """dk, dv (bf16, written in place) from the recomputed P and dS."""
     B, H, N, d = q.shape
-    _check(lib().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec),
-                             _ptr(dq_acc), _ptr(dk), _ptr(dv), B, H, N, d, _scale(d, scale),
-                             int(bool(causal)), _stream(q.device)), "fa_bwd_main")
+    _check(lib().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dk),
+                             _ptr(dv), B, H, N, d, _scale(d, scale), int(bool(causal)),
+                             _stream(q.device)), "fa_bwd_dkdv")
 
 
-def bwd_dq_convert(dq_acc, dq, scale=None):
-    B, H, N, d = dq.shape
-    _check(lib().fa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, H, N, d, _scale(d, scale),
-                                   _stream(dq.device)), "fa_bwd_dq_convert")
+def bwd_dq(q, k, v, do, lse, Dvec, dq, causal=False, scale=None):
+    """dq (bf16, written in place) from the recomputed dS."""
+    B, H, N, d = q.shape
+    _check(lib().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dq),
+                           B, H, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)),
+           "fa_bwd_dq")
 
 
 def last_device_error(device=None) -> int:

@@ -30,13 +30,6 @@ int check_scale(float scale) {
   return FA_OK;
 }
 
-size_t dq_acc_bytes(int B, int H, int N, int d) {
-  return static_cast<size_t>(B) * H * N * d * sizeof(float);
-}
-size_t dvec_offset(int B, int H, int N, int d) {
-  return (dq_acc_bytes(B, H, N, d) + 255) & ~static_cast<size_t>(255);
-}
-
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
@@ -72,44 +65,46 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d) != FA_OK) return 0;
-  return dvec_offset(B, H, N, d) + static_cast<size_t>(B) * H * N * sizeof(float);
+  return static_cast<size_t>(B) * H * N * sizeof(float);
 }
 
-int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H,
-                      int N, int d, void* stream) {
-  if (!o || !dO || !Dvec || !dq_acc) return FA_ERR_INVALID_ARG;
+int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, int H, int N, int d,
+                      void* stream) {
+  if (!o || !dO || !Dvec) return FA_ERR_INVALID_ARG;
   int st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
-  if (!aligned16(o) || !aligned16(dO) || !aligned16(Dvec) || !aligned16(dq_acc))
-    return FA_ERR_MISALIGNED;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(Dvec)) return FA_ERR_MISALIGNED;
   return map_cuda(fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o),
-                                            static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc,
-                                            B * H, N, d, static_cast<cudaStream_t>(stream)));
+                                            static_cast<const __nv_bfloat16*>(dO), Dvec, B * H, N,
+                                            d, static_cast<cudaStream_t>(stream)));
 }
 
-int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                const float* Dvec, float* dq_acc, void* dk, void* dv, int B, int H, int N, int d,
-                float scale, int causal, void* stream) {
-  if (!q || !k || !v || !dO || !lse || !Dvec || !dq_acc || !dk || !dv) return FA_ERR_INVALID_ARG;
+int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                const float* Dvec, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                int causal, void* stream) {
+  if (!q || !k || !v || !dO || !lse || !Dvec || !dk || !dv) return FA_ERR_INVALID_ARG;
   int st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
-      !aligned16(Dvec) || !aligned16(dq_acc) || !aligned16(dk) || !aligned16(dv))
+      !aligned16(Dvec) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
-  return map_cuda(fa::launch_bwd_main(q, k, v, dO, dk, dv, lse, Dvec, dq_acc, B * H, N, d, scale,
+  return map_cuda(fa::launch_bwd_dkdv(q, k, v, dO, dk, dv, lse, Dvec, B * H, N, d, scale,
                                       causal != 0, static_cast<cudaStream_t>(stream)));
 }
 
-int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale,
-                      void* stream) {
-  if (!dq_acc || !dq) return FA_ERR_INVALID_ARG;
+int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+              const float* Dvec, void* dq, int B, int H, int N, int d, float scale, int causal,
+              void* stream) {
+  if (!q || !k || !v || !dO || !lse || !Dvec || !dq) return FA_ERR_INVALID_ARG;
   int st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
-  if (!aligned16(dq_acc) || !aligned16(dq)) return FA_ERR_MISALIGNED;
-  return map_cuda(fa::launch_bwd_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), B * H, N, d,
-                                            scale, static_cast<cudaStream_t>(stream)));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(Dvec) || !aligned16(dq))
+    return FA_ERR_MISALIGNED;
+  return map_cuda(fa::launch_bwd_dq(q, k, v, dO, dq, lse, Dvec, B * H, N, d, scale, causal != 0,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
@@ -121,13 +116,12 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!workspace || ws_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_WORKSPACE;
   if (!aligned16(workspace) || !aligned16(o) || !aligned16(dq)) return FA_ERR_MISALIGNED;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* Dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + dvec_offset(B, H, N, d));
-  st = fa_bwd_preprocess(o, dO, Dvec, dq_acc, B, H, N, d, stream);
+  float* Dvec = static_cast<float*>(workspace);
+  st = fa_bwd_preprocess(o, dO, Dvec, B, H, N, d, stream);
   if (st != FA_OK) return st;
-  st = fa_bwd_main(q, k, v, dO, lse, Dvec, dq_acc, dk, dv, B, H, N, d, scale, causal, stream);
+  st = fa_bwd_dkdv(q, k, v, dO, lse, Dvec, dk, dv, B, H, N, d, scale, causal, stream);
   if (st != FA_OK) return st;
-  return fa_bwd_dq_convert(dq_acc, dq, B, H, N, d, scale, stream);
+  return fa_bwd_dq(q, k, v, dO, lse, Dvec, dq, B, H, N, d, scale, causal, stream);
 }
 
 int fa_last_device_error(void* stream) {

@@ -10,27 +10,28 @@
 //     dQ = scale · dS K,  dK = scale · dSᵀ Q.
 //
 // Three kernels:
-//   preprocess  D = rowsum(dO ∘ O) and a zeroed fp32 dQ accumulator
-//   main        one CTA per (head, 128-key tile): K_j and V_j stay in shared
-//               memory while the CTA sweeps 64-row query tiles (from the
-//               diagonal on when causal). Per tile: Sᵀ = K Qᵢᵀ and
+//   preprocess  D = rowsum(dO ∘ O).
+//   dkdv        one CTA per (head, 128-key tile): K_j and V_j stay in shared
+//               memory while the CTA sweeps 128-row query tiles (from the
+//               diagonal on when causal). Per tile, Sᵀ = K Qᵢᵀ and
 //               dPᵀ = V dOᵢᵀ land in TMEM; the compute warps turn them into
-//               Pᵀ and dSᵀ (bf16, written back into TMEM, dSᵀ also into shared
-//               memory); dV += Pᵀ dOᵢ and dK += dSᵀ Qᵢ accumulate in TMEM over
-//               the whole sweep; dQᵢᵀ = Kᵀ dSᵢᵀ lands in TMEM with the head
-//               dimension on the lanes; the dQ warps restage it as [query][d]
-//               rows in shared memory and add it to the fp32 accumulator with
-//               bulk reductions.
-//   dq_convert  dq = bf16(scale · dQ accumulator)
+//               Pᵀ and dSᵀ (bf16, written back into TMEM) and
+//               dV += Pᵀ dOᵢ, dK += dSᵀ Qᵢ accumulate in TMEM over the sweep.
+//   dq          one CTA per (head, 128-row query tile): Q_i and dO_i are
+//               copied into TMEM once and serve as the A operand while the
+//               CTA sweeps 128-key tiles; S = Qᵢ Kⱼᵀ and dP = dOᵢ Vⱼᵀ are
+//               recomputed, dS (bf16, TMEM) feeds dQ += dS Kⱼ, and dQ is
+//               written once, in bf16, at the end.
+// Computing dQ in its own sweep recomputes S and dP (seven products per
+// query/key tile pair instead of five) but needs no cross-CTA reduction: on
+// this part the fp32 reduction traffic of a dQ accumulated from every key
+// tile (4 bytes x N x d per key tile) is bounded by L2 reduction throughput
+// well below what the tensor cores need.
 //
-// Roles in the main kernel (448 threads): warp 0 TMA, warp 1 TMEM owner and
-// MMA issuer, warps 2..9 compute (two warps per TMEM lane quarter, each
-// owning half of the 64 query columns; thread = key row), warps 10..13 read
-// dQᵀ out of TMEM. TMEM columns: dV 0.., dK 128.., two S buffers 256 and
-// 320 (Sᵀ_{i+1} is ready while tile i's gradient products run), dP 384,
-// dQᵀ 448. Products that reuse TMEM columns read by an earlier product are
-// issued after it on the same thread, and tcgen05 MMAs execute in issue
-// order.
+// Both sweep kernels use 128-wide tiles so that every product has N = 128
+// (an MMA with N = 64 takes nearly as long as one with N = 128 on this part).
+// Products that overwrite TMEM columns another product reads are issued
+// after it on the same thread; tcgen05 MMAs execute in issue order.
 #include <cuda_bf16.h>
 
 #include "fa_common.h"
@@ -49,7 +50,6 @@ template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          float* __restrict__ Dvec,
-                                                         float* __restrict__ dq_acc,
                                                          long long rows) {
   constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 bytes) each
   constexpr int RPB = 256 / TPR;
@@ -69,111 +69,130 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
       acc = fmaf(fa2.x, fb2.x, acc);
       acc = fmaf(fa2.y, fb2.y, acc);
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + off);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int w = TPR / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
   if (row < rows && part == 0) Dvec[row] = acc;
 }
 
-// ------------------------------------------------------------ dq convert
+// ------------------------------------------------------- shared helpers
 
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
-                                                         __nv_bfloat16* __restrict__ dq,
-                                                         long long n8, float scale) {
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    uint4 out;
-    out.x = pack_bf16x2(a.x * scale, a.y * scale);
-    out.y = pack_bf16x2(a.z * scale, a.w * scale);
-    out.z = pack_bf16x2(b.x * scale, b.y * scale);
-    out.w = pack_bf16x2(b.z * scale, b.w * scale);
-    reinterpret_cast<uint4*>(dq)[i] = out;
+constexpr int TILE = 128;       // rows of every K, V, Q, dO tile
+constexpr int HEAD_GROUP = 4;   // heads whose tiles are scheduled together
+constexpr int SWEEP_THREADS = 320;  // 10 warps: TMA, MMA, 8 compute
+
+template <int D>
+struct Tiles {
+  static constexpr int PANELS = D / 64;
+  static constexpr int BYTES = TILE * D * 2;  // one 128-row tile
+  static constexpr int PANEL = TILE * 128;    // 64 columns x 128 rows
+};
+
+// Stage columns [c_begin, c_begin + NCOLS) of a [128 rows] fp32 tile held in
+// TMEM (lane = row) as bf16, times `mul`, into a swizzled shared-memory tile
+// (panels of 64 columns) ready for a TMA store.
+template <int NCOLS>
+__device__ __forceinline__ void stage_tmem_rows_bf16(uint32_t taddr, uint8_t* dst, int r, int c_begin,
+                                                     float mul) {
+#pragma unroll
+  for (int cc = 0; cc < NCOLS; cc += 32) {
+    const int c = c_begin + cc;
+    uint32_t a[32];
+    tmem_ld32(taddr + c, a);
+    tmem_ld_wait();
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      const int col0 = c + ch * 8;
+      const int panel = col0 / 64;
+      const int chunk = (col0 % 64) / 8;
+      uint4 v;
+      v.x = pack_bf16x2(__uint_as_float(a[ch * 8 + 0]) * mul, __uint_as_float(a[ch * 8 + 1]) * mul);
+      v.y = pack_bf16x2(__uint_as_float(a[ch * 8 + 2]) * mul, __uint_as_float(a[ch * 8 + 3]) * mul);
+      v.z = pack_bf16x2(__uint_as_float(a[ch * 8 + 4]) * mul, __uint_as_float(a[ch * 8 + 5]) * mul);
+      v.w = pack_bf16x2(__uint_as_float(a[ch * 8 + 6]) * mul, __uint_as_float(a[ch * 8 + 7]) * mul);
+      *reinterpret_cast<uint4*>(dst + panel * (TILE * 128) + r * 128 + ((chunk ^ (r & 7)) * 16)) = v;
+    }
   }
 }
 
-// ------------------------------------------------------------ main kernel
+// Aligned shared-memory base; returns nullptr (and records an error) when
+// the 1024-byte aligned layout does not fit the allocation.
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw, int bytes, int alloc) {
+  const uint32_t pad = (1024u - (smem_u32(raw) & 1023u)) & 1023u;
+  if (pad + static_cast<uint32_t>(bytes) > static_cast<uint32_t>(alloc)) {
+    if (threadIdx.x == 0) atomicExch(&g_bwd_err, DEV_TIMEOUT);
+    return nullptr;
+  }
+  return raw + pad;
+}
 
-constexpr int BK = 128;  // keys per CTA (M of the S, dP, dV, dK products)
-constexpr int BQ = 64;   // query rows per tile (N of S and dP, K of dV and dK)
-constexpr int QST = 3;   // Q / dO stages: tiles i, i+1 in use while i+2 lands
-constexpr int THREADS = 448;  // 14 warps
-// TMEM columns (fp32 words): accumulators for dV and dK, two S buffers, dP
-// and the dQᵀ tile.
-constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 384, COL_DQ = 448;
-constexpr int HEAD_GROUP = 4;  // heads whose key tiles are scheduled together
+constexpr int kMaxDynSmem = 232448;  // 227 KB per-block opt-in limit
+
+// Dynamic allocation: the layout plus alignment slack, at least 116 KB so
+// only one CTA (and one 512-column TMEM allocation) is resident per SM.
+constexpr int alloc_for(int bytes) {
+  return (bytes + 1024 <= kMaxDynSmem) ? (bytes + 1024 < 118784 ? 118784 : bytes + 1024) : kMaxDynSmem;
+}
+
+// ------------------------------------------------------------ dK, dV sweep
+
+constexpr uint32_t KV_COL_DV = 0, KV_COL_DK = 128, KV_COL_S = 256, KV_COL_DP = 384;
 
 template <int D>
-struct Smem {
-  static constexpr int PANELS = D / 64;
-  static constexpr int KV_TILE = BK * D * 2;       // one K or V tile
-  static constexpr int Q_TILE = BQ * D * 2;        // one Q or dO tile
-  static constexpr int KV_PANEL = BK * 128;        // 64 columns of a K/V tile
-  static constexpr int Q_PANEL = BQ * 128;         // 64 columns of a Q/dO tile
+struct DkdvSmem {
+  using T = Tiles<D>;
+  static constexpr int QST = 2;
   static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = K_OFF + KV_TILE;
-  static constexpr int Q_OFF = V_OFF + KV_TILE;
-  static constexpr int DO_OFF = Q_OFF + QST * Q_TILE;
-  static constexpr int DS_OFF = DO_OFF + QST * Q_TILE;
-  static constexpr int DS_TILE = BK * BQ * 2;      // dSᵀ tile: 128 key rows x 64 queries
-  static constexpr int STAT_OFF = DS_OFF + 2 * DS_TILE;
-  static constexpr int STAT_BYTES = 8 * 64 * 4;    // per compute warp: 32 lse + 32 D
-  static constexpr int DQ_STAGE_OFF = STAT_OFF + STAT_BYTES;
-  static constexpr int DQ_STAGE_BYTES = 32 * D * 4;  // 32 query rows of fp32 dQ
-  static constexpr int BAR_OFF = DQ_STAGE_OFF + DQ_STAGE_BYTES;
-  // kv_full, q_full[QST], q_empty[QST], s_full[2], dp_full, ds_ready,
-  // dq_full, dq_free, dq_done[2], final
-  static constexpr int NBARS = 1 + 2 * QST + 2 + 1 + 1 + 1 + 1 + 2 + 1;
+  static constexpr int V_OFF = K_OFF + T::BYTES;
+  static constexpr int Q_OFF = V_OFF + T::BYTES;
+  static constexpr int DO_OFF = Q_OFF + QST * T::BYTES;
+  static constexpr int STAT_OFF = DO_OFF + QST * T::BYTES;
+  static constexpr int STAT_BYTES = 2 * 2 * TILE * 4;  // two buffers of (lse, D) per query
+  static constexpr int BAR_OFF = STAT_OFF + STAT_BYTES;
+  // kv_full, q_full[2], q_empty[2], s_full, dp_full, ds_ready, final
+  static constexpr int NBARS = 1 + 2 * QST + 4;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
-  static constexpr int ALLOC = (BYTES + 1024) > 118784 ? (BYTES + 1024) : 118784;
+  static constexpr int ALLOC = alloc_for(BYTES);
+  static_assert(BYTES <= kMaxDynSmem, "shared memory layout exceeds the per-block limit");
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(THREADS, 1)
-    bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+__global__ void __launch_bounds__(SWEEP_THREADS, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tdk,
                     const __grid_constant__ CUtensorMap tdv, const float* __restrict__ lse,
-                    const float* __restrict__ Dvec, float* __restrict__ dq_acc, int BH, int N,
-                    float scale, float scale_log2) {
-  using L = Smem<D>;
+                    const float* __restrict__ Dvec, int BH, int N, float scale, float scale_log2) {
+  using L = DkdvSmem<D>;
+  using T = Tiles<D>;
+  constexpr int QST = L::QST;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = aligned_smem(smem_raw, L::BYTES, L::ALLOC);
+  if (smem == nullptr) return;
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
   uint8_t* sQ = smem + L::Q_OFF;
   uint8_t* sdO = smem + L::DO_OFF;
-  uint8_t* sdS = smem + L::DS_OFF;
   float* sStat = reinterpret_cast<float*>(smem + L::STAT_OFF);
-  float* sDqStage = reinterpret_cast<float*>(smem + L::DQ_STAGE_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + QST;
   uint64_t* s_full = q_empty + QST;
-  uint64_t* dp_full = s_full + 2;
+  uint64_t* dp_full = s_full + 1;
   uint64_t* ds_ready = dp_full + 1;
-  uint64_t* dq_full = ds_ready + 1;
-  uint64_t* dq_free = dq_full + 1;
-  uint64_t* dq_done = dq_free + 1;
-  uint64_t* final_bar = dq_done + 2;
+  uint64_t* final_bar = ds_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_qt = (N + BQ - 1) / BQ;
-  const int n_kt = (N + BK - 1) / BK;
+  const int n_t = (N + TILE - 1) / TILE;
   int kt, bh;  // causal: heaviest key tile (kt = 0) first within each head group
-  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_kt, HEAD_GROUP, &kt, &bh);
-  const int k0 = kt * BK;
-  const int qt_begin = CAUSAL ? (k0 / BQ) : 0;  // first query tile with a visible pair
-  const int n_it = n_qt - qt_begin;
+  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_t, HEAD_GROUP, &kt, &bh);
+  const int k0 = kt * TILE;
+  const int qt_begin = CAUSAL ? kt : 0;  // first query tile with a visible pair
+  const int n_it = n_t - qt_begin;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -181,14 +200,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
+    mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(ds_ready, 8);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 4);
-    mbar_init(&dq_done[0], 1);
-    mbar_init(&dq_done[1], 1);
     mbar_init(final_bar, 1);
     fence_mbar_init();
   }
@@ -209,20 +223,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
-      mbar_arrive_expect_tx(kv_full, 2 * L::KV_TILE);
-      for (int p = 0; p < L::PANELS; ++p) {
-        tma_load_3d(sK + p * L::KV_PANEL, &tk, kv_full, p * 64, k0, bh);
-        tma_load_3d(sV + p * L::KV_PANEL, &tv, kv_full, p * 64, k0, bh);
+      mbar_arrive_expect_tx(kv_full, 2 * T::BYTES);
+      for (int p = 0; p < T::PANELS; ++p) {
+        tma_load_3d(sK + p * T::PANEL, &tk, kv_full, p * 64, k0, bh);
+        tma_load_3d(sV + p * T::PANEL, &tv, kv_full, p * 64, k0, bh);
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % QST;
         if (!mbar_wait(&q_empty[s], ((it / QST) & 1) ^ 1, err)) break;
-        const int q0 = (qt_begin + it) * BQ;
-        mbar_arrive_expect_tx(&q_full[s], 2 * L::Q_TILE);
-        for (int p = 0; p < L::PANELS; ++p) {
-          tma_load_3d(sQ + s * L::Q_TILE + p * L::Q_PANEL, &tq, &q_full[s], p * 64, q0, bh);
-          tma_load_3d(sdO + s * L::Q_TILE + p * L::Q_PANEL, &tdo, &q_full[s], p * 64, q0, bh);
+        const int q0 = (qt_begin + it) * TILE;
+        mbar_arrive_expect_tx(&q_full[s], 2 * T::BYTES);
+        for (int p = 0; p < T::PANELS; ++p) {
+          tma_load_3d(sQ + s * T::BYTES + p * T::PANEL, &tq, &q_full[s], p * 64, q0, bh);
+          tma_load_3d(sdO + s * T::BYTES + p * T::PANEL, &tdo, &q_full[s], p * 64, q0, bh);
         }
         issued = it + 1;
       }
@@ -233,287 +247,468 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(BK, BQ, false, false);  // Sᵀ, dPᵀ: K-major both
-      constexpr uint32_t id_g = idesc_bf16(BK, D, false, true);    // dV, dK: A in TMEM, B MN-major
-      constexpr uint32_t id_q = idesc_bf16(128, BQ, true, true);   // dQᵀ = Kᵀ dSᵀ: both MN-major
+      constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // Sᵀ, dPᵀ: K-major both
+      constexpr uint32_t id_g = idesc_bf16(TILE, D, false, true);      // dV, dK: A TMEM, B MN-major
       const uint32_t k_base = smem_u32(sK);
       const uint32_t v_base = smem_u32(sV);
-      // Sᵀ_i = K Q_iᵀ  (or dPᵀ_i = V dO_iᵀ): 128 keys x 64 queries, K = D.
+      // Sᵀ = K Qᵀ (or dPᵀ = V dOᵀ): 128 keys x 128 queries, K = D.
       auto issue_kq = [&](uint32_t a_base, uint32_t b_base, uint32_t d_col) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          mma_ss(tmem + d_col, sdesc_kmajor(a_base + (ks / 4) * L::KV_PANEL, (ks % 4) * 16),
-                 sdesc_kmajor(b_base + (ks / 4) * L::Q_PANEL, (ks % 4) * 16), id_s, ks > 0);
+          const uint32_t poff = (ks / 4) * T::PANEL;
+          mma_ss(tmem + d_col, sdesc_kmajor(a_base + poff, (ks % 4) * 16),
+                 sdesc_kmajor(b_base + poff, (ks % 4) * 16), id_s, ks > 0);
         }
       };
       bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(&q_full[0], 0, err);
       if (ok) {
         tc_fence_after();
-        issue_kq(k_base, smem_u32(sQ), COL_S);
-        tc_commit(&s_full[0]);
-        issue_kq(v_base, smem_u32(sdO), COL_DP);
+        issue_kq(k_base, smem_u32(sQ), KV_COL_S);
+        tc_commit(s_full);
+        issue_kq(v_base, smem_u32(sdO), KV_COL_DP);
         tc_commit(dp_full);
-        if (n_it > 1) {
-          ok = mbar_wait(&q_full[1], 0, err);
-          if (ok) {
-            tc_fence_after();
-            issue_kq(k_base, smem_u32(sQ + L::Q_TILE), COL_S + BQ);
-            tc_commit(&s_full[1]);
-          }
-        }
       }
       for (int i = 0; i < n_it && ok; ++i) {
         const int st = i % QST;
-        const int b = i & 1;
-        const uint32_t q_base = smem_u32(sQ + st * L::Q_TILE);
-        const uint32_t do_base = smem_u32(sdO + st * L::Q_TILE);
+        const uint32_t q_base = smem_u32(sQ + st * T::BYTES);
+        const uint32_t do_base = smem_u32(sdO + st * T::BYTES);
         ok = mbar_wait(ds_ready, i & 1, err);
         if (!ok) break;
         tc_fence_after();
-        // dV += Pᵀ dO_i and dK += dSᵀ Q_i. Pᵀ / dSᵀ are bf16 in TMEM: the two
-        // 32-query halves sit at column offsets 0 and 32 of their buffers.
+        // dV += Pᵀ dO_i: A = Pᵀ in TMEM (bf16; the 64-query halves at column
+        // offsets 0 and 64 of the S columns), B = dO_i MN-major.
 #pragma unroll
-        for (int ks = 0; ks < BQ / 16; ++ks) {
-          const uint32_t acol = (ks / 2) * 32 + (ks % 2) * 8;
-          mma_ts(tmem + COL_DV, tmem + COL_S + b * BQ + acol,
-                 sdesc_mnmajor(do_base, ks * 16, L::Q_PANEL), id_g, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int ks = 0; ks < BQ / 16; ++ks) {
-          const uint32_t acol = (ks / 2) * 32 + (ks % 2) * 8;
-          mma_ts(tmem + COL_DK, tmem + COL_DP + acol, sdesc_mnmajor(q_base, ks * 16, L::Q_PANEL),
+        for (int ks = 0; ks < TILE / 16; ++ks) {
+          const uint32_t acol = (ks / 4) * 64 + (ks % 4) * 8;
+          mma_ts(tmem + KV_COL_DV, tmem + KV_COL_S + acol, sdesc_mnmajor(do_base, ks * 16, T::PANEL),
                  id_g, (i > 0 || ks > 0) ? 1u : 0u);
         }
-        // dQᵀ_i = Kᵀ dSᵀ_i (head dim on TMEM lanes; with D = 64 lanes 64..127
-        // hold unused products of the neighbouring V tile).
-        if (i > 0) {
-          ok = mbar_wait(dq_free, (i - 1) & 1, err);
+        // Sᵀ_{i+1} overwrites the S columns after the dV product read Pᵀ_i.
+        const bool more = i + 1 < n_it;
+        const int s1 = (i + 1) % QST;
+        if (more) {
+          ok = mbar_wait(&q_full[s1], ((i + 1) / QST) & 1, err);
           if (!ok) break;
           tc_fence_after();
+          issue_kq(k_base, smem_u32(sQ + s1 * T::BYTES), KV_COL_S);
+          tc_commit(s_full);
         }
-        const uint32_t ds_base = smem_u32(sdS + b * L::DS_TILE);
+        // dK += dSᵀ Q_i: A = dSᵀ in TMEM (dP columns), B = Q_i MN-major.
 #pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks) {
-          mma_ss(tmem + COL_DQ, sdesc_mnmajor(k_base, ks * 16, L::KV_PANEL),
-                 sdesc_mnmajor(ds_base, ks * 16, L::KV_PANEL), id_q, ks > 0);
+        for (int ks = 0; ks < TILE / 16; ++ks) {
+          const uint32_t acol = (ks / 4) * 64 + (ks % 4) * 8;
+          mma_ts(tmem + KV_COL_DK, tmem + KV_COL_DP + acol, sdesc_mnmajor(q_base, ks * 16, T::PANEL),
+                 id_g, (i > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(dq_full);
-        tc_commit(&dq_done[b]);
-        tc_commit(&q_empty[st]);
-        // Next tiles: dPᵀ_{i+1} reuses the dP columns after the dK product
-        // that read dSᵀ_i; Sᵀ_{i+2} reuses buffer b after the dV product that
-        // read Pᵀ_i (both issued above, executed in issue order).
-        if (i + 1 < n_it) {
-          issue_kq(v_base, smem_u32(sdO + ((i + 1) % QST) * L::Q_TILE), COL_DP);
+        tc_commit(&q_empty[st]);  // Q_i and dO_i have no further readers
+        // dPᵀ_{i+1} overwrites the dP columns after the dK product read dSᵀ_i.
+        if (more) {
+          issue_kq(v_base, smem_u32(sdO + s1 * T::BYTES), KV_COL_DP);
           tc_commit(dp_full);
-        }
-        if (i + 2 < n_it) {
-          const int s2 = (i + 2) % QST;
-          ok = mbar_wait(&q_full[s2], ((i + 2) / QST) & 1, err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_kq(k_base, smem_u32(sQ + s2 * L::Q_TILE), COL_S + b * BQ);
-          tc_commit(&s_full[b]);
         }
       }
       tc_commit(final_bar);
       mbar_wait(final_bar, 0, err);
     }
-  } else if (warp < 10) {
+  } else {
     // ------------------------------------------------------------ compute
-    // Warps 2..9: two warps per TMEM lane quarter, each owning 32 of the 64
-    // query columns of a tile. Thread = key row r (TMEM lane).
+    // Warps 2..9: two warps per TMEM lane quarter; warp half h owns query
+    // columns 64h..64h+63 of each tile. Thread = key row r (TMEM lane).
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
+    const int ct = threadIdx.x - 64;  // 0..255 over the compute warps
     const int r = quarter * 32 + lane;
     const int key = k0 + r;
     const bool key_ok = key < N;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float* lse_h = lse + static_cast<size_t>(bh) * N;
     const float* D_h = Dvec + static_cast<size_t>(bh) * N;
-    float* my_lse = sStat + (warp - 2) * 64;
-    float* my_D = my_lse + 32;
     constexpr float LOG2E = 1.4426950408889634f;
+    // Per-tile (lse, D) of the 128 queries, double-buffered in shared memory:
+    // compute thread ct fills entry ct % 128 of lse (ct < 128) or of D.
+    auto load_stat = [&](int tile) -> float {
+      const int q = (qt_begin + tile) * TILE + (ct & 127);
+      if (ct < 128) return (tile < n_it && q < N) ? lse_h[q] * LOG2E : INFINITY;
+      return (tile < n_it && q < N) ? D_h[q] : 0.f;
+    };
+    sStat[ct] = load_stat(0);  // buffer 0: lse[0..127], D[128..255]
+    float stat_nx = load_stat(1);
+    named_bar_sync(1, 256);
     bool ok = true;
-    // lse and D of the next tile are loaded one tile ahead (registers), so
-    // their global-memory latency is off the per-tile critical path.
-    float lse_nx = INFINITY, D_nx = 0.f;
-    {
-      const int q = qt_begin * BQ + half * 32 + lane;
-      if (q < N) {
-        lse_nx = lse_h[q] * LOG2E;
-        D_nx = D_h[q];
-      }
-    }
     for (int i = 0; i < n_it; ++i) {
-      const int qt = qt_begin + i;
-      const int q0 = qt * BQ + half * 32;  // first query of this warp's half
-      const int b = i & 1;
-      __syncwarp();
-      my_lse[lane] = lse_nx;
-      my_D[lane] = D_nx;
-      __syncwarp();
-      {
-        const int q = q0 + BQ + lane;
-        lse_nx = INFINITY;
-        D_nx = 0.f;
-        if (i + 1 < n_it && q < N) {
-          lse_nx = lse_h[q] * LOG2E;
-          D_nx = D_h[q];
-        }
-      }
-      ok = mbar_wait(&s_full[b], (i >> 1) & 1, err);
+      const int q0 = (qt_begin + i) * TILE + half * 64;  // first query of this warp's half
+      const float* s_lse = sStat + (i & 1) * 256 + half * 64;
+      const float* s_D = s_lse + 128;
+      ok = mbar_wait(s_full, i & 1, err);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + COL_S + b * BQ + half * 32;
-      const uint32_t dp_addr = tmem + lane_addr + COL_DP + half * 32;
-      uint32_t raw[32];
-      tmem_ld32(s_addr, raw);
-      tmem_ld_wait();
-      float p[32];
-      const bool need_mask = !key_ok || (CAUSAL && q0 < k0 + BK);
+      const uint32_t s_addr = tmem + lane_addr + KV_COL_S + half * 64;
+      const uint32_t dp_addr = tmem + lane_addr + KV_COL_DP + half * 64;
+      float p[64];
+      const bool masked = !key_ok || (CAUSAL && q0 < k0 + TILE);
 #pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(my_lse + c);
-        p[c + 0] = ex2(fmaf(__uint_as_float(raw[c + 0]), scale_log2, -l4.x));
-        p[c + 1] = ex2(fmaf(__uint_as_float(raw[c + 1]), scale_log2, -l4.y));
-        p[c + 2] = ex2(fmaf(__uint_as_float(raw[c + 2]), scale_log2, -l4.z));
-        p[c + 3] = ex2(fmaf(__uint_as_float(raw[c + 3]), scale_log2, -l4.w));
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t raw[32];
+        tmem_ld32(s_addr + 32 * h2, raw);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + 32 * h2 + c);
+          float* pp = p + 32 * h2 + c;
+          pp[0] = ex2(fmaf(__uint_as_float(raw[c + 0]), scale_log2, -l4.x));
+          pp[1] = ex2(fmaf(__uint_as_float(raw[c + 1]), scale_log2, -l4.y));
+          pp[2] = ex2(fmaf(__uint_as_float(raw[c + 2]), scale_log2, -l4.z));
+          pp[3] = ex2(fmaf(__uint_as_float(raw[c + 3]), scale_log2, -l4.w));
+        }
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (!key_ok || (CAUSAL && q0 + 32 * h2 + c < key)) p[32 * h2 + c] = 0.f;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(p[32 * h2 + 2 * t], p[32 * h2 + 2 * t + 1]);
+        tmem_st16(s_addr + 16 * h2, pk);
       }
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (!key_ok || (CAUSAL && q0 + c < key)) p[c] = 0.f;
-      }
-      uint32_t pk[16];
-#pragma unroll
-      for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(p[2 * t], p[2 * t + 1]);
-      tmem_st16(s_addr, pk);
-      // dSᵀ = Pᵀ ∘ (dPᵀ − D)
+      // dSᵀ = Pᵀ ∘ (dPᵀ − D), bf16 into this warp's own dP columns.
       ok = mbar_wait(dp_full, i & 1, err);
       if (!ok) break;
       tc_fence_after();
-      tmem_ld32(dp_addr, raw);
-      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(my_D + c);
-        const float a0 = p[c + 0] * (__uint_as_float(raw[c + 0]) - d4.x);
-        const float a1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - d4.y);
-        const float a2 = p[c + 2] * (__uint_as_float(raw[c + 2]) - d4.z);
-        const float a3 = p[c + 3] * (__uint_as_float(raw[c + 3]) - d4.w);
-        pk[c / 2] = pack_bf16x2(a0, a1);
-        pk[c / 2 + 1] = pack_bf16x2(a2, a3);
-      }
-      tmem_st16(dp_addr, pk);
-      // dSᵀ into shared memory for the dQ product: row = key, 64 queries of
-      // 2 bytes = one 128-byte swizzled row; this half is chunks 4h..4h+3.
-      if (i >= 2) {
-        ok = mbar_wait(&dq_done[b], ((i - 2) >> 1) & 1, err);
-        if (!ok) break;
-      }
-      uint8_t* ds_row = sdS + b * L::DS_TILE + r * 128;
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t raw[32];
+        tmem_ld32(dp_addr + 32 * h2, raw);
+        tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int chunk = half * 4 + ch;
-        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
-            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        for (int c = 0; c < 32; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(s_D + 32 * h2 + c);
+          const float* pp = p + 32 * h2 + c;
+          pk[c / 2] = pack_bf16x2(pp[0] * (__uint_as_float(raw[c + 0]) - d4.x),
+                                  pp[1] * (__uint_as_float(raw[c + 1]) - d4.y));
+          pk[c / 2 + 1] = pack_bf16x2(pp[2] * (__uint_as_float(raw[c + 2]) - d4.z),
+                                      pp[3] * (__uint_as_float(raw[c + 3]) - d4.w));
+        }
+        tmem_st16(dp_addr + 16 * h2, pk);
       }
       tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_ready);
+      // Next tile's (lse, D) into the other buffer; its previous readers
+      // passed the barrier at the end of the previous iteration.
+      sStat[((i + 1) & 1) * 256 + ct] = stat_nx;
+      stat_nx = load_stat(i + 2);
+      named_bar_sync(1, 256);
+    }
+    // -------------------------------------------------------------- epilogue
+    // Wait for the last products; the stage-0 Q and dO buffers then stage
+    // dK (scaled) and dV for the TMA stores.
+    if (ok) ok = mbar_wait(final_bar, 0, err);
+    if (ok) {
+      tc_fence_after();
+      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + KV_COL_DK, sQ, r, half * (D / 2), scale);
+      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + KV_COL_DV, sdO, r, half * (D / 2), 1.f);
       fence_async_smem();
+    }
+    named_bar_sync(1, 256);
+    if (ok && warp == 2 && lane == 0) {
+      for (int p = 0; p < T::PANELS; ++p) {
+        tma_store_3d(&tdk, sQ + p * T::PANEL, p * 64, k0, bh);
+        tma_store_3d(&tdv, sdO + p * T::PANEL, p * 64, k0, bh);
+      }
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ dQ sweep
+
+constexpr uint32_t Q_COL_S = 0, Q_COL_DP = 128, Q_COL_DQ = 256, Q_COL_Q = 384, Q_COL_DO = 448;
+
+template <int D>
+struct DqSmem {
+  using T = Tiles<D>;
+  static constexpr int KST = 2;
+  static constexpr int Q_OFF = 0;   // Q tile; later the dQ staging tile
+  static constexpr int DO_OFF = Q_OFF + T::BYTES;
+  static constexpr int K_OFF = DO_OFF + T::BYTES;
+  static constexpr int V_OFF = K_OFF + KST * T::BYTES;
+  static constexpr int BAR_OFF = V_OFF + KST * T::BYTES;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], a_ready, s_full,
+  // dp_full, ds_ready, final
+  static constexpr int NBARS = 1 + 4 * KST + 5;
+  static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int BYTES = TMEM_SLOT_OFF + 16;
+  static constexpr int ALLOC = alloc_for(BYTES);
+  static_assert(BYTES <= kMaxDynSmem, "shared memory layout exceeds the per-block limit");
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(SWEEP_THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const __grid_constant__ CUtensorMap tdq, const float* __restrict__ lse,
+                  const float* __restrict__ Dvec, int BH, int N, float scale, float scale_log2) {
+  using L = DqSmem<D>;
+  using T = Tiles<D>;
+  constexpr int KST = L::KST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw, L::BYTES, L::ALLOC);
+  if (smem == nullptr) return;
+  uint8_t* sQ = smem + L::Q_OFF;
+  uint8_t* sdO = smem + L::DO_OFF;
+  uint8_t* sK = smem + L::K_OFF;
+  uint8_t* sV = smem + L::V_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + KST;
+  uint64_t* v_full = k_empty + KST;
+  uint64_t* v_empty = v_full + KST;
+  uint64_t* a_ready = v_empty + KST;  // Q and dO copied into TMEM
+  uint64_t* s_full = a_ready + 1;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* ds_ready = dp_full + 1;
+  uint64_t* final_bar = ds_ready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_t = (N + TILE - 1) / TILE;
+  int t, bh;  // causal: heaviest query tile (the last one) first within each head group
+  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_t, HEAD_GROUP, &t, &bh);
+  const int qt = n_t - 1 - t;
+  const int q0 = qt * TILE;
+  const int n_kv = CAUSAL ? qt + 1 : n_t;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    mbar_init(a_ready, 8);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_ready, 8);
+    mbar_init(final_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint32_t* err = &g_bwd_err;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(q_full, 2 * T::BYTES);
+      for (int p = 0; p < T::PANELS; ++p) {
+        tma_load_3d(sQ + p * T::PANEL, &tq, q_full, p * 64, q0, bh);
+        tma_load_3d(sdO + p * T::PANEL, &tdo, q_full, p * 64, q0, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % KST;
+        const uint32_t ph = ((j / KST) & 1) ^ 1;
+        if (!mbar_wait(&k_empty[s], ph, err)) break;
+        mbar_arrive_expect_tx(&k_full[s], T::BYTES);
+        for (int p = 0; p < T::PANELS; ++p)
+          tma_load_3d(sK + s * T::BYTES + p * T::PANEL, &tk, &k_full[s], p * 64, j * TILE, bh);
+        if (!mbar_wait(&v_empty[s], ph, err)) break;
+        mbar_arrive_expect_tx(&v_full[s], T::BYTES);
+        for (int p = 0; p < T::PANELS; ++p)
+          tma_load_3d(sV + s * T::BYTES + p * T::PANEL, &tv, &v_full[s], p * 64, j * TILE, bh);
+        issued = j + 1;
+      }
+      mbar_wait(q_full, 0, err);
+      for (int j = max(0, issued - KST); j < issued; ++j) {
+        mbar_wait(&k_full[j % KST], (j / KST) & 1, err);
+        mbar_wait(&v_full[j % KST], (j / KST) & 1, err);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // S, dP: A TMEM, B K-major
+      constexpr uint32_t id_q = idesc_bf16(TILE, D, false, true);      // dQ: A TMEM, B MN-major
+      // S = Q Kⱼᵀ (or dP = dO Vⱼᵀ): A = Q (dO) in TMEM, B = Kⱼ (Vⱼ) K-major.
+      auto issue_ab = [&](uint32_t a_col, uint32_t b_base, uint32_t d_col) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          mma_ts(tmem + d_col, tmem + a_col + ks * 8,
+                 sdesc_kmajor(b_base + (ks / 4) * T::PANEL, (ks % 4) * 16), id_s, ks > 0);
+        }
+      };
+      bool ok = mbar_wait(a_ready, 0, err) && mbar_wait(&k_full[0], 0, err);
+      if (ok) {
+        tc_fence_after();
+        issue_ab(Q_COL_Q, smem_u32(sK), Q_COL_S);
+        tc_commit(s_full);
+        ok = mbar_wait(&v_full[0], 0, err);
+        if (ok) {
+          tc_fence_after();
+          issue_ab(Q_COL_DO, smem_u32(sV), Q_COL_DP);
+          tc_commit(dp_full);
+          tc_commit(&v_empty[0]);
+        }
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j % KST;
+        ok = mbar_wait(ds_ready, j & 1, err);
+        if (!ok) break;
+        tc_fence_after();
+        const bool more = j + 1 < n_kv;
+        const int s1 = (j + 1) % KST;
+        // S_{j+1}: the compute warps have read S_j (ds_ready).
+        if (more) {
+          ok = mbar_wait(&k_full[s1], ((j + 1) / KST) & 1, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ab(Q_COL_Q, smem_u32(sK + s1 * T::BYTES), Q_COL_S);
+          tc_commit(s_full);
+        }
+        // dQ += dS_j Kⱼ: A = dS in TMEM (bf16 in the dP columns, halves at
+        // offsets 0 and 64), B = Kⱼ MN-major.
+        const uint32_t kb = smem_u32(sK + s * T::BYTES);
+#pragma unroll
+        for (int ks = 0; ks < TILE / 16; ++ks) {
+          const uint32_t acol = (ks / 4) * 64 + (ks % 4) * 8;
+          mma_ts(tmem + Q_COL_DQ, tmem + Q_COL_DP + acol, sdesc_mnmajor(kb, ks * 16, T::PANEL), id_q,
+                 (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(&k_empty[s]);
+        // dP_{j+1} overwrites the dP columns after the dQ product read dS_j.
+        if (more) {
+          ok = mbar_wait(&v_full[s1], ((j + 1) / KST) & 1, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ab(Q_COL_DO, smem_u32(sV + s1 * T::BYTES), Q_COL_DP);
+          tc_commit(dp_full);
+          tc_commit(&v_empty[s1]);
+        }
+      }
+      tc_commit(final_bar);
+      mbar_wait(final_bar, 0, err);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    // Warps 2..9: thread = query row r (TMEM lane); warp half h owns key
+    // columns 64h..64h+63 of each tile.
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const int q = q0 + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    constexpr float LOG2E = 1.4426950408889634f;
+    const float lse2 = (q < N) ? lse[static_cast<size_t>(bh) * N + q] * LOG2E : 0.f;
+    const float Dq = (q < N) ? Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
+    bool ok = mbar_wait(q_full, 0, err);
+    if (ok) {
+      // Copy this row of Q (half 0) or dO (half 1) into TMEM as bf16 pairs:
+      // column c holds elements 2c (low half) and 2c + 1.
+      const uint8_t* src = (half == 0 ? sQ : sdO);
+      const uint32_t dst = tmem + lane_addr + (half == 0 ? Q_COL_Q : Q_COL_DO);
+#pragma unroll
+      for (int c16 = 0; c16 < D / 2; c16 += 16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int chunk = c16 / 4 + ch;  // 16-byte chunk = 8 elements = 4 columns
+          const int panel = chunk / 8;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + panel * T::PANEL + r * 128 +
+                                                          (((chunk % 8) ^ (r & 7)) * 16));
+          w[ch * 4 + 0] = v.x;
+          w[ch * 4 + 1] = v.y;
+          w[ch * 4 + 2] = v.z;
+          w[ch * 4 + 3] = v.w;
+        }
+        tmem_st16(dst + c16, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(a_ready);
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int kb0 = j * TILE + half * 64;  // first key of this warp's half
+      ok = mbar_wait(s_full, j & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_addr = tmem + lane_addr + Q_COL_S + half * 64;
+      const uint32_t dp_addr = tmem + lane_addr + Q_COL_DP + half * 64;
+      float p[64];
+      const bool masked = (kb0 + 64 > N) || (CAUSAL && kb0 + 63 > q0);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t raw[32];
+        tmem_ld32(s_addr + 32 * h2, raw);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) p[32 * h2 + c] = ex2(fmaf(__uint_as_float(raw[c]), scale_log2, -lse2));
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int key = kb0 + 32 * h2 + c;
+            if (key >= N || (CAUSAL && key > q)) p[32 * h2 + c] = 0.f;
+          }
+        }
+      }
+      ok = mbar_wait(dp_full, j & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t raw[32];
+        tmem_ld32(dp_addr + 32 * h2, raw);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2) {
+          const float* pp = p + 32 * h2 + 2 * t2;
+          pk[t2] = pack_bf16x2(pp[0] * (__uint_as_float(raw[2 * t2]) - Dq),
+                               pp[1] * (__uint_as_float(raw[2 * t2 + 1]) - Dq));
+        }
+        tmem_st16(dp_addr + 16 * h2, pk);
+      }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_ready);
     }
     // -------------------------------------------------------------- epilogue
-    // The last dQ product's completion implies every MMA of this CTA is done;
-    // the Q and dO stage buffers then stage dK and dV for the TMA stores.
-    if (ok) ok = mbar_wait(&dq_done[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, err);
+    // dQ (scaled) in bf16, staged in the Q buffer (copied to TMEM long ago).
+    if (ok) ok = mbar_wait(final_bar, 0, err);
     if (ok) {
       tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < D / 2; cc += 32) {
-        const int c = half * (D / 2) + cc;
-        uint32_t a[32], bb[32];
-        tmem_ld32(tmem + lane_addr + COL_DK + c, a);
-        tmem_ld32(tmem + lane_addr + COL_DV + c, bb);
-        tmem_ld_wait();
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int col0 = c + ch * 8;
-          const int panel = col0 / 64;
-          const int chunk = (col0 % 64) / 8;
-          const int off = panel * L::KV_PANEL + r * 128 + ((chunk ^ (r & 7)) * 16);
-          uint4 vk, vv;
-          vk.x = pack_bf16x2(__uint_as_float(a[ch * 8 + 0]) * scale, __uint_as_float(a[ch * 8 + 1]) * scale);
-          vk.y = pack_bf16x2(__uint_as_float(a[ch * 8 + 2]) * scale, __uint_as_float(a[ch * 8 + 3]) * scale);
-          vk.z = pack_bf16x2(__uint_as_float(a[ch * 8 + 4]) * scale, __uint_as_float(a[ch * 8 + 5]) * scale);
-          vk.w = pack_bf16x2(__uint_as_float(a[ch * 8 + 6]) * scale, __uint_as_float(a[ch * 8 + 7]) * scale);
-          vv.x = pack_bf16x2(__uint_as_float(bb[ch * 8 + 0]), __uint_as_float(bb[ch * 8 + 1]));
-          vv.y = pack_bf16x2(__uint_as_float(bb[ch * 8 + 2]), __uint_as_float(bb[ch * 8 + 3]));
-          vv.z = pack_bf16x2(__uint_as_float(bb[ch * 8 + 4]), __uint_as_float(bb[ch * 8 + 5]));
-          vv.w = pack_bf16x2(__uint_as_float(bb[ch * 8 + 6]), __uint_as_float(bb[ch * 8 + 7]));
-          *reinterpret_cast<uint4*>(sQ + off) = vk;
-          *reinterpret_cast<uint4*>(sdO + off) = vv;
-        }
-      }
+      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + Q_COL_DQ, sQ, r, half * (D / 2), scale);
       fence_async_smem();
     }
     named_bar_sync(1, 256);
     if (ok && warp == 2 && lane == 0) {
-      for (int p = 0; p < L::PANELS; ++p) {
-        tma_store_3d(&tdk, sQ + p * L::KV_PANEL, p * 64, k0, bh);
-        tma_store_3d(&tdv, sdO + p * L::KV_PANEL, p * 64, k0, bh);
-      }
+      for (int p = 0; p < T::PANELS; ++p) tma_store_3d(&tdq, sQ + p * T::PANEL, p * 64, q0, bh);
       tma_store_commit();
       tma_store_wait_all();
     }
-  } else {
-    // ------------------------------------------------------------ dQ warps
-    // Warps 10..13: read dQᵀ_i out of TMEM (lane = head-dim index, column =
-    // query), release the TMEM columns, then stage 32 query rows at a time in
-    // shared memory in the accumulator's [query][d] layout and add them to
-    // the fp32 accumulator with one bulk reduction (rows q0.. are contiguous).
-    const int quarter = warp & 3;
-    const int dd = quarter * 32 + lane;
-    const uint32_t dq_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + COL_DQ;
-    float* acc_h = dq_acc + static_cast<size_t>(bh) * N * D;
-    const bool active = (D == 128) || (quarter < 2);
-    const bool issuer = (warp == 10 && lane == 0);
-    for (int i = 0; i < n_it; ++i) {
-      const bool got = mbar_wait(dq_full, i & 1, err);
-      if (named_bar_any(2, 128, !got)) break;  // all four warps leave together
-      tc_fence_after();
-      uint32_t v[2][32];
-      tmem_ld32(dq_addr, v[0]);
-      tmem_ld32(dq_addr + 32, v[1]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-      const int q0 = (qt_begin + i) * BQ;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int rows = min(32, N - (q0 + 32 * h));
-        // the previous bulk reduction must have finished reading the stage
-        if (issuer) bulk_wait_read_all();
-        named_bar_sync(2, 128);
-        if (rows > 0) {
-          if (active) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) sDqStage[c * D + dd] = __uint_as_float(v[h][c]);
-          }
-          fence_async_smem();
-        }
-        named_bar_sync(2, 128);
-        if (issuer && rows > 0) {
-          bulk_reduce_add_f32(acc_h + static_cast<size_t>(q0 + 32 * h) * D, sDqStage,
-                              static_cast<uint32_t>(rows) * D * 4u);
-          tma_store_commit();
-        }
-      }
-    }
-    if (issuer) tma_store_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -524,61 +719,81 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int D, bool CAUSAL>
-static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
-                                 const CUtensorMap& tv, const CUtensorMap& tdo,
-                                 const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
-                                 const float* Dvec, float* dq_acc, int BH, int N, float scale,
-                                 cudaStream_t stream) {
-  auto kern = bwd_main_kernel<D, CAUSAL>;
-  const int smem = Smem<D>::ALLOC;
+static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, const CUtensorMap& tdk,
+                                 const CUtensorMap& tdv, const float* lse, const float* Dvec, int BH,
+                                 int N, float scale, cudaStream_t stream) {
+  auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+  const int smem = DkdvSmem<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int n_kt = (N + BK - 1) / BK;
-  dim3 grid(static_cast<unsigned>(n_kt) * static_cast<unsigned>(BH));
-  kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, scale,
-                                        scale * 1.4426950408889634f);
+  const int n_t = (N + TILE - 1) / TILE;
+  dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BH));
+  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale,
+                                               scale * 1.4426950408889634f);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse,
+                               const float* Dvec, int BH, int N, float scale, cudaStream_t stream) {
+  auto kern = bwd_dq_kernel<D, CAUSAL>;
+  const int smem = DqSmem<D>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_t = (N + TILE - 1) / TILE;
+  dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BH));
+  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale,
+                                               scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
 
 }  // namespace bwd
 
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dO, float* Dvec,
-                                  float* dq_acc, int BH, int N, int d, cudaStream_t stream) {
+                                  int BH, int N, int d, cudaStream_t stream) {
   const long long rows = static_cast<long long>(BH) * N;
   if (d == 64) {
     const long long blocks = (rows + 31) / 32;
-    bwd::preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o, dO, Dvec, dq_acc, rows);
+    bwd::preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o, dO, Dvec, rows);
   } else {
     const long long blocks = (rows + 15) / 16;
-    bwd::preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o, dO, Dvec, dq_acc, rows);
+    bwd::preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o, dO, Dvec, rows);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(const void* q, const void* k, const void* v, const void* dO,
-                            void* dk, void* dv, const float* lse, const float* Dvec,
-                            float* dq_acc, int BH, int N, int d, float scale, bool causal,
-                            cudaStream_t stream) {
+cudaError_t launch_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                            void* dv, const float* lse, const float* Dvec, int BH, int N, int d,
+                            float scale, bool causal, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!make_tmap_bf16(&tq, q, BH, N, d, bwd::BQ) || !make_tmap_bf16(&tdo, dO, BH, N, d, bwd::BQ) ||
-      !make_tmap_bf16(&tk, k, BH, N, d, bwd::BK) || !make_tmap_bf16(&tv, v, BH, N, d, bwd::BK) ||
-      !make_tmap_bf16(&tdk, dk, BH, N, d, bwd::BK) || !make_tmap_bf16(&tdv, dv, BH, N, d, bwd::BK))
+  const int T = bwd::TILE;
+  if (!make_tmap_bf16(&tq, q, BH, N, d, T) || !make_tmap_bf16(&tdo, dO, BH, N, d, T) ||
+      !make_tmap_bf16(&tk, k, BH, N, d, T) || !make_tmap_bf16(&tv, v, BH, N, d, T) ||
+      !make_tmap_bf16(&tdk, dk, BH, N, d, T) || !make_tmap_bf16(&tdv, dv, BH, N, d, T))
     return cudaErrorInvalidValue;
   if (d == 64)
-    return causal ? bwd::launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, scale, stream)
-                  : bwd::launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, scale, stream);
-  return causal ? bwd::launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, scale, stream)
-                : bwd::launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, dq_acc, BH, N, scale, stream);
+    return causal ? bwd::launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream)
+                  : bwd::launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream);
+  return causal ? bwd::launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream)
+                : bwd::launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream);
 }
 
-cudaError_t launch_bwd_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int BH, int N, int d,
-                                  float scale, cudaStream_t stream) {
-  const long long n8 = static_cast<long long>(BH) * N * d / 8;
-  long long blocks = (n8 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (blocks < 1) blocks = 1;
-  bwd::dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(dq_acc, dq, n8, scale);
-  return cudaGetLastError();
+cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                          const float* lse, const float* Dvec, int BH, int N, int d, float scale,
+                          bool causal, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  const int T = bwd::TILE;
+  if (!make_tmap_bf16(&tq, q, BH, N, d, T) || !make_tmap_bf16(&tdo, dO, BH, N, d, T) ||
+      !make_tmap_bf16(&tk, k, BH, N, d, T) || !make_tmap_bf16(&tv, v, BH, N, d, T) ||
+      !make_tmap_bf16(&tdq, dq, BH, N, d, T))
+    return cudaErrorInvalidValue;
+  if (d == 64)
+    return causal ? bwd::launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream)
+                  : bwd::launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream);
+  return causal ? bwd::launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream)
+                : bwd::launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream);
 }
 
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream) {

@@ -10,19 +10,19 @@
 namespace fa {
 
 // Kernel launchers. Pointers are device pointers to contiguous [BH][N][d]
-// bf16 tensors (lse, Dvec: [BH][N] fp32; dq_acc: [BH][N][d] fp32); each
+// bf16 tensors (lse, Dvec: [BH][N] fp32); each
 // launcher builds the TMA descriptors its kernel needs. Arguments are assumed
 // validated by the caller. Return the launch (or descriptor) error.
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
                        int N, int d, float scale, bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dO, float* Dvec,
-                                  float* dq_acc, int BH, int N, int d, cudaStream_t stream);
-cudaError_t launch_bwd_main(const void* q, const void* k, const void* v, const void* dO,
-                            void* dk, void* dv, const float* lse, const float* Dvec,
-                            float* dq_acc, int BH, int N, int d, float scale, bool causal,
-                            cudaStream_t stream);
-cudaError_t launch_bwd_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int BH, int N, int d,
-                                  float scale, cudaStream_t stream);
+                                  int BH, int N, int d, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                            void* dv, const float* lse, const float* Dvec, int BH, int N, int d,
+                            float scale, bool causal, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                          const float* lse, const float* Dvec, int BH, int N, int d, float scale,
+                          bool causal, cudaStream_t stream);
 
 // Device error words (one per translation unit): read, then clear.
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream);

@@ -1,7 +1,7 @@
 // Allocation-free variant of the backward pass.
 //
-// fa_bwd needs device scratch (an fp32 dQ accumulator and the fp32 row
-// vector D) and expects the caller to provide it. Some callers cannot make
+// fa_bwd needs device scratch (the fp32 row vector D = rowsum(dO ∘ O)) and
+// expects the caller to provide it. Some callers cannot make
 // that allocation: a host application that owns all device memory through
 // its own fixed pool and gives plug-ins no allocator, a runtime that forbids
 // device allocation after start-up (fixed memory budget, real-time loop), or
@@ -15,8 +15,8 @@
 //     library until the process exits;
 //   * shared by every call on a device: calls whose kernels overlap on the
 //     GPU (other streams, other host threads) race on it;
-//   * it keeps the last call's contents; the preprocess kernel re-zeroes the
-//     dQ accumulator and rewrites D on every call, so nothing stale is read.
+//   * it keeps the last call's contents; the preprocess kernel rewrites D on
+//     every call before anything reads it, so nothing stale is read.
 // The array's device address is looked up once per device (with that device
 // current) on the first call there.
 #include <cuda_bf16.h>
@@ -69,20 +69,17 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     return FA_ERR_MISALIGNED;
   void* scratch = scratch_on_current_device();
   if (!scratch) return FA_ERR_CUDA;
-  float* dq_acc = static_cast<float*>(scratch);
-  const size_t acc_bytes = static_cast<size_t>(B) * H * N * d * sizeof(float);
-  float* Dvec = reinterpret_cast<float*>(static_cast<char*>(scratch) +
-                                         ((acc_bytes + 255) & ~static_cast<size_t>(255)));
+  float* Dvec = static_cast<float*>(scratch);
   const int BH = B * H;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o),
-                                static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, BH, N, d,
+                                static_cast<const __nv_bfloat16*>(dO), Dvec, BH, N, d,
                                 s) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (fa::launch_bwd_main(q, k, v, dO, dk, dv, lse, Dvec, dq_acc, BH, N, d, scale, causal != 0,
-                          s) != cudaSuccess)
+  if (fa::launch_bwd_dkdv(q, k, v, dO, dk, dv, lse, Dvec, BH, N, d, scale, causal != 0, s) !=
+      cudaSuccess)
     return FA_ERR_CUDA;
-  if (fa::launch_bwd_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), BH, N, d, scale, s) !=
+  if (fa::launch_bwd_dq(q, k, v, dO, dq, lse, Dvec, BH, N, d, scale, causal != 0, s) !=
       cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;

@@ -71,8 +71,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int d, float scale, int causal, void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
- * [B][H][N][d] followed by the fp32 row vector D [B][H][N]
+ * Bytes of device workspace fa_bwd needs: the fp32 row vector D [B][H][N]
  * (D_i = Σ_c dO_ic · O_ic). Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
@@ -85,28 +84,29 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   dq, dk, dv      [B][H][N][d] bf16 outputs.
  *   workspace       device buffer of at least fa_bwd_workspace_bytes(...)
  *                   bytes, 16-byte aligned; contents on entry are ignored.
- * Launches three kernels in order on `stream`: preprocess (D and zeroed dQ
- * accumulator), the main dK/dV/dQ kernel, and the dQ conversion.
+ * Launches three kernels in order on `stream`: preprocess (D), the dK/dV
+ * sweep over query tiles, and the dQ sweep over key tiles.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
            int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
- * The three backward stages as separate calls (fa_bwd runs all three).
- * They share fa_bwd's argument rules; `Dvec` is fp32 [B][H][N] and `dq_acc`
- * fp32 [B][H][N][d], both caller-owned device memory.
- *   fa_bwd_preprocess : Dvec_i = Σ_c dO_ic·O_ic; dq_acc = 0.
- *   fa_bwd_main       : dk, dv (bf16, final) and dq_acc += unscaled dS·K.
- *   fa_bwd_dq_convert : dq = bf16(scale · dq_acc).
+ * The three backward stages as separate calls (fa_bwd runs all three, in
+ * this order, on one stream). They share fa_bwd's argument rules; `Dvec` is
+ * fp32 [B][H][N] caller-owned device memory.
+ *   fa_bwd_preprocess : Dvec_i = Σ_c dO_ic·O_ic.
+ *   fa_bwd_dkdv       : dk = scale·dSᵀ q and dv = Pᵀ dO (bf16, final).
+ *   fa_bwd_dq         : dq = scale·dS k (bf16, final).
  */
-int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H,
-                      int N, int d, void* stream);
-int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                const float* Dvec, float* dq_acc, void* dk, void* dv, int B, int H, int N, int d,
-                float scale, int causal, void* stream);
-int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale,
+int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, int H, int N, int d,
                       void* stream);
+int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                const float* Dvec, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                int causal, void* stream);
+int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+              const float* Dvec, void* dq, int B, int H, int N, int d, float scale, int causal,
+              void* stream);
 
 /* Size in bytes of the static scratch area behind fa_bwd_noalloc (32 MiB). */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -120,14 +120,14 @@ int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d,
  * synchronisation.
  *
  * Same arguments and results as fa_bwd, minus the workspace: the scratch
- * (fp32 dQ accumulator and D vector, fa_bwd_workspace_bytes(B,H,N,d) bytes)
- * is a file-scope __device__ array of FA_BWD_NOALLOC_SCRATCH_BYTES inside
+ * (the fp32 D vector, fa_bwd_workspace_bytes(B,H,N,d) bytes) is a
+ * file-scope __device__ array of FA_BWD_NOALLOC_SCRATCH_BYTES inside
  * the library image, held on every GPU that loads the library until the
  * process exits. The call itself allocates nothing (no cudaMalloc,
  * cudaFree or allocating library routine).
  *   - Problems whose scratch need exceeds FA_BWD_NOALLOC_SCRATCH_BYTES are
  *     rejected with FA_ERR_WORKSPACE before anything is launched
- *     (B*H*N*(d+1)*4 bytes, rounded up; e.g. B=8 H=12 N=1024 d=64 fits).
+ *     (B*H*N*4 bytes: up to 8,388,608 query rows over all heads).
  *   - The first call on a device looks up the array's device address with
  *     that device current (a one-time set-up per device); make that first
  *     call before any stream capture.
@@ -135,7 +135,7 @@ int fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d,
  *     overlap on the GPU (different streams or host threads without
  *     ordering between them) race on it and give undefined results; order
  *     such calls on one stream. The array keeps the last call's contents;
- *     each call re-zeroes the accumulator and rewrites D before use.
+ *     each call rewrites D before anything reads it.
  */
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,

@@ -68,10 +68,7 @@ def test_fwd_argument_errors(L):
 
 def test_bwd_workspace_size(L):
     B, H, N, d = 2, 3, 100, 64
-    n = B * H * N
-    acc = n * d * 4
-    expect = ((acc + 255) // 256) * 256 + n * 4
-    assert L.fa_bwd_workspace_bytes(B, H, N, d) == expect
+    assert L.fa_bwd_workspace_bytes(B, H, N, d) == B * H * N * 4  # the fp32 D vector
     assert L.fa_bwd_workspace_bytes(B, H, 0, d) == 0
     assert L.fa_bwd_workspace_bytes(B, H, N, 80) == 0
 
@@ -90,10 +87,11 @@ def test_bwd_argument_errors(L):
     assert call(ws_bytes=ws - 1) == 6
     assert call(workspace=MIS) == 3
     # stage entry points
-    assert L.fa_bwd_preprocess(FAKE, FAKE, FAKE, NUL, 1, 1, 16, 64, NUL) == 1
-    assert L.fa_bwd_main(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MIS, 1, 1, 16, 64,
+    assert L.fa_bwd_preprocess(FAKE, FAKE, NUL, 1, 1, 16, 64, NUL) == 1
+    assert L.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MIS, 1, 1, 16, 64,
                          0.125, 0, NUL) == 3
-    assert L.fa_bwd_dq_convert(FAKE, FAKE, 1, 1, 16, 64, 0.0, NUL) == 1
+    assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0.0, 1, NUL) == 1
+    assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 96, 0.1, 1, NUL) == 2
 
 
 def test_product_path_does_not_import_the_oracle():
