@@ -2,20 +2,32 @@
 //
 // Method (CMU 10-423 L17–L18 notes, section "FlashAttention 本身"; dcwnkz.com
 // GPU-tricks article, FlashAttention section and its six-score worked
-// example): for one block of 128 query rows, sweep the keys/values in tiles
-// of 128; keep per row the running max m, the running denominator l and the
+// example): for a block of query rows, sweep the keys/values in tiles of
+// 128; keep per row the running max m, the running denominator l and the
 // running weighted sum O; when a tile raises m, multiply l and O by
 // e^(m_old - m_new) before adding the tile; divide by l once at the end.
 // S = Q Kᵀ and P never leave the SM: S lives in tensor memory (TMEM), P is
 // written back into TMEM as bf16 and fed straight to the P·V MMA.
 //
-// Roles inside one CTA (192 threads):
-//   warp 0      TMA producer: Q once, then K_j / V_j into a 2-stage ring
-//   warp 1      TMEM owner and MMA issuer (one elected lane)
-//   warps 2..5  softmax: one thread per query row (TMEM lane), rescale of O,
-//               epilogue (O / l -> bf16 -> TMA store, lse)
-// TMEM columns: three S buffers at 0, 128, 256 (so S_{j+3} is only written
-// after the P·V MMA that read buffer j%3 has completed), O at 384.
+// One CTA owns two 128-row query tiles (Q0, Q1) of one head and sweeps the
+// key/value tiles once for both ("ping-pong"): while one softmax group
+// exponentiates its S tile, the tensor core runs the other group's products.
+// Roles (320 threads):
+//   warp 0      TMA producer: Q0, Q1 once, then K_j / V_j into 2-stage rings
+//   warp 1      TMEM owner and MMA issuer (one lane)
+//   warps 2..5  softmax group 0 (Q0), one thread per query row (TMEM lane)
+//   warps 6..9  softmax group 1 (Q1)
+// TMEM columns: S0 0.., S1 128.., O0 256.., O1 384... The MMA order is
+//   S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 ...
+// S_g,j+1 overwrites the columns PV_g,j reads P from; it is issued after it
+// on the same thread and tcgen05 MMAs execute in issue order.
+//
+// Rescaling: the exponent reference m of a row is raised to the running max
+// only when the max has grown past it by more than RESCALE_LOG2 (in log2
+// units); O and l are then multiplied by 2^(m_old - m_new) as in the worked
+// example. Between raises P = 2^(s - m) may exceed 1 (at most 2^RESCALE_LOG2),
+// which bf16 and the fp32 sums carry as well; the final O / l is the same
+// quantity because numerator and denominator share the reference.
 //
 // Causal masking ("07-16 下午：分布式大模型训练与推理", section 自回归语言模型推理):
 // query i sees keys j <= i; tiles above the diagonal are skipped, the
@@ -32,25 +44,25 @@ static __device__ uint32_t g_fwd_err;
 
 namespace fwd {
 
-constexpr int BM = 128;       // query rows per CTA
+constexpr int BM = 128;       // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;       // keys per tile
-constexpr int NSB = 3;        // S buffers in TMEM
-constexpr int THREADS = 192;  // 6 warps
-constexpr uint32_t O_COL = 384;
+constexpr int THREADS = 320;  // 10 warps
 constexpr int HEAD_GROUP = 8;
+constexpr float RESCALE_LOG2 = 8.f;
 
 template <int D>
 struct Smem {
   static constexpr int PANELS = D / 64;
   static constexpr int STAGES = 2;
   static constexpr int TILE_BYTES = BM * D * 2;  // = BN * D * 2
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + TILE_BYTES;
+  static constexpr int PANEL = BM * 128;
+  static constexpr int Q_OFF = 0;                // Q0, Q1 (later the O staging tiles)
+  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-  // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2],
-  //           s_full[3], p_ready[3], pv_done[3], final
-  static constexpr int NBARS = 1 + 4 * STAGES + 3 * NSB + 1;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
+  // p_ready[2], pv_done[2], final
+  static constexpr int NBARS = 1 + 4 * STAGES + 6 + 1;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   // Slack for 1024-byte alignment; at least 116 KB so that only one CTA
@@ -76,24 +88,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* k_empty = k_full + L::STAGES;
   uint64_t* v_full = k_empty + L::STAGES;
   uint64_t* v_empty = v_full + L::STAGES;
-  uint64_t* s_full = v_empty + L::STAGES;
-  uint64_t* p_ready = s_full + NSB;
-  uint64_t* pv_done = p_ready + NSB;
-  uint64_t* final_bar = pv_done + NSB;
+  uint64_t* s_full = v_empty + L::STAGES;   // [2], one per group
+  uint64_t* p_ready = s_full + 2;           // [2]
+  uint64_t* pv_done = p_ready + 2;          // [2]
+  uint64_t* final_bar = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   // Heads in groups of HEAD_GROUP (their K/V stay in L2 while the group
-  // runs); within a group the heaviest (causal) query tiles go first.
-  const int n_qt = (N + BM - 1) / BM;
+  // runs); within a group the heaviest (causal) query blocks go first.
+  const int n_qb = (N + 2 * BM - 1) / (2 * BM);  // blocks of two query tiles
   int t, bh;
-  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_qt, HEAD_GROUP, &t, &bh);
-  const int qt = n_qt - 1 - t;
-  const int q0 = qt * BM;
+  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_qb, HEAD_GROUP, &t, &bh);
+  const int qb = n_qb - 1 - t;
+  const int qrow0 = qb * 2 * BM;
   const int n_kt_all = (N + BN - 1) / BN;
-  const int n_kt = CAUSAL ? min(n_kt_all, qt + 1) : n_kt_all;
+  // key tiles per group: group g covers rows qrow0 + 128g .. + 127
+  const int n_g0 = CAUSAL ? min(n_kt_all, 2 * qb + 1) : n_kt_all;
+  const int n_g1 = CAUSAL ? min(n_kt_all, 2 * qb + 2) : n_kt_all;
+  const int n_kt = n_g1;  // n_g1 >= n_g0 >= 1
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -103,10 +118,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < NSB; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_ready[b], 4);
-      mbar_init(&pv_done[b], 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&p_ready[g], 4);
+      mbar_init(&pv_done[g], 1);
     }
     mbar_init(final_bar, 1);
     fence_mbar_init();
@@ -127,23 +142,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
-      for (int p = 0; p < L::PANELS; ++p) tma_load_3d(sQ + p * (BM * 128), &tq, q_full, p * 64, q0, bh);
+      mbar_arrive_expect_tx(q_full, 2 * L::TILE_BYTES);
+      for (int g = 0; g < 2; ++g)
+        for (int p = 0; p < L::PANELS; ++p)
+          tma_load_3d(sQ + g * L::TILE_BYTES + p * L::PANEL, &tq, q_full, p * 64, qrow0 + g * BM, bh);
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < n_kt && ok; ++j) {
         const int s = j % L::STAGES;
-        const uint32_t ph = (j / L::STAGES) & 1;
-        ok = mbar_wait(&k_empty[s], ph ^ 1, err);
+        const uint32_t ph = ((j / L::STAGES) & 1) ^ 1;
+        ok = mbar_wait(&k_empty[s], ph, err);
         if (!ok) break;
         mbar_arrive_expect_tx(&k_full[s], L::TILE_BYTES);
         for (int p = 0; p < L::PANELS; ++p)
-          tma_load_3d(sK + s * L::TILE_BYTES + p * (BN * 128), &tk, &k_full[s], p * 64, j * BN, bh);
-        ok = mbar_wait(&v_empty[s], ph ^ 1, err);
+          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &k_full[s], p * 64, j * BN, bh);
+        ok = mbar_wait(&v_empty[s], ph, err);
         if (!ok) break;
         mbar_arrive_expect_tx(&v_full[s], L::TILE_BYTES);
         for (int p = 0; p < L::PANELS; ++p)
-          tma_load_3d(sV + s * L::TILE_BYTES + p * (BN * 128), &tv, &v_full[s], p * 64, j * BN, bh);
+          tma_load_3d(sV + s * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[s], p * 64, j * BN, bh);
         issued = j + 1;
       }
       // Drain: never leave the CTA with copies still landing in its smem.
@@ -160,66 +177,84 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
-      bool ok = mbar_wait(q_full, 0, err);
-      auto issue_s = [&](int jj) -> bool {
-        const int s = jj % L::STAGES;
-        if (!mbar_wait(&k_full[s], (jj / L::STAGES) & 1, err)) return false;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + (jj % NSB) * BN;
-        const uint32_t q_base = smem_u32(sQ);
-        const uint32_t k_base = smem_u32(sK + s * L::TILE_BYTES);
+      // S_g = Q_g K_jᵀ into the S columns of group g.
+      auto issue_s = [&](int g, int j) {
+        const uint32_t q_base = smem_u32(sQ + g * L::TILE_BYTES);
+        const uint32_t k_base = smem_u32(sK + (j % L::STAGES) * L::TILE_BYTES);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t poff = (ks / 4) * (BM * 128);
-          mma_ss(d_tmem, sdesc_kmajor(q_base + poff, (ks % 4) * 16),
+          const uint32_t poff = (ks / 4) * L::PANEL;
+          mma_ss(tmem + g * BN, sdesc_kmajor(q_base + poff, (ks % 4) * 16),
                  sdesc_kmajor(k_base + poff, (ks % 4) * 16), idesc_s, ks > 0);
         }
-        tc_commit(&s_full[jj % NSB]);
-        tc_commit(&k_empty[s]);
-        return true;
+        tc_commit(&s_full[g]);
       };
-      for (int jj = 0; jj < min(NSB, n_kt) && ok; ++jj) ok = issue_s(jj);
-      for (int j = 0; j < n_kt && ok; ++j) {
-        const int s = j % L::STAGES;
-        const int b = j % NSB;
-        ok = mbar_wait(&v_full[s], (j / L::STAGES) & 1, err) &&
-             mbar_wait(&p_ready[b], (j / NSB) & 1, err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(sV + s * L::TILE_BYTES);
-        const uint32_t p_tmem = tmem + b * BN;
+      // O_g += P_g V_j; P_g is bf16 in the first 64 S columns of group g.
+      auto issue_pv = [&](int g, int j) {
+        const uint32_t v_base = smem_u32(sV + (j % L::STAGES) * L::TILE_BYTES);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          mma_ts(tmem + O_COL, p_tmem + ks * 8, sdesc_mnmajor(v_base, ks * 16, BN * 128), idesc_o,
-                 (j > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(tmem + 256 + g * 128, tmem + g * BN + ks * 8, sdesc_mnmajor(v_base, ks * 16, L::PANEL),
+                 idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(&pv_done[b]);
-        tc_commit(&v_empty[s]);
-        // S_{j+2} reuses the buffer of P_{j-1}: wait until P V_{j-1} is done.
-        if (j >= 1 && j + 2 < n_kt) {
-          ok = mbar_wait(&pv_done[(j - 1) % NSB], ((j - 1) / NSB) & 1, err);
-          if (ok) ok = issue_s(j + 2);
-        }
+        tc_commit(&pv_done[g]);
+      };
+      bool ok = mbar_wait(q_full, 0, err) && mbar_wait(&k_full[0], 0, err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc_commit(&k_empty[0]);
       }
-      // All issued MMAs complete before TMEM is released.
+      for (int j = 0; j < n_kt && ok; ++j) {
+        const int s = j % L::STAGES;
+        const int s1 = (j + 1) % L::STAGES;
+        ok = mbar_wait(&v_full[s], (j / L::STAGES) & 1, err);
+        if (!ok) break;
+        bool k_next_ready = false;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const int n_g = (g == 0) ? n_g0 : n_g1;
+          if (j >= n_g) continue;
+          ok = mbar_wait(&p_ready[g], j & 1, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(g, j);
+          if (j + 1 < n_g) {
+            if (!k_next_ready) {
+              ok = mbar_wait(&k_full[s1], ((j + 1) / L::STAGES) & 1, err);
+              if (!ok) break;
+              tc_fence_after();
+              k_next_ready = true;
+            }
+            issue_s(g, j + 1);
+          }
+        }
+        if (!ok) break;
+        tc_commit(&v_empty[s]);
+        if (k_next_ready) tc_commit(&k_empty[s1]);
+      }
       tc_commit(final_bar);
       mbar_wait(final_bar, 0, err);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int g = (warp - 2) >> 2;  // group
+    const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
+    const int q0 = qrow0 + g * BM;
     const int qrow = q0 + r;
+    const int n_mine = (g == 0) ? n_g0 : n_g1;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    float m = -INFINITY;  // running max, in log2 units of scaled scores
-    float l = 0.f;        // running denominator
+    const uint32_t s_addr = tmem + lane_addr + g * BN;
+    const uint32_t o_addr = tmem + lane_addr + 256 + g * 128;
+    float m = -INFINITY;  // exponent reference (log2 units of scaled scores)
+    float l = 0.f;        // running denominator relative to m
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      const int b = j % NSB;
-      ok = mbar_wait(&s_full[b], (j / NSB) & 1, err);
+    for (int j = 0; j < n_mine; ++j) {
+      ok = mbar_wait(&s_full[g], j & 1, err);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + b * BN;
       uint32_t raw[4][32];
       tmem_ld32(s_addr + 0, raw[0]);
       tmem_ld32(s_addr + 32, raw[1]);
@@ -230,8 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(raw[c / 32][c % 32]);
       const int k0 = j * BN;
-      const bool need_mask = (k0 + BN > N) || (CAUSAL && k0 + BN - 1 > q0);
-      if (need_mask) {
+      if ((k0 + BN > N) || (CAUSAL && k0 + BN - 1 > q0)) {
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const int key = k0 + c;
@@ -247,69 +281,67 @@ __global__ void __launch_bounds__(THREADS, 1)
         mx3 = fmaxf(mx3, x[c + 3]);
       }
       const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
-      const float m_new = fmaxf(m, tile_max);
-      const float alpha = ex2(m - m_new);  // e^(m_old - m_new); 0 on the first tile
+      // Raise the reference when the max outgrew it by more than the
+      // threshold (always on the first tile, where m = -inf).
+      const bool warp_raise = __any_sync(0xffffffffu, tile_max > m + RESCALE_LOG2);
+      float alpha = 1.f;
+      if (warp_raise) {
+        const float m_new = fmaxf(m, tile_max);
+        alpha = ex2(m - m_new);  // 0 on the first tile
+        m = m_new;
+        l *= alpha;
+      }
       float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[BN / 2];
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = ex2(fmaf(x[c], scale_log2, -m_new));
-        const float p1 = ex2(fmaf(x[c + 1], scale_log2, -m_new));
-        sum0 += p0;
-        sum1 += p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2) {
+          const float p0 = ex2(fmaf(x[c + 2 * t2], scale_log2, -m));
+          const float p1 = ex2(fmaf(x[c + 2 * t2 + 1], scale_log2, -m));
+          sum0 += p0;
+          sum1 += p1;
+          pk[t2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + c / 2, pk);  // P (bf16) into the first 64 S columns
       }
-      l = l * alpha + (sum0 + sum1);
-      m = m_new;
-      // P (bf16) overwrites the first 64 columns of this S buffer.
-#pragma unroll
-      for (int c = 0; c < BN / 2; c += 16) {
-        uint32_t part[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) part[t] = pk[c + t];
-        tmem_st16(s_addr + c, part);
-      }
-      // Rescale O by alpha once P V_{j-1} has landed (skipped when the whole
-      // warp's rows kept their max, i.e. alpha == 1 everywhere).
-      if (j > 0) {
-        ok = mbar_wait(&pv_done[(j - 1) % NSB], ((j - 1) / NSB) & 1, err);
+      l += sum0 + sum1;
+      // O *= alpha once P V_{j-1} has landed (only when this warp raised).
+      if (warp_raise && j > 0) {
+        ok = mbar_wait(&pv_done[g], (j - 1) & 1, err);
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t o_addr = tmem + lane_addr + O_COL;
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + c, o);
-            tmem_ld_wait();
-            uint32_t a[16], bb[16];
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + c, o);
+          tmem_ld_wait();
+          uint32_t a[16], bb[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              a[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-              bb[t] = __float_as_uint(__uint_as_float(o[16 + t]) * alpha);
-            }
-            tmem_st16(o_addr + c, a);
-            tmem_st16(o_addr + c + 16, bb);
+          for (int t2 = 0; t2 < 16; ++t2) {
+            a[t2] = __float_as_uint(__uint_as_float(o[t2]) * alpha);
+            bb[t2] = __float_as_uint(__uint_as_float(o[16 + t2]) * alpha);
           }
+          tmem_st16(o_addr + c, a);
+          tmem_st16(o_addr + c + 16, bb);
         }
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[b]);
+      if (lane == 0) mbar_arrive(&p_ready[g]);
     }
     // -------------------------------------------------------------- epilogue
-    if (ok) ok = mbar_wait(&pv_done[(n_kt - 1) % NSB], ((n_kt - 1) / NSB) & 1, err);
+    if (ok) ok = mbar_wait(&pv_done[g], (n_mine - 1) & 1, err);
+    uint8_t* stage = sQ + g * L::TILE_BYTES;  // Q_g is no longer read by any MMA
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const uint32_t o_addr = tmem + lane_addr + O_COL;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
         tmem_ld32(o_addr + c, o);
         tmem_ld_wait();
-        // 32 columns = 4 chunks of 16 bytes, written in the 128-byte swizzle.
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int col0 = c + ch * 8;
@@ -320,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           val.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * inv_l, __uint_as_float(o[ch * 8 + 3]) * inv_l);
           val.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * inv_l, __uint_as_float(o[ch * 8 + 5]) * inv_l);
           val.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * inv_l, __uint_as_float(o[ch * 8 + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(sQ + panel * (BM * 128) + r * 128 + ((chunk ^ (r & 7)) * 16)) = val;
+          *reinterpret_cast<uint4*>(stage + panel * L::PANEL + r * 128 + ((chunk ^ (r & 7)) * 16)) = val;
         }
       }
       if (qrow < N) {
@@ -329,9 +361,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       fence_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (ok && warp == 2 && lane == 0) {
-      for (int p = 0; p < L::PANELS; ++p) tma_store_3d(&to, sQ + p * (BM * 128), p * 64, q0, bh);
+    named_bar_sync(1 + g, 128);
+    if (ok && (warp & 3) == 2 && lane == 0 && q0 < N) {
+      for (int p = 0; p < L::PANELS; ++p) tma_store_3d(&to, stage + p * L::PANEL, p * 64, q0, bh);
       tma_store_commit();
       tma_store_wait_all();
     }
@@ -352,8 +384,8 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
   const int smem = Smem<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int n_qt = (N + BM - 1) / BM;
-  dim3 grid(static_cast<unsigned>(n_qt) * static_cast<unsigned>(BH));
+  const int n_qb = (N + 2 * BM - 1) / (2 * BM);
+  dim3 grid(static_cast<unsigned>(n_qb) * static_cast<unsigned>(BH));
   const float scale_log2 = scale * 1.4426950408889634f;
   kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, to, lse, BH, N, scale_log2);
   return cudaGetLastError();
