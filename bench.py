@@ -298,13 +298,14 @@ def run_ours(args, w, rank, world, dist):
     peaks, peak_kind = load_peaks()
 
     # Dominant kernel: the one with the largest share of the step. Its
-    # algorithmic FLOPs: fwd 4·d per pair (QKᵀ, PV); dkdv 8·d (Sᵀ, dPᵀ, dV,
-    # dK); dq 6·d (S, dP, dQ) — the dq sweep recomputes S and dP.
+    # algorithmic FLOPs (the method's products it performs, 2mkn each):
+    # fwd 4·d per pair (QKᵀ, PV); dkdv 8·d (recomputed Sᵀ, dPᵀ, dV, dK);
+    # dq 2·d (dQ; its second recomputation of S and dP is not counted).
     bsrc = ["exact_tiled_attention_24_gb300/csrc/fa_bwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
     fsrc = ["exact_tiled_attention_24_gb300/csrc/fa_fwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
     cands = [("fwd", fwd_ms, F_fwd, fsrc)]
     if has_bwd:
-        cands += [("bwd_dkdv", dkdv_ms, F_fwd * 2, bsrc), ("bwd_dq", dq_ms, F_fwd * 3 // 2, bsrc)]
+        cands += [("bwd_dkdv", dkdv_ms, F_fwd * 2, bsrc), ("bwd_dq", dq_ms, F_fwd // 2, bsrc)]
     dom, dom_ms, dom_flops, srcs = max(cands, key=lambda c: c[1])
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
