@@ -249,61 +249,64 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // Sᵀ, dPᵀ: K-major both
       constexpr uint32_t id_g = idesc_bf16(TILE, D, false, true);      // dV, dK: A TMEM, B MN-major
-      const uint32_t k_base = smem_u32(sK);
-      const uint32_t v_base = smem_u32(sV);
+      static_assert(QST == 2, "descriptor selection assumes two stages");
+      // Descriptors of every operand buffer, built once; each MMA step only
+      // adds a compile-time offset.
+      const uint64_t dK = sdesc_kmajor(smem_u32(sK), 0), dV = sdesc_kmajor(smem_u32(sV), 0);
+      const uint64_t dQk0 = sdesc_kmajor(smem_u32(sQ), 0), dQk1 = sdesc_kmajor(smem_u32(sQ + T::BYTES), 0);
+      const uint64_t dOk0 = sdesc_kmajor(smem_u32(sdO), 0), dOk1 = sdesc_kmajor(smem_u32(sdO + T::BYTES), 0);
+      const uint64_t dQm0 = sdesc_mnmajor(smem_u32(sQ), 0, T::PANEL);
+      const uint64_t dQm1 = sdesc_mnmajor(smem_u32(sQ + T::BYTES), 0, T::PANEL);
+      const uint64_t dOm0 = sdesc_mnmajor(smem_u32(sdO), 0, T::PANEL);
+      const uint64_t dOm1 = sdesc_mnmajor(smem_u32(sdO + T::BYTES), 0, T::PANEL);
       // Sᵀ = K Qᵀ (or dPᵀ = V dOᵀ): 128 keys x 128 queries, K = D.
-      auto issue_kq = [&](uint32_t a_base, uint32_t b_base, uint32_t d_col) {
+      auto issue_kq = [&](uint64_t a, uint64_t b, uint32_t d_col) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t poff = (ks / 4) * T::PANEL;
-          mma_ss(tmem + d_col, sdesc_kmajor(a_base + poff, (ks % 4) * 16),
-                 sdesc_kmajor(b_base + poff, (ks % 4) * 16), id_s, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + d_col, desc_add(a, kmajor_step(ks, T::PANEL)), desc_add(b, kmajor_step(ks, T::PANEL)),
+                 id_s, ks > 0);
+      };
+      // D_col += A(TMEM, 64-query halves at column offsets 0 and 64) · B (MN-major).
+      auto issue_grad = [&](uint32_t d_col, uint32_t a_col, uint64_t b, uint32_t acc0) {
+#pragma unroll
+        for (int ks = 0; ks < TILE / 16; ++ks)
+          mma_ts(tmem + d_col, tmem + a_col + (ks / 4) * 64 + (ks % 4) * 8, desc_add(b, mnmajor_step(ks)),
+                 id_g, ks > 0 ? 1u : acc0);
       };
       bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(&q_full[0], 0, err);
       if (ok) {
         tc_fence_after();
-        issue_kq(k_base, smem_u32(sQ), KV_COL_S);
+        issue_kq(dK, dQk0, KV_COL_S);
         tc_commit(s_full);
-        issue_kq(v_base, smem_u32(sdO), KV_COL_DP);
+        issue_kq(dV, dOk0, KV_COL_DP);
         tc_commit(dp_full);
       }
       for (int i = 0; i < n_it && ok; ++i) {
         const int st = i % QST;
-        const uint32_t q_base = smem_u32(sQ + st * T::BYTES);
-        const uint32_t do_base = smem_u32(sdO + st * T::BYTES);
-        ok = mbar_wait(ds_ready, i & 1, err);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += Pᵀ dO_i: A = Pᵀ in TMEM (bf16; the 64-query halves at column
-        // offsets 0 and 64 of the S columns), B = dO_i MN-major.
-#pragma unroll
-        for (int ks = 0; ks < TILE / 16; ++ks) {
-          const uint32_t acol = (ks / 4) * 64 + (ks % 4) * 8;
-          mma_ts(tmem + KV_COL_DV, tmem + KV_COL_S + acol, sdesc_mnmajor(do_base, ks * 16, T::PANEL),
-                 id_g, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        // Sᵀ_{i+1} overwrites the S columns after the dV product read Pᵀ_i.
-        const bool more = i + 1 < n_it;
         const int s1 = (i + 1) % QST;
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        const bool more = i + 1 < n_it;
+        // The next tile's Q/dO ahead of the wait for this tile's dSᵀ.
         if (more) {
           ok = mbar_wait(&q_full[s1], ((i + 1) / QST) & 1, err);
           if (!ok) break;
-          tc_fence_after();
-          issue_kq(k_base, smem_u32(sQ + s1 * T::BYTES), KV_COL_S);
+        }
+        ok = mbar_wait(ds_ready, i & 1, err);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += Pᵀ dO_i (Pᵀ in the S columns).
+        issue_grad(KV_COL_DV, KV_COL_S, st ? dOm1 : dOm0, acc0);
+        // Sᵀ_{i+1} overwrites the S columns after the dV product read Pᵀ_i.
+        if (more) {
+          issue_kq(dK, s1 ? dQk1 : dQk0, KV_COL_S);
           tc_commit(s_full);
         }
-        // dK += dSᵀ Q_i: A = dSᵀ in TMEM (dP columns), B = Q_i MN-major.
-#pragma unroll
-        for (int ks = 0; ks < TILE / 16; ++ks) {
-          const uint32_t acol = (ks / 4) * 64 + (ks % 4) * 8;
-          mma_ts(tmem + KV_COL_DK, tmem + KV_COL_DP + acol, sdesc_mnmajor(q_base, ks * 16, T::PANEL),
-                 id_g, (i > 0 || ks > 0) ? 1u : 0u);
-        }
+        // dK += dSᵀ Q_i (dSᵀ in the dP columns).
+        issue_grad(KV_COL_DK, KV_COL_DP, st ? dQm1 : dQm0, acc0);
         tc_commit(&q_empty[st]);  // Q_i and dO_i have no further readers
         // dPᵀ_{i+1} overwrites the dP columns after the dK product read dSᵀ_i.
         if (more) {
-          issue_kq(v_base, smem_u32(sdO + s1 * T::BYTES), KV_COL_DP);
+          issue_kq(dV, s1 ? dOk1 : dOk0, KV_COL_DP);
           tc_commit(dp_full);
         }
       }
@@ -442,9 +445,8 @@ struct DqSmem {
   static constexpr int K_OFF = DO_OFF + T::BYTES;
   static constexpr int V_OFF = K_OFF + KST * T::BYTES;
   static constexpr int BAR_OFF = V_OFF + KST * T::BYTES;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], a_ready, s_full,
-  // dp_full, ds_ready, final
-  static constexpr int NBARS = 1 + 4 * KST + 5;
+  // q_full, kv_full[2], kv_empty[2], a_ready, s_full, dp_full, ds_ready, final
+  static constexpr int NBARS = 1 + 2 * KST + 5;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   static constexpr int ALLOC = alloc_for(BYTES);
@@ -469,11 +471,9 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   uint8_t* sV = smem + L::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + KST;
-  uint64_t* v_full = k_empty + KST;
-  uint64_t* v_empty = v_full + KST;
-  uint64_t* a_ready = v_empty + KST;  // Q and dO copied into TMEM
+  uint64_t* kv_full = bars + 1;       // K_j and V_j of one stage
+  uint64_t* kv_empty = kv_full + KST;
+  uint64_t* a_ready = kv_empty + KST;  // Q and dO copied into TMEM
   uint64_t* s_full = a_ready + 1;
   uint64_t* dp_full = s_full + 1;
   uint64_t* ds_ready = dp_full + 1;
@@ -492,10 +492,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < KST; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     mbar_init(a_ready, 8);
     mbar_init(s_full, 1);
@@ -529,82 +527,70 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % KST;
-        const uint32_t ph = ((j / KST) & 1) ^ 1;
-        if (!mbar_wait(&k_empty[s], ph, err)) break;
-        mbar_arrive_expect_tx(&k_full[s], T::BYTES);
-        for (int p = 0; p < T::PANELS; ++p)
-          tma_load_3d(sK + s * T::BYTES + p * T::PANEL, &tk, &k_full[s], p * 64, j * TILE, bh);
-        if (!mbar_wait(&v_empty[s], ph, err)) break;
-        mbar_arrive_expect_tx(&v_full[s], T::BYTES);
-        for (int p = 0; p < T::PANELS; ++p)
-          tma_load_3d(sV + s * T::BYTES + p * T::PANEL, &tv, &v_full[s], p * 64, j * TILE, bh);
+        if (!mbar_wait(&kv_empty[s], ((j / KST) & 1) ^ 1, err)) break;
+        mbar_arrive_expect_tx(&kv_full[s], 2 * T::BYTES);
+        for (int p = 0; p < T::PANELS; ++p) {
+          tma_load_3d(sK + s * T::BYTES + p * T::PANEL, &tk, &kv_full[s], p * 64, j * TILE, bh);
+          tma_load_3d(sV + s * T::BYTES + p * T::PANEL, &tv, &kv_full[s], p * 64, j * TILE, bh);
+        }
         issued = j + 1;
       }
       mbar_wait(q_full, 0, err);
-      for (int j = max(0, issued - KST); j < issued; ++j) {
-        mbar_wait(&k_full[j % KST], (j / KST) & 1, err);
-        mbar_wait(&v_full[j % KST], (j / KST) & 1, err);
-      }
+      for (int j = max(0, issued - KST); j < issued; ++j)
+        mbar_wait(&kv_full[j % KST], (j / KST) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // S, dP: A TMEM, B K-major
       constexpr uint32_t id_q = idesc_bf16(TILE, D, false, true);      // dQ: A TMEM, B MN-major
+      static_assert(KST == 2, "descriptor selection assumes two stages");
+      const uint64_t dKk0 = sdesc_kmajor(smem_u32(sK), 0), dKk1 = sdesc_kmajor(smem_u32(sK + T::BYTES), 0);
+      const uint64_t dVk0 = sdesc_kmajor(smem_u32(sV), 0), dVk1 = sdesc_kmajor(smem_u32(sV + T::BYTES), 0);
+      const uint64_t dKm0 = sdesc_mnmajor(smem_u32(sK), 0, T::PANEL);
+      const uint64_t dKm1 = sdesc_mnmajor(smem_u32(sK + T::BYTES), 0, T::PANEL);
       // S = Q Kⱼᵀ (or dP = dO Vⱼᵀ): A = Q (dO) in TMEM, B = Kⱼ (Vⱼ) K-major.
-      auto issue_ab = [&](uint32_t a_col, uint32_t b_base, uint32_t d_col) {
+      auto issue_ab = [&](uint32_t a_col, uint64_t b, uint32_t d_col) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          mma_ts(tmem + d_col, tmem + a_col + ks * 8,
-                 sdesc_kmajor(b_base + (ks / 4) * T::PANEL, (ks % 4) * 16), id_s, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ts(tmem + d_col, tmem + a_col + ks * 8, desc_add(b, kmajor_step(ks, T::PANEL)), id_s, ks > 0);
       };
-      bool ok = mbar_wait(a_ready, 0, err) && mbar_wait(&k_full[0], 0, err);
+      bool ok = mbar_wait(a_ready, 0, err) && mbar_wait(&kv_full[0], 0, err);
       if (ok) {
         tc_fence_after();
-        issue_ab(Q_COL_Q, smem_u32(sK), Q_COL_S);
+        issue_ab(Q_COL_Q, dKk0, Q_COL_S);
         tc_commit(s_full);
-        ok = mbar_wait(&v_full[0], 0, err);
-        if (ok) {
-          tc_fence_after();
-          issue_ab(Q_COL_DO, smem_u32(sV), Q_COL_DP);
-          tc_commit(dp_full);
-          tc_commit(&v_empty[0]);
-        }
+        issue_ab(Q_COL_DO, dVk0, Q_COL_DP);
+        tc_commit(dp_full);
       }
       for (int j = 0; j < n_kv && ok; ++j) {
         const int s = j % KST;
+        const int s1 = (j + 1) % KST;
+        const bool more = j + 1 < n_kv;
+        if (more) {
+          ok = mbar_wait(&kv_full[s1], ((j + 1) / KST) & 1, err);
+          if (!ok) break;
+        }
         ok = mbar_wait(ds_ready, j & 1, err);
         if (!ok) break;
         tc_fence_after();
-        const bool more = j + 1 < n_kv;
-        const int s1 = (j + 1) % KST;
         // S_{j+1}: the compute warps have read S_j (ds_ready).
         if (more) {
-          ok = mbar_wait(&k_full[s1], ((j + 1) / KST) & 1, err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_ab(Q_COL_Q, smem_u32(sK + s1 * T::BYTES), Q_COL_S);
+          issue_ab(Q_COL_Q, s1 ? dKk1 : dKk0, Q_COL_S);
           tc_commit(s_full);
         }
         // dQ += dS_j Kⱼ: A = dS in TMEM (bf16 in the dP columns, halves at
         // offsets 0 and 64), B = Kⱼ MN-major.
-        const uint32_t kb = smem_u32(sK + s * T::BYTES);
+        const uint64_t bk = s ? dKm1 : dKm0;
 #pragma unroll
-        for (int ks = 0; ks < TILE / 16; ++ks) {
-          const uint32_t acol = (ks / 4) * 64 + (ks % 4) * 8;
-          mma_ts(tmem + Q_COL_DQ, tmem + Q_COL_DP + acol, sdesc_mnmajor(kb, ks * 16, T::PANEL), id_q,
-                 (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        tc_commit(&k_empty[s]);
+        for (int ks = 0; ks < TILE / 16; ++ks)
+          mma_ts(tmem + Q_COL_DQ, tmem + Q_COL_DP + (ks / 4) * 64 + (ks % 4) * 8,
+                 desc_add(bk, mnmajor_step(ks)), id_q, (j > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(&kv_empty[s]);  // K_j (S_j, dQ_j) and V_j (dP_j) are free
         // dP_{j+1} overwrites the dP columns after the dQ product read dS_j.
         if (more) {
-          ok = mbar_wait(&v_full[s1], ((j + 1) / KST) & 1, err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_ab(Q_COL_DO, smem_u32(sV + s1 * T::BYTES), Q_COL_DP);
+          issue_ab(Q_COL_DO, s1 ? dVk1 : dVk0, Q_COL_DP);
           tc_commit(dp_full);
-          tc_commit(&v_empty[s1]);
         }
       }
       tc_commit(final_bar);

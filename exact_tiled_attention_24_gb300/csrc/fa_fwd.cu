@@ -13,7 +13,7 @@
 // key/value tiles once for both ("ping-pong"): while one softmax group
 // exponentiates its S tile, the tensor core runs the other group's products.
 // Roles (320 threads):
-//   warp 0      TMA producer: Q0, Q1 once, then K_j / V_j into 2-stage rings
+//   warp 0      TMA producer: Q0, Q1 once, then (K_j, V_j) into a 2-stage ring
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..5  softmax group 0 (Q0), one thread per query row (TMEM lane)
 //   warps 6..9  softmax group 1 (Q1)
@@ -60,9 +60,8 @@ struct Smem {
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  // p_ready[2], pv_done[2], final
-  static constexpr int NBARS = 1 + 4 * STAGES + 6 + 1;
+  // q_full, kv_full[2], kv_empty[2], s_full[2], p_ready[2], pv_done[2], final
+  static constexpr int NBARS = 1 + 2 * STAGES + 6 + 1;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   // Slack for 1024-byte alignment; at least 116 KB so that only one CTA
@@ -84,11 +83,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sV = smem + L::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + L::STAGES;
-  uint64_t* v_full = k_empty + L::STAGES;
-  uint64_t* v_empty = v_full + L::STAGES;
-  uint64_t* s_full = v_empty + L::STAGES;   // [2], one per group
+  uint64_t* kv_full = bars + 1;             // K_j and V_j of one stage
+  uint64_t* kv_empty = kv_full + L::STAGES;
+  uint64_t* s_full = kv_empty + L::STAGES;  // [2], one per group
   uint64_t* p_ready = s_full + 2;           // [2]
   uint64_t* pv_done = p_ready + 2;          // [2]
   uint64_t* final_bar = pv_done + 2;
@@ -113,10 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&s_full[g], 1);
@@ -147,71 +142,65 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int p = 0; p < L::PANELS; ++p)
           tma_load_3d(sQ + g * L::TILE_BYTES + p * L::PANEL, &tq, q_full, p * 64, qrow0 + g * BM, bh);
       int issued = 0;
-      bool ok = true;
-      for (int j = 0; j < n_kt && ok; ++j) {
+      for (int j = 0; j < n_kt; ++j) {
         const int s = j % L::STAGES;
-        const uint32_t ph = ((j / L::STAGES) & 1) ^ 1;
-        ok = mbar_wait(&k_empty[s], ph, err);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&k_full[s], L::TILE_BYTES);
-        for (int p = 0; p < L::PANELS; ++p)
-          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &k_full[s], p * 64, j * BN, bh);
-        ok = mbar_wait(&v_empty[s], ph, err);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&v_full[s], L::TILE_BYTES);
-        for (int p = 0; p < L::PANELS; ++p)
-          tma_load_3d(sV + s * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[s], p * 64, j * BN, bh);
+        if (!mbar_wait(&kv_empty[s], ((j / L::STAGES) & 1) ^ 1, err)) break;
+        mbar_arrive_expect_tx(&kv_full[s], 2 * L::TILE_BYTES);
+        for (int p = 0; p < L::PANELS; ++p) {
+          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &kv_full[s], p * 64, j * BN, bh);
+          tma_load_3d(sV + s * L::TILE_BYTES + p * L::PANEL, &tv, &kv_full[s], p * 64, j * BN, bh);
+        }
         issued = j + 1;
       }
       // Drain: never leave the CTA with copies still landing in its smem.
       mbar_wait(q_full, 0, err);
-      for (int j = max(0, issued - L::STAGES); j < issued; ++j) {
-        const int s = j % L::STAGES;
-        const uint32_t ph = (j / L::STAGES) & 1;
-        mbar_wait(&k_full[s], ph, err);
-        mbar_wait(&v_full[s], ph, err);
-      }
+      for (int j = max(0, issued - L::STAGES); j < issued; ++j)
+        mbar_wait(&kv_full[j % L::STAGES], (j / L::STAGES) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
-      // S_g = Q_g K_jᵀ into the S columns of group g.
-      auto issue_s = [&](int g, int j) {
-        const uint32_t q_base = smem_u32(sQ + g * L::TILE_BYTES);
-        const uint32_t k_base = smem_u32(sK + (j % L::STAGES) * L::TILE_BYTES);
+      // Descriptors of every operand buffer, built once (kept in registers:
+      // selected by value, never indexed).
+      static_assert(L::STAGES == 2, "descriptor selection assumes two stages");
+      const uint64_t dq0 = sdesc_kmajor(smem_u32(sQ), 0);
+      const uint64_t dq1 = sdesc_kmajor(smem_u32(sQ + L::TILE_BYTES), 0);
+      const uint64_t dk0 = sdesc_kmajor(smem_u32(sK), 0);
+      const uint64_t dk1 = sdesc_kmajor(smem_u32(sK + L::TILE_BYTES), 0);
+      const uint64_t dv0 = sdesc_mnmajor(smem_u32(sV), 0, L::PANEL);
+      const uint64_t dv1 = sdesc_mnmajor(smem_u32(sV + L::TILE_BYTES), 0, L::PANEL);
+      // S_g = Q_g K_jᵀ into the S columns of group g (K_j in stage s).
+      auto issue_s = [&](int g, int s) {
+        const uint64_t a = g ? dq1 : dq0, b = s ? dk1 : dk0;
+        const uint32_t d = tmem + g * BN;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t poff = (ks / 4) * L::PANEL;
-          mma_ss(tmem + g * BN, sdesc_kmajor(q_base + poff, (ks % 4) * 16),
-                 sdesc_kmajor(k_base + poff, (ks % 4) * 16), idesc_s, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(d, desc_add(a, kmajor_step(ks, L::PANEL)), desc_add(b, kmajor_step(ks, L::PANEL)),
+                 idesc_s, ks > 0);
         tc_commit(&s_full[g]);
       };
       // O_g += P_g V_j; P_g is bf16 in the first 64 S columns of group g.
-      auto issue_pv = [&](int g, int j) {
-        const uint32_t v_base = smem_u32(sV + (j % L::STAGES) * L::TILE_BYTES);
+      auto issue_pv = [&](int g, int s, uint32_t acc0) {
+        const uint64_t b = s ? dv1 : dv0;
+        const uint32_t d = tmem + 256 + g * 128;
+        const uint32_t a = tmem + g * BN;
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          mma_ts(tmem + 256 + g * 128, tmem + g * BN + ks * 8, sdesc_mnmajor(v_base, ks * 16, L::PANEL),
-                 idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ts(d, a + ks * 8, desc_add(b, mnmajor_step(ks)), idesc_o, ks > 0 ? 1u : acc0);
         tc_commit(&pv_done[g]);
       };
-      bool ok = mbar_wait(q_full, 0, err) && mbar_wait(&k_full[0], 0, err);
+      bool ok = mbar_wait(q_full, 0, err) && mbar_wait(&kv_full[0], 0, err);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         issue_s(1, 0);
-        tc_commit(&k_empty[0]);
       }
       for (int j = 0; j < n_kt && ok; ++j) {
         const int s = j % L::STAGES;
         const int s1 = (j + 1) % L::STAGES;
-        ok = mbar_wait(&v_full[s], (j / L::STAGES) & 1, err);
-        if (!ok) break;
-        bool k_next_ready = false;
+        bool next_ready = false;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const int n_g = (g == 0) ? n_g0 : n_g1;
@@ -219,20 +208,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = mbar_wait(&p_ready[g], j & 1, err);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(g, j);
+          issue_pv(g, s, j > 0 ? 1u : 0u);
           if (j + 1 < n_g) {
-            if (!k_next_ready) {
-              ok = mbar_wait(&k_full[s1], ((j + 1) / L::STAGES) & 1, err);
+            if (!next_ready) {
+              ok = mbar_wait(&kv_full[s1], ((j + 1) / L::STAGES) & 1, err);
               if (!ok) break;
               tc_fence_after();
-              k_next_ready = true;
+              next_ready = true;
             }
-            issue_s(g, j + 1);
+            issue_s(g, s1);
           }
         }
         if (!ok) break;
-        tc_commit(&v_empty[s]);
-        if (k_next_ready) tc_commit(&k_empty[s1]);
+        tc_commit(&kv_empty[s]);  // K_j (read by S_j) and V_j (read by PV_j) are free
       }
       tc_commit(final_bar);
       mbar_wait(final_bar, 0, err);

@@ -255,6 +255,22 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor(uint32_t base, uint32_t k0, ui
   return sdesc_sw128(base + k0 * 128u, panel_stride, 1024u);
 }
 
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple
+// of 16). Descriptors are built once per buffer and advanced by
+// compile-time offsets per MMA step: the issuing thread then spends almost
+// no time between MMAs (the tensor core buffers only ~100 cycles of issued
+// work, so issue overhead turns directly into idle tensor time).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+// Offset of K step ks (16 elements) of a K-major operand stored as 64-column
+// panels `panel_bytes` apart.
+__host__ __device__ constexpr uint32_t kmajor_step(int ks, uint32_t panel_bytes) {
+  return static_cast<uint32_t>(ks / 4) * panel_bytes + static_cast<uint32_t>(ks % 4) * 32u;
+}
+// Offset of K step ks of an MN-major operand (two 8-row groups per step).
+__host__ __device__ constexpr uint32_t mnmajor_step(int ks) { return static_cast<uint32_t>(ks) * 2048u; }
+
 // TMEM load: 32 lanes x 32 bits, N consecutive columns per thread.
 #define FA_TMEM_LD_X16(taddr, r)                                                               \
   asm volatile(                                                                                \
