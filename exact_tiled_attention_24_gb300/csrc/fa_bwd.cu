@@ -246,73 +246,72 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // Sᵀ, dPᵀ: K-major both
-      constexpr uint32_t id_g = idesc_bf16(TILE, D, false, true);      // dV, dK: A TMEM, B MN-major
-      static_assert(QST == 2, "descriptor selection assumes two stages");
-      // Descriptors of every operand buffer, built once; each MMA step only
-      // adds a compile-time offset.
-      const uint64_t dK = sdesc_kmajor(smem_u32(sK), 0), dV = sdesc_kmajor(smem_u32(sV), 0);
-      const uint64_t dQk0 = sdesc_kmajor(smem_u32(sQ), 0), dQk1 = sdesc_kmajor(smem_u32(sQ + T::BYTES), 0);
-      const uint64_t dOk0 = sdesc_kmajor(smem_u32(sdO), 0), dOk1 = sdesc_kmajor(smem_u32(sdO + T::BYTES), 0);
-      const uint64_t dQm0 = sdesc_mnmajor(smem_u32(sQ), 0, T::PANEL);
-      const uint64_t dQm1 = sdesc_mnmajor(smem_u32(sQ + T::BYTES), 0, T::PANEL);
-      const uint64_t dOm0 = sdesc_mnmajor(smem_u32(sdO), 0, T::PANEL);
-      const uint64_t dOm1 = sdesc_mnmajor(smem_u32(sdO + T::BYTES), 0, T::PANEL);
-      // Sᵀ = K Qᵀ (or dPᵀ = V dOᵀ): 128 keys x 128 queries, K = D.
-      auto issue_kq = [&](uint64_t a, uint64_t b, uint32_t d_col) {
+    // Whole warp runs the loop (warp-uniform descriptors); one elected lane
+    // issues MMAs and commits.
+    constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // Sᵀ, dPᵀ: K-major both
+    constexpr uint32_t id_g = idesc_bf16(TILE, D, false, true);      // dV, dK: A TMEM, B MN-major
+    static_assert(QST == 2, "descriptor selection assumes two stages");
+    const uint64_t dK = sdesc_kmajor(smem_u32(sK), 0), dV = sdesc_kmajor(smem_u32(sV), 0);
+    const uint64_t dQk0 = sdesc_kmajor(smem_u32(sQ), 0), dQk1 = sdesc_kmajor(smem_u32(sQ + T::BYTES), 0);
+    const uint64_t dOk0 = sdesc_kmajor(smem_u32(sdO), 0), dOk1 = sdesc_kmajor(smem_u32(sdO + T::BYTES), 0);
+    const uint64_t dQm0 = sdesc_mnmajor(smem_u32(sQ), 0, T::PANEL);
+    const uint64_t dQm1 = sdesc_mnmajor(smem_u32(sQ + T::BYTES), 0, T::PANEL);
+    const uint64_t dOm0 = sdesc_mnmajor(smem_u32(sdO), 0, T::PANEL);
+    const uint64_t dOm1 = sdesc_mnmajor(smem_u32(sdO + T::BYTES), 0, T::PANEL);
+    // Sᵀ = K Qᵀ (or dPᵀ = V dOᵀ): 128 keys x 128 queries, K = D; then commit.
+    auto issue_kq = [&](uint64_t a, uint64_t b, uint32_t d_col, uint64_t* bar) {
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_ss(tmem + d_col, desc_add(a, kmajor_step(ks, T::PANEL)), desc_add(b, kmajor_step(ks, T::PANEL)),
                  id_s, ks > 0);
-      };
-      // D_col += A(TMEM, 64-query halves at column offsets 0 and 64) · B (MN-major).
-      auto issue_grad = [&](uint32_t d_col, uint32_t a_col, uint64_t b, uint32_t acc0) {
+        tc_commit(bar);
+      }
+      __syncwarp();
+    };
+    // D_col += A(TMEM, 64-query halves at column offsets 0 and 64) · B (MN-major).
+    auto issue_grad = [&](uint32_t d_col, uint32_t a_col, uint64_t b, uint32_t acc0, uint64_t* bar) {
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < TILE / 16; ++ks)
           mma_ts(tmem + d_col, tmem + a_col + (ks / 4) * 64 + (ks % 4) * 8, desc_add(b, mnmajor_step(ks)),
                  id_g, ks > 0 ? 1u : acc0);
-      };
-      bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(&q_full[0], 0, err);
-      if (ok) {
-        tc_fence_after();
-        issue_kq(dK, dQk0, KV_COL_S);
-        tc_commit(s_full);
-        issue_kq(dV, dOk0, KV_COL_DP);
-        tc_commit(dp_full);
+        if (bar != nullptr) tc_commit(bar);
       }
-      for (int i = 0; i < n_it && ok; ++i) {
-        const int st = i % QST;
-        const int s1 = (i + 1) % QST;
-        const uint32_t acc0 = i > 0 ? 1u : 0u;
-        const bool more = i + 1 < n_it;
-        // The next tile's Q/dO ahead of the wait for this tile's dSᵀ.
-        if (more) {
-          ok = mbar_wait(&q_full[s1], ((i + 1) / QST) & 1, err);
-          if (!ok) break;
-        }
-        ok = mbar_wait(ds_ready, i & 1, err);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += Pᵀ dO_i (Pᵀ in the S columns).
-        issue_grad(KV_COL_DV, KV_COL_S, st ? dOm1 : dOm0, acc0);
-        // Sᵀ_{i+1} overwrites the S columns after the dV product read Pᵀ_i.
-        if (more) {
-          issue_kq(dK, s1 ? dQk1 : dQk0, KV_COL_S);
-          tc_commit(s_full);
-        }
-        // dK += dSᵀ Q_i (dSᵀ in the dP columns).
-        issue_grad(KV_COL_DK, KV_COL_DP, st ? dQm1 : dQm0, acc0);
-        tc_commit(&q_empty[st]);  // Q_i and dO_i have no further readers
-        // dPᵀ_{i+1} overwrites the dP columns after the dK product read dSᵀ_i.
-        if (more) {
-          issue_kq(dV, s1 ? dOk1 : dOk0, KV_COL_DP);
-          tc_commit(dp_full);
-        }
-      }
-      tc_commit(final_bar);
-      mbar_wait(final_bar, 0, err);
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(kv_full, 0, err) && mbar_wait_warp(&q_full[0], 0, err);
+    if (ok) {
+      tc_fence_after();
+      issue_kq(dK, dQk0, KV_COL_S, s_full);
+      issue_kq(dV, dOk0, KV_COL_DP, dp_full);
     }
+    for (int i = 0; i < n_it && ok; ++i) {
+      const int st = i % QST;
+      const int s1 = (i + 1) % QST;
+      const uint32_t acc0 = i > 0 ? 1u : 0u;
+      const bool more = i + 1 < n_it;
+      // The next tile's Q/dO ahead of the wait for this tile's dSᵀ.
+      if (more) {
+        ok = mbar_wait_warp(&q_full[s1], ((i + 1) / QST) & 1, err);
+        if (!ok) break;
+      }
+      ok = mbar_wait_warp(ds_ready, i & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      // dV += Pᵀ dO_i (Pᵀ in the S columns).
+      issue_grad(KV_COL_DV, KV_COL_S, st ? dOm1 : dOm0, acc0, nullptr);
+      // Sᵀ_{i+1} overwrites the S columns after the dV product read Pᵀ_i.
+      if (more) issue_kq(dK, s1 ? dQk1 : dQk0, KV_COL_S, s_full);
+      // dK += dSᵀ Q_i (dSᵀ in the dP columns); Q_i and dO_i then have no
+      // further readers.
+      issue_grad(KV_COL_DK, KV_COL_DP, st ? dQm1 : dQm0, acc0, &q_empty[st]);
+      // dPᵀ_{i+1} overwrites the dP columns after the dK product read dSᵀ_i.
+      if (more) issue_kq(dV, s1 ? dOk1 : dOk0, KV_COL_DP, dp_full);
+    }
+    if (elect_one()) tc_commit(final_bar);
+    __syncwarp();
+    mbar_wait_warp(final_bar, 0, err);
   } else {
     // ------------------------------------------------------------ compute
     // Warps 2..9: two warps per TMEM lane quarter; warp half h owns query
@@ -541,61 +540,61 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // S, dP: A TMEM, B K-major
-      constexpr uint32_t id_q = idesc_bf16(TILE, D, false, true);      // dQ: A TMEM, B MN-major
-      static_assert(KST == 2, "descriptor selection assumes two stages");
-      const uint64_t dKk0 = sdesc_kmajor(smem_u32(sK), 0), dKk1 = sdesc_kmajor(smem_u32(sK + T::BYTES), 0);
-      const uint64_t dVk0 = sdesc_kmajor(smem_u32(sV), 0), dVk1 = sdesc_kmajor(smem_u32(sV + T::BYTES), 0);
-      const uint64_t dKm0 = sdesc_mnmajor(smem_u32(sK), 0, T::PANEL);
-      const uint64_t dKm1 = sdesc_mnmajor(smem_u32(sK + T::BYTES), 0, T::PANEL);
-      // S = Q Kⱼᵀ (or dP = dO Vⱼᵀ): A = Q (dO) in TMEM, B = Kⱼ (Vⱼ) K-major.
-      auto issue_ab = [&](uint32_t a_col, uint64_t b, uint32_t d_col) {
+    // Whole warp runs the loop (warp-uniform descriptors); one elected lane
+    // issues MMAs and commits.
+    constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // S, dP: A TMEM, B K-major
+    constexpr uint32_t id_q = idesc_bf16(TILE, D, false, true);      // dQ: A TMEM, B MN-major
+    static_assert(KST == 2, "descriptor selection assumes two stages");
+    const uint64_t dKk0 = sdesc_kmajor(smem_u32(sK), 0), dKk1 = sdesc_kmajor(smem_u32(sK + T::BYTES), 0);
+    const uint64_t dVk0 = sdesc_kmajor(smem_u32(sV), 0), dVk1 = sdesc_kmajor(smem_u32(sV + T::BYTES), 0);
+    const uint64_t dKm0 = sdesc_mnmajor(smem_u32(sK), 0, T::PANEL);
+    const uint64_t dKm1 = sdesc_mnmajor(smem_u32(sK + T::BYTES), 0, T::PANEL);
+    // S = Q Kⱼᵀ (or dP = dO Vⱼᵀ): A = Q (dO) in TMEM, B = Kⱼ (Vⱼ) K-major.
+    auto issue_ab = [&](uint32_t a_col, uint64_t b, uint32_t d_col, uint64_t* bar) {
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_ts(tmem + d_col, tmem + a_col + ks * 8, desc_add(b, kmajor_step(ks, T::PANEL)), id_s, ks > 0);
-      };
-      bool ok = mbar_wait(a_ready, 0, err) && mbar_wait(&kv_full[0], 0, err);
-      if (ok) {
-        tc_fence_after();
-        issue_ab(Q_COL_Q, dKk0, Q_COL_S);
-        tc_commit(s_full);
-        issue_ab(Q_COL_DO, dVk0, Q_COL_DP);
-        tc_commit(dp_full);
+        tc_commit(bar);
       }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % KST;
-        const int s1 = (j + 1) % KST;
-        const bool more = j + 1 < n_kv;
-        if (more) {
-          ok = mbar_wait(&kv_full[s1], ((j + 1) / KST) & 1, err);
-          if (!ok) break;
-        }
-        ok = mbar_wait(ds_ready, j & 1, err);
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(a_ready, 0, err) && mbar_wait_warp(&kv_full[0], 0, err);
+    if (ok) {
+      tc_fence_after();
+      issue_ab(Q_COL_Q, dKk0, Q_COL_S, s_full);
+      issue_ab(Q_COL_DO, dVk0, Q_COL_DP, dp_full);
+    }
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int s = j % KST;
+      const int s1 = (j + 1) % KST;
+      const bool more = j + 1 < n_kv;
+      if (more) {
+        ok = mbar_wait_warp(&kv_full[s1], ((j + 1) / KST) & 1, err);
         if (!ok) break;
-        tc_fence_after();
-        // S_{j+1}: the compute warps have read S_j (ds_ready).
-        if (more) {
-          issue_ab(Q_COL_Q, s1 ? dKk1 : dKk0, Q_COL_S);
-          tc_commit(s_full);
-        }
-        // dQ += dS_j Kⱼ: A = dS in TMEM (bf16 in the dP columns, halves at
-        // offsets 0 and 64), B = Kⱼ MN-major.
-        const uint64_t bk = s ? dKm1 : dKm0;
+      }
+      ok = mbar_wait_warp(ds_ready, j & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      // S_{j+1}: the compute warps have read S_j (ds_ready).
+      if (more) issue_ab(Q_COL_Q, s1 ? dKk1 : dKk0, Q_COL_S, s_full);
+      // dQ += dS_j Kⱼ: A = dS in TMEM (bf16 in the dP columns, halves at
+      // offsets 0 and 64), B = Kⱼ MN-major; then K_j and V_j are free.
+      const uint64_t bk = s ? dKm1 : dKm0;
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < TILE / 16; ++ks)
           mma_ts(tmem + Q_COL_DQ, tmem + Q_COL_DP + (ks / 4) * 64 + (ks % 4) * 8,
                  desc_add(bk, mnmajor_step(ks)), id_q, (j > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(&kv_empty[s]);  // K_j (S_j, dQ_j) and V_j (dP_j) are free
-        // dP_{j+1} overwrites the dP columns after the dQ product read dS_j.
-        if (more) {
-          issue_ab(Q_COL_DO, s1 ? dVk1 : dVk0, Q_COL_DP);
-          tc_commit(dp_full);
-        }
+        tc_commit(&kv_empty[s]);
       }
-      tc_commit(final_bar);
-      mbar_wait(final_bar, 0, err);
+      __syncwarp();
+      // dP_{j+1} overwrites the dP columns after the dQ product read dS_j.
+      if (more) issue_ab(Q_COL_DO, s1 ? dVk1 : dVk0, Q_COL_DP, dp_full);
     }
+    if (elect_one()) tc_commit(final_bar);
+    __syncwarp();
+    mbar_wait_warp(final_bar, 0, err);
   } else {
     // ------------------------------------------------------------ compute
     // Warps 2..9: thread = query row r (TMEM lane); warp half h owns key

@@ -13,8 +13,8 @@
 // key/value tiles once for both ("ping-pong"): while one softmax group
 // exponentiates its S tile, the tensor core runs the other group's products.
 // Roles (320 threads):
-//   warp 0      TMA producer: Q0, Q1 once, then (K_j, V_j) into a 2-stage ring
-//   warp 1      TMEM owner and MMA issuer (one lane)
+//   warp 0      TMA producer: Q0, Q1 once, then K_j and V_j into 2-stage rings
+//   warp 1      TMEM owner and MMA issuer (warp-uniform, one elected lane issues)
 //   warps 2..5  softmax group 0 (Q0), one thread per query row (TMEM lane)
 //   warps 6..9  softmax group 1 (Q1)
 // TMEM columns: S0 0.., S1 128.., O0 256.., O1 384... The MMA order is
@@ -60,8 +60,9 @@ struct Smem {
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-  // q_full, kv_full[2], kv_empty[2], s_full[2], p_ready[2], pv_done[2], final
-  static constexpr int NBARS = 1 + 2 * STAGES + 6 + 1;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
+  // p_ready[2], pv_done[2], final
+  static constexpr int NBARS = 1 + 4 * STAGES + 6 + 1;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   // Slack for 1024-byte alignment; at least 116 KB so that only one CTA
@@ -83,9 +84,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sV = smem + L::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;             // K_j and V_j of one stage
-  uint64_t* kv_empty = kv_full + L::STAGES;
-  uint64_t* s_full = kv_empty + L::STAGES;  // [2], one per group
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + L::STAGES;
+  uint64_t* v_full = k_empty + L::STAGES;
+  uint64_t* v_empty = v_full + L::STAGES;
+  uint64_t* s_full = v_empty + L::STAGES;   // [2], one per group
   uint64_t* p_ready = s_full + 2;           // [2]
   uint64_t* pv_done = p_ready + 2;          // [2]
   uint64_t* final_bar = pv_done + 2;
@@ -110,8 +113,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&s_full[g], 1);
@@ -141,90 +146,125 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int g = 0; g < 2; ++g)
         for (int p = 0; p < L::PANELS; ++p)
           tma_load_3d(sQ + g * L::TILE_BYTES + p * L::PANEL, &tq, q_full, p * 64, qrow0 + g * BM, bh);
-      int issued = 0;
+      // K_j is read only by the S products and its stage is released right
+      // after them; V_j is released after the P·V products. K loads therefore
+      // run ahead of V loads.
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kt; ++j) {
         const int s = j % L::STAGES;
-        if (!mbar_wait(&kv_empty[s], ((j / L::STAGES) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * L::TILE_BYTES);
-        for (int p = 0; p < L::PANELS; ++p) {
-          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &kv_full[s], p * 64, j * BN, bh);
-          tma_load_3d(sV + s * L::TILE_BYTES + p * L::PANEL, &tv, &kv_full[s], p * 64, j * BN, bh);
+        const uint32_t ph = ((j / L::STAGES) & 1) ^ 1;
+        if (!mbar_wait(&k_empty[s], ph, err)) break;
+        mbar_arrive_expect_tx(&k_full[s], L::TILE_BYTES);
+        for (int p = 0; p < L::PANELS; ++p)
+          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &k_full[s], p * 64, j * BN, bh);
+        k_issued = j + 1;
+        // V_{j-1} after K_j: V is needed one softmax later than K.
+        if (j >= 1) {
+          const int jv = j - 1, sv = jv % L::STAGES;
+          if (!mbar_wait(&v_empty[sv], ((jv / L::STAGES) & 1) ^ 1, err)) break;
+          mbar_arrive_expect_tx(&v_full[sv], L::TILE_BYTES);
+          for (int p = 0; p < L::PANELS; ++p)
+            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bh);
+          v_issued = jv + 1;
         }
-        issued = j + 1;
+      }
+      if (v_issued == n_kt - 1 && k_issued == n_kt) {
+        const int jv = n_kt - 1, sv = jv % L::STAGES;
+        if (mbar_wait(&v_empty[sv], ((jv / L::STAGES) & 1) ^ 1, err)) {
+          mbar_arrive_expect_tx(&v_full[sv], L::TILE_BYTES);
+          for (int p = 0; p < L::PANELS; ++p)
+            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bh);
+          v_issued = n_kt;
+        }
       }
       // Drain: never leave the CTA with copies still landing in its smem.
       mbar_wait(q_full, 0, err);
-      for (int j = max(0, issued - L::STAGES); j < issued; ++j)
-        mbar_wait(&kv_full[j % L::STAGES], (j / L::STAGES) & 1, err);
+      for (int j = max(0, k_issued - L::STAGES); j < k_issued; ++j)
+        mbar_wait(&k_full[j % L::STAGES], (j / L::STAGES) & 1, err);
+      for (int j = max(0, v_issued - L::STAGES); j < v_issued; ++j)
+        mbar_wait(&v_full[j % L::STAGES], (j / L::STAGES) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
-      // Descriptors of every operand buffer, built once (kept in registers:
-      // selected by value, never indexed).
-      static_assert(L::STAGES == 2, "descriptor selection assumes two stages");
-      const uint64_t dq0 = sdesc_kmajor(smem_u32(sQ), 0);
-      const uint64_t dq1 = sdesc_kmajor(smem_u32(sQ + L::TILE_BYTES), 0);
-      const uint64_t dk0 = sdesc_kmajor(smem_u32(sK), 0);
-      const uint64_t dk1 = sdesc_kmajor(smem_u32(sK + L::TILE_BYTES), 0);
-      const uint64_t dv0 = sdesc_mnmajor(smem_u32(sV), 0, L::PANEL);
-      const uint64_t dv1 = sdesc_mnmajor(smem_u32(sV + L::TILE_BYTES), 0, L::PANEL);
-      // S_g = Q_g K_jᵀ into the S columns of group g (K_j in stage s).
-      auto issue_s = [&](int g, int s) {
-        const uint64_t a = g ? dq1 : dq0, b = s ? dk1 : dk0;
-        const uint32_t d = tmem + g * BN;
+    // The whole warp runs this loop (descriptors stay warp-uniform, so the
+    // per-MMA work is cheap even while the softmax warps saturate the issue
+    // slots); one elected lane issues the MMAs and commits.
+    constexpr uint32_t idesc_s = idesc_bf16(BM, BN, false, false);
+    constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
+    static_assert(L::STAGES == 2, "descriptor selection assumes two stages");
+    const uint64_t dq0 = sdesc_kmajor(smem_u32(sQ), 0);
+    const uint64_t dq1 = sdesc_kmajor(smem_u32(sQ + L::TILE_BYTES), 0);
+    const uint64_t dk0 = sdesc_kmajor(smem_u32(sK), 0);
+    const uint64_t dk1 = sdesc_kmajor(smem_u32(sK + L::TILE_BYTES), 0);
+    const uint64_t dv0 = sdesc_mnmajor(smem_u32(sV), 0, L::PANEL);
+    const uint64_t dv1 = sdesc_mnmajor(smem_u32(sV + L::TILE_BYTES), 0, L::PANEL);
+    // S_g = Q_g K_jᵀ into the S columns of group g (K_j in stage s).
+    auto issue_s = [&](int g, int s) {
+      const uint64_t a = g ? dq1 : dq0, b = s ? dk1 : dk0;
+      const uint32_t d = tmem + g * BN;
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_ss(d, desc_add(a, kmajor_step(ks, L::PANEL)), desc_add(b, kmajor_step(ks, L::PANEL)),
                  idesc_s, ks > 0);
         tc_commit(&s_full[g]);
-      };
-      // O_g += P_g V_j; P_g is bf16 in the first 64 S columns of group g.
-      auto issue_pv = [&](int g, int s, uint32_t acc0) {
-        const uint64_t b = s ? dv1 : dv0;
-        const uint32_t d = tmem + 256 + g * 128;
-        const uint32_t a = tmem + g * BN;
+      }
+      __syncwarp();
+    };
+    // O_g += P_g V_j; P_g is bf16 in the first 64 S columns of group g.
+    auto issue_pv = [&](int g, int s, uint32_t acc0) {
+      const uint64_t b = s ? dv1 : dv0;
+      const uint32_t d = tmem + 256 + g * 128;
+      const uint32_t a = tmem + g * BN;
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
           mma_ts(d, a + ks * 8, desc_add(b, mnmajor_step(ks)), idesc_o, ks > 0 ? 1u : acc0);
         tc_commit(&pv_done[g]);
-      };
-      bool ok = mbar_wait(q_full, 0, err) && mbar_wait(&kv_full[0], 0, err);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
       }
-      for (int j = 0; j < n_kt && ok; ++j) {
-        const int s = j % L::STAGES;
-        const int s1 = (j + 1) % L::STAGES;
-        bool next_ready = false;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const int n_g = (g == 0) ? n_g0 : n_g1;
-          if (j >= n_g) continue;
-          ok = mbar_wait(&p_ready[g], j & 1, err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(g, s, j > 0 ? 1u : 0u);
-          if (j + 1 < n_g) {
-            if (!next_ready) {
-              ok = mbar_wait(&kv_full[s1], ((j + 1) / L::STAGES) & 1, err);
-              if (!ok) break;
-              tc_fence_after();
-              next_ready = true;
-            }
-            issue_s(g, s1);
-          }
-        }
-        if (!ok) break;
-        tc_commit(&kv_empty[s]);  // K_j (read by S_j) and V_j (read by PV_j) are free
-      }
-      tc_commit(final_bar);
-      mbar_wait(final_bar, 0, err);
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) tc_commit(bar);
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(q_full, 0, err) && mbar_wait_warp(&k_full[0], 0, err);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+      commit(&k_empty[0]);
     }
+    for (int j = 0; j < n_kt && ok; ++j) {
+      const int s = j % L::STAGES;
+      const int s1 = (j + 1) % L::STAGES;
+      bool next_ready = false;
+      ok = mbar_wait_warp(&v_full[s], (j / L::STAGES) & 1, err);
+      if (!ok) break;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int n_g = (g == 0) ? n_g0 : n_g1;
+        if (j >= n_g) continue;
+        ok = mbar_wait_warp(&p_ready[g], j & 1, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(g, s, j > 0 ? 1u : 0u);
+        if (j + 1 < n_g) {
+          if (!next_ready) {
+            ok = mbar_wait_warp(&k_full[s1], ((j + 1) / L::STAGES) & 1, err);
+            if (!ok) break;
+            tc_fence_after();
+            next_ready = true;
+          }
+          issue_s(g, s1);
+        }
+      }
+      if (!ok) break;
+      commit(&v_empty[s]);                 // V_j: read by PV_j
+      if (next_ready) commit(&k_empty[s1]);  // K_{j+1}: read by S_{j+1}
+    }
+    commit(final_bar);
+    mbar_wait_warp(final_bar, 0, err);
   } else {
     // ------------------------------------------------------------ softmax
     const int g = (warp - 2) >> 2;  // group

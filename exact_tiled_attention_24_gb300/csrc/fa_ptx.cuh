@@ -71,6 +71,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// Warp-wide form of mbar_wait for roles run by a whole warp: every lane
+// waits, and the warp agrees on the outcome so control flow stays uniform.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err);
+
 // Bounded wait for the phase with the given parity to complete. On time-out
 // it records DEV_TIMEOUT in *err and returns false; callers then abandon the
 // tile loop and fall through to their normal teardown.
@@ -85,6 +89,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  const bool ok = mbar_wait(bar, parity, err);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ------------------------------------------------------------------ TMA
