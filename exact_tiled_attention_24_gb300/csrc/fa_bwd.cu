@@ -438,12 +438,14 @@ constexpr uint32_t Q_COL_S = 0, Q_COL_DP = 128, Q_COL_DQ = 256, Q_COL_Q = 384, Q
 template <int D>
 struct DqSmem {
   using T = Tiles<D>;
-  static constexpr int KST = 2;
-  static constexpr int Q_OFF = 0;   // Q tile; later the dQ staging tile
-  static constexpr int DO_OFF = Q_OFF + T::BYTES;
-  static constexpr int K_OFF = DO_OFF + T::BYTES;
-  static constexpr int V_OFF = K_OFF + KST * T::BYTES;
-  static constexpr int BAR_OFF = V_OFF + KST * T::BYTES;
+  // Three K/V stages: 0 and 1 are dedicated; stage 2 is the Q/dO region,
+  // free once Q and dO have been copied into TMEM.
+  static constexpr int KST = 3;
+  static constexpr int Q_OFF = 0;   // Q tile, then K of stage 2, then the dQ staging tile
+  static constexpr int DO_OFF = Q_OFF + T::BYTES;  // dO tile, then V of stage 2
+  static constexpr int K_OFF = DO_OFF + T::BYTES;  // K of stages 0, 1
+  static constexpr int V_OFF = K_OFF + 2 * T::BYTES;  // V of stages 0, 1
+  static constexpr int BAR_OFF = V_OFF + 2 * T::BYTES;
   // q_full, kv_full[2], kv_empty[2], a_ready, s_full, dp_full, ds_ready, final
   static constexpr int NBARS = 1 + 2 * KST + 5;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
@@ -466,8 +468,9 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   if (smem == nullptr) return;
   uint8_t* sQ = smem + L::Q_OFF;
   uint8_t* sdO = smem + L::DO_OFF;
-  uint8_t* sK = smem + L::K_OFF;
-  uint8_t* sV = smem + L::V_OFF;
+  // K and V tile of stage s
+  auto kst = [&](int st) { return st < 2 ? smem + L::K_OFF + st * T::BYTES : sQ; };
+  auto vst = [&](int st) { return st < 2 ? smem + L::V_OFF + st * T::BYTES : sdO; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;       // K_j and V_j of one stage
@@ -527,10 +530,14 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % KST;
         if (!mbar_wait(&kv_empty[s], ((j / KST) & 1) ^ 1, err)) break;
+        // Stage 2 overlays Q and dO: first use waits for their copy to TMEM.
+        if (j == 2 && !mbar_wait(a_ready, 0, err)) break;
         mbar_arrive_expect_tx(&kv_full[s], 2 * T::BYTES);
+        uint8_t* kd = kst(s);
+        uint8_t* vd = vst(s);
         for (int p = 0; p < T::PANELS; ++p) {
-          tma_load_3d(sK + s * T::BYTES + p * T::PANEL, &tk, &kv_full[s], p * 64, j * TILE, bh);
-          tma_load_3d(sV + s * T::BYTES + p * T::PANEL, &tv, &kv_full[s], p * 64, j * TILE, bh);
+          tma_load_3d(kd + p * T::PANEL, &tk, &kv_full[s], p * 64, j * TILE, bh);
+          tma_load_3d(vd + p * T::PANEL, &tv, &kv_full[s], p * 64, j * TILE, bh);
         }
         issued = j + 1;
       }
@@ -544,11 +551,15 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     // issues MMAs and commits.
     constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // S, dP: A TMEM, B K-major
     constexpr uint32_t id_q = idesc_bf16(TILE, D, false, true);      // dQ: A TMEM, B MN-major
-    static_assert(KST == 2, "descriptor selection assumes two stages");
-    const uint64_t dKk0 = sdesc_kmajor(smem_u32(sK), 0), dKk1 = sdesc_kmajor(smem_u32(sK + T::BYTES), 0);
-    const uint64_t dVk0 = sdesc_kmajor(smem_u32(sV), 0), dVk1 = sdesc_kmajor(smem_u32(sV + T::BYTES), 0);
-    const uint64_t dKm0 = sdesc_mnmajor(smem_u32(sK), 0, T::PANEL);
-    const uint64_t dKm1 = sdesc_mnmajor(smem_u32(sK + T::BYTES), 0, T::PANEL);
+    static_assert(KST == 3, "descriptor selection assumes three stages");
+    const uint64_t dKk0 = sdesc_kmajor(smem_u32(kst(0)), 0), dKk1 = sdesc_kmajor(smem_u32(kst(1)), 0),
+                   dKk2 = sdesc_kmajor(smem_u32(kst(2)), 0);
+    const uint64_t dVk0 = sdesc_kmajor(smem_u32(vst(0)), 0), dVk1 = sdesc_kmajor(smem_u32(vst(1)), 0),
+                   dVk2 = sdesc_kmajor(smem_u32(vst(2)), 0);
+    const uint64_t dKm0 = sdesc_mnmajor(smem_u32(kst(0)), 0, T::PANEL),
+                   dKm1 = sdesc_mnmajor(smem_u32(kst(1)), 0, T::PANEL),
+                   dKm2 = sdesc_mnmajor(smem_u32(kst(2)), 0, T::PANEL);
+    auto sel = [](int st, uint64_t a, uint64_t b, uint64_t c) { return st == 0 ? a : (st == 1 ? b : c); };
     // S = Q Kⱼᵀ (or dP = dO Vⱼᵀ): A = Q (dO) in TMEM, B = Kⱼ (Vⱼ) K-major.
     auto issue_ab = [&](uint32_t a_col, uint64_t b, uint32_t d_col, uint64_t* bar) {
       if (elect_one()) {
@@ -577,10 +588,10 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       // S_{j+1}: the compute warps have read S_j (ds_ready).
-      if (more) issue_ab(Q_COL_Q, s1 ? dKk1 : dKk0, Q_COL_S, s_full);
+      if (more) issue_ab(Q_COL_Q, sel(s1, dKk0, dKk1, dKk2), Q_COL_S, s_full);
       // dQ += dS_j Kⱼ: A = dS in TMEM (bf16 in the dP columns, halves at
       // offsets 0 and 64), B = Kⱼ MN-major; then K_j and V_j are free.
-      const uint64_t bk = s ? dKm1 : dKm0;
+      const uint64_t bk = sel(s, dKm0, dKm1, dKm2);
       if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < TILE / 16; ++ks)
@@ -590,7 +601,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       }
       __syncwarp();
       // dP_{j+1} overwrites the dP columns after the dQ product read dS_j.
-      if (more) issue_ab(Q_COL_DO, s1 ? dVk1 : dVk0, Q_COL_DP, dp_full);
+      if (more) issue_ab(Q_COL_DO, sel(s1, dVk0, dVk1, dVk2), Q_COL_DP, dp_full);
     }
     if (elect_one()) tc_commit(final_bar);
     __syncwarp();
