@@ -141,16 +141,21 @@ constexpr uint32_t KV_COL_DV = 0, KV_COL_DK = 128, KV_COL_S = 256, KV_COL_DP = 3
 template <int D>
 struct DkdvSmem {
   using T = Tiles<D>;
-  static constexpr int QST = 2;
+  // Q tiles are read last by dK += dSᵀ Q, the product issued latest in a
+  // tile's round, and first by the next-but-one Sᵀ: three Q stages keep the
+  // load a full round ahead. dO is free one product after dV reads it.
+  static constexpr int QST = 3;
+  static constexpr int OST = 2;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + T::BYTES;
   static constexpr int Q_OFF = V_OFF + T::BYTES;
   static constexpr int DO_OFF = Q_OFF + QST * T::BYTES;
-  static constexpr int STAT_OFF = DO_OFF + QST * T::BYTES;
+  static constexpr int STAT_OFF = DO_OFF + OST * T::BYTES;
   static constexpr int STAT_BYTES = 2 * 2 * TILE * 4;  // two buffers of (lse, D) per query
   static constexpr int BAR_OFF = STAT_OFF + STAT_BYTES;
-  // kv_full, q_full[2], q_empty[2], s_full, dp_full, ds_ready, final
-  static constexpr int NBARS = 1 + 2 * QST + 4;
+  // kv_full, in_full[QST] (Q_i and dO_i of tile i landed), q_empty[QST],
+  // o_empty[OST], s_full, p_ready, dp_full, ds_ready, final
+  static constexpr int NBARS = 1 + 2 * QST + OST + 5;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   static constexpr int ALLOC = alloc_for(BYTES);
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   using L = DkdvSmem<D>;
   using T = Tiles<D>;
   constexpr int QST = L::QST;
+  constexpr int OST = L::OST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw, L::BYTES, L::ALLOC);
   if (smem == nullptr) return;
@@ -177,10 +183,12 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   float* sStat = reinterpret_cast<float*>(smem + L::STAT_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;
-  uint64_t* q_empty = q_full + QST;
-  uint64_t* s_full = q_empty + QST;
-  uint64_t* dp_full = s_full + 1;
+  uint64_t* in_full = bars + 1;
+  uint64_t* q_empty = in_full + QST;
+  uint64_t* o_empty = q_empty + QST;
+  uint64_t* s_full = o_empty + OST;
+  uint64_t* p_ready = s_full + 1;
+  uint64_t* dp_full = p_ready + 1;
   uint64_t* ds_ready = dp_full + 1;
   uint64_t* final_bar = ds_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
@@ -197,10 +205,12 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < QST; ++s) {
-      mbar_init(&q_full[s], 1);
+      mbar_init(&in_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
+    for (int s = 0; s < OST; ++s) mbar_init(&o_empty[s], 1);
     mbar_init(s_full, 1);
+    mbar_init(p_ready, 8);
     mbar_init(dp_full, 1);
     mbar_init(ds_ready, 8);
     mbar_init(final_bar, 1);
@@ -228,21 +238,25 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         tma_load_3d(sK + p * T::PANEL, &tk, kv_full, p * 64, k0, bh);
         tma_load_3d(sV + p * T::PANEL, &tv, kv_full, p * 64, k0, bh);
       }
+      // Q_i and dO_i complete on one barrier, so the issuer waits once per
+      // tile for its inputs.
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % QST;
-        if (!mbar_wait(&q_empty[s], ((it / QST) & 1) ^ 1, err)) break;
         const int q0 = (qt_begin + it) * TILE;
-        mbar_arrive_expect_tx(&q_full[s], 2 * T::BYTES);
+        const int sq = it % QST, so = it % OST;
+        if (!mbar_wait(&q_empty[sq], ((it / QST) & 1) ^ 1, err)) break;
+        if (!mbar_wait(&o_empty[so], ((it / OST) & 1) ^ 1, err)) break;
+        mbar_arrive_expect_tx(&in_full[sq], 2 * T::BYTES);
         for (int p = 0; p < T::PANELS; ++p) {
-          tma_load_3d(sQ + s * T::BYTES + p * T::PANEL, &tq, &q_full[s], p * 64, q0, bh);
-          tma_load_3d(sdO + s * T::BYTES + p * T::PANEL, &tdo, &q_full[s], p * 64, q0, bh);
+          tma_load_3d(sQ + sq * T::BYTES + p * T::PANEL, &tq, &in_full[sq], p * 64, q0, bh);
+          tma_load_3d(sdO + so * T::BYTES + p * T::PANEL, &tdo, &in_full[sq], p * 64, q0, bh);
         }
         issued = it + 1;
       }
+      // No copy may still be in flight when the CTA exits.
       mbar_wait(kv_full, 0, err);
       for (int it = max(0, issued - QST); it < issued; ++it)
-        mbar_wait(&q_full[it % QST], (it / QST) & 1, err);
+        mbar_wait(&in_full[it % QST], (it / QST) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -250,14 +264,17 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     // issues MMAs and commits.
     constexpr uint32_t id_s = idesc_bf16(TILE, TILE, false, false);  // Sᵀ, dPᵀ: K-major both
     constexpr uint32_t id_g = idesc_bf16(TILE, D, false, true);      // dV, dK: A TMEM, B MN-major
-    static_assert(QST == 2, "descriptor selection assumes two stages");
+    static_assert(QST == 3 && OST == 2, "descriptor selection assumes three Q and two dO stages");
     const uint64_t dK = sdesc_kmajor(smem_u32(sK), 0), dV = sdesc_kmajor(smem_u32(sV), 0);
-    const uint64_t dQk0 = sdesc_kmajor(smem_u32(sQ), 0), dQk1 = sdesc_kmajor(smem_u32(sQ + T::BYTES), 0);
+    const uint64_t dQk0 = sdesc_kmajor(smem_u32(sQ), 0), dQk1 = sdesc_kmajor(smem_u32(sQ + T::BYTES), 0),
+                   dQk2 = sdesc_kmajor(smem_u32(sQ + 2 * T::BYTES), 0);
     const uint64_t dOk0 = sdesc_kmajor(smem_u32(sdO), 0), dOk1 = sdesc_kmajor(smem_u32(sdO + T::BYTES), 0);
     const uint64_t dQm0 = sdesc_mnmajor(smem_u32(sQ), 0, T::PANEL);
     const uint64_t dQm1 = sdesc_mnmajor(smem_u32(sQ + T::BYTES), 0, T::PANEL);
+    const uint64_t dQm2 = sdesc_mnmajor(smem_u32(sQ + 2 * T::BYTES), 0, T::PANEL);
     const uint64_t dOm0 = sdesc_mnmajor(smem_u32(sdO), 0, T::PANEL);
     const uint64_t dOm1 = sdesc_mnmajor(smem_u32(sdO + T::BYTES), 0, T::PANEL);
+    auto sel3 = [](int st, uint64_t a, uint64_t b, uint64_t c) { return st == 0 ? a : (st == 1 ? b : c); };
     // Sᵀ = K Qᵀ (or dPᵀ = V dOᵀ): 128 keys x 128 queries, K = D; then commit.
     auto issue_kq = [&](uint64_t a, uint64_t b, uint32_t d_col, uint64_t* bar) {
       if (elect_one()) {
@@ -280,34 +297,39 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       }
       __syncwarp();
     };
-    bool ok = mbar_wait_warp(kv_full, 0, err) && mbar_wait_warp(&q_full[0], 0, err);
+    bool ok = mbar_wait_warp(kv_full, 0, err) && mbar_wait_warp(&in_full[0], 0, err);
     if (ok) {
       tc_fence_after();
       issue_kq(dK, dQk0, KV_COL_S, s_full);
       issue_kq(dV, dOk0, KV_COL_DP, dp_full);
     }
+    // Round i: dV_i, Sᵀ_{i+1}, dK_i, dPᵀ_{i+1}. dV_i needs only Pᵀ_i, so it
+    // and Sᵀ_{i+1} keep the tensor pipe busy while the compute warps turn
+    // dPᵀ_i into dSᵀ_i. The wait for tile i+1's inputs comes first: it is
+    // normally met already and overlaps the wait for Pᵀ_i.
     for (int i = 0; i < n_it && ok; ++i) {
-      const int st = i % QST;
-      const int s1 = (i + 1) % QST;
+      const int sq = i % QST, so = i % OST;
+      const int sq1 = (i + 1) % QST, so1 = (i + 1) % OST;
       const uint32_t acc0 = i > 0 ? 1u : 0u;
       const bool more = i + 1 < n_it;
-      // The next tile's Q/dO ahead of the wait for this tile's dSᵀ.
       if (more) {
-        ok = mbar_wait_warp(&q_full[s1], ((i + 1) / QST) & 1, err);
+        ok = mbar_wait_warp(&in_full[sq1], ((i + 1) / QST) & 1, err);
         if (!ok) break;
       }
+      ok = mbar_wait_warp(p_ready, i & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      // dV += Pᵀ dO_i (Pᵀ in the S columns); dO_i then has no further reader.
+      issue_grad(KV_COL_DV, KV_COL_S, so ? dOm1 : dOm0, acc0, &o_empty[so]);
+      // Sᵀ_{i+1} overwrites the S columns after the dV product read Pᵀ_i.
+      if (more) issue_kq(dK, sel3(sq1, dQk0, dQk1, dQk2), KV_COL_S, s_full);
       ok = mbar_wait_warp(ds_ready, i & 1, err);
       if (!ok) break;
       tc_fence_after();
-      // dV += Pᵀ dO_i (Pᵀ in the S columns).
-      issue_grad(KV_COL_DV, KV_COL_S, st ? dOm1 : dOm0, acc0, nullptr);
-      // Sᵀ_{i+1} overwrites the S columns after the dV product read Pᵀ_i.
-      if (more) issue_kq(dK, s1 ? dQk1 : dQk0, KV_COL_S, s_full);
-      // dK += dSᵀ Q_i (dSᵀ in the dP columns); Q_i and dO_i then have no
-      // further readers.
-      issue_grad(KV_COL_DK, KV_COL_DP, st ? dQm1 : dQm0, acc0, &q_empty[st]);
+      // dK += dSᵀ Q_i (dSᵀ in the dP columns); Q_i then has no further reader.
+      issue_grad(KV_COL_DK, KV_COL_DP, sel3(sq, dQm0, dQm1, dQm2), acc0, &q_empty[sq]);
       // dPᵀ_{i+1} overwrites the dP columns after the dK product read dSᵀ_i.
-      if (more) issue_kq(dV, s1 ? dOk1 : dOk0, KV_COL_DP, dp_full);
+      if (more) issue_kq(dV, so1 ? dOk1 : dOk0, KV_COL_DP, dp_full);
     }
     if (elect_one()) tc_commit(final_bar);
     __syncwarp();
@@ -326,14 +348,17 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     const float* lse_h = lse + static_cast<size_t>(bh) * N;
     const float* D_h = Dvec + static_cast<size_t>(bh) * N;
     constexpr float LOG2E = 1.4426950408889634f;
-    // Per-tile (lse, D) of the 128 queries, double-buffered in shared memory:
-    // compute thread ct fills entry ct % 128 of lse (ct < 128) or of D.
+    // Per-tile (lse·log2 e, D) of the 128 queries, double-buffered in shared
+    // memory: compute thread ct fills entry ct % 128 of lse (ct < 128) or of
+    // D. A value is loaded one tile before it is stored, and only the store
+    // reads the loaded register, so no warp waits on the load.
+    const float stat_mul = ct < 128 ? LOG2E : 1.f;
     auto load_stat = [&](int tile) -> float {
       const int q = (qt_begin + tile) * TILE + (ct & 127);
-      if (ct < 128) return (tile < n_it && q < N) ? lse_h[q] * LOG2E : INFINITY;
+      if (ct < 128) return (tile < n_it && q < N) ? lse_h[q] : INFINITY;
       return (tile < n_it && q < N) ? D_h[q] : 0.f;
     };
-    sStat[ct] = load_stat(0);  // buffer 0: lse[0..127], D[128..255]
+    sStat[ct] = load_stat(0) * stat_mul;  // buffer 0: lse[0..127], D[128..255]
     float stat_nx = load_stat(1);
     named_bar_sync(1, 256);
     bool ok = true;
@@ -348,20 +373,21 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       const uint32_t dp_addr = tmem + lane_addr + KV_COL_DP + half * 64;
       float p[64];
       const bool masked = !key_ok || (CAUSAL && q0 < k0 + TILE);
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t raw[32];
-        tmem_ld32(s_addr + 32 * h2, raw);
+      {
+        uint32_t raw[64];
+        tmem_ld64(s_addr, raw);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + 32 * h2 + c);
-          float* pp = p + 32 * h2 + c;
-          pp[0] = ex2(fmaf(__uint_as_float(raw[c + 0]), scale_log2, -l4.x));
-          pp[1] = ex2(fmaf(__uint_as_float(raw[c + 1]), scale_log2, -l4.y));
-          pp[2] = ex2(fmaf(__uint_as_float(raw[c + 2]), scale_log2, -l4.z));
-          pp[3] = ex2(fmaf(__uint_as_float(raw[c + 3]), scale_log2, -l4.w));
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + c);
+          p[c + 0] = ex2(fmaf(__uint_as_float(raw[c + 0]), scale_log2, -l4.x));
+          p[c + 1] = ex2(fmaf(__uint_as_float(raw[c + 1]), scale_log2, -l4.y));
+          p[c + 2] = ex2(fmaf(__uint_as_float(raw[c + 2]), scale_log2, -l4.z));
+          p[c + 3] = ex2(fmaf(__uint_as_float(raw[c + 3]), scale_log2, -l4.w));
         }
+      }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
         if (masked) {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
@@ -372,26 +398,32 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(p[32 * h2 + 2 * t], p[32 * h2 + 2 * t + 1]);
         tmem_st16(s_addr + 16 * h2, pk);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_ready);
       // dSᵀ = Pᵀ ∘ (dPᵀ − D), bf16 into this warp's own dP columns.
       ok = mbar_wait(dp_full, i & 1, err);
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t raw[32];
-        tmem_ld32(dp_addr + 32 * h2, raw);
+      {
+        uint32_t raw[64];
+        tmem_ld64(dp_addr, raw);
         tmem_ld_wait();
-        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(s_D + 32 * h2 + c);
-          const float* pp = p + 32 * h2 + c;
-          pk[c / 2] = pack_bf16x2(pp[0] * (__uint_as_float(raw[c + 0]) - d4.x),
-                                  pp[1] * (__uint_as_float(raw[c + 1]) - d4.y));
-          pk[c / 2 + 1] = pack_bf16x2(pp[2] * (__uint_as_float(raw[c + 2]) - d4.z),
-                                      pp[3] * (__uint_as_float(raw[c + 3]) - d4.w));
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(s_D + 32 * h2 + c);
+            const float* pp = p + 32 * h2 + c;
+            const uint32_t* rr = raw + 32 * h2 + c;
+            pk[c / 2] = pack_bf16x2(pp[0] * (__uint_as_float(rr[0]) - d4.x), pp[1] * (__uint_as_float(rr[1]) - d4.y));
+            pk[c / 2 + 1] =
+                pack_bf16x2(pp[2] * (__uint_as_float(rr[2]) - d4.z), pp[3] * (__uint_as_float(rr[3]) - d4.w));
+          }
+          tmem_st16(dp_addr + 16 * h2, pk);
         }
-        tmem_st16(dp_addr + 16 * h2, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       if (lane == 0) mbar_arrive(ds_ready);
       // Next tile's (lse, D) into the other buffer; its previous readers
       // passed the barrier at the end of the previous iteration.
-      sStat[((i + 1) & 1) * 256 + ct] = stat_nx;
+      sStat[((i + 1) & 1) * 256 + ct] = stat_nx * stat_mul;
       stat_nx = load_stat(i + 2);
       named_bar_sync(1, 256);
     }
@@ -446,8 +478,9 @@ struct DqSmem {
   static constexpr int K_OFF = DO_OFF + T::BYTES;  // K of stages 0, 1
   static constexpr int V_OFF = K_OFF + 2 * T::BYTES;  // V of stages 0, 1
   static constexpr int BAR_OFF = V_OFF + 2 * T::BYTES;
-  // q_full, kv_full[2], kv_empty[2], a_ready, s_full, dp_full, ds_ready, final
-  static constexpr int NBARS = 1 + 2 * KST + 5;
+  // q_full, kv_full[KST], kv_empty[KST], a_ready, s_full, s_free, dp_full,
+  // ds_ready, final
+  static constexpr int NBARS = 1 + 2 * KST + 6;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   static constexpr int ALLOC = alloc_for(BYTES);
@@ -477,7 +510,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   uint64_t* kv_empty = kv_full + KST;
   uint64_t* a_ready = kv_empty + KST;  // Q and dO copied into TMEM
   uint64_t* s_full = a_ready + 1;
-  uint64_t* dp_full = s_full + 1;
+  uint64_t* s_free = s_full + 1;  // the compute warps hold S_j in registers
+  uint64_t* dp_full = s_free + 1;
   uint64_t* ds_ready = dp_full + 1;
   uint64_t* final_bar = ds_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
@@ -499,6 +533,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     }
     mbar_init(a_ready, 8);
     mbar_init(s_full, 1);
+    mbar_init(s_free, 8);
     mbar_init(dp_full, 1);
     mbar_init(ds_ready, 8);
     mbar_init(final_bar, 1);
@@ -576,6 +611,9 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       issue_ab(Q_COL_Q, dKk0, Q_COL_S, s_full);
       issue_ab(Q_COL_DO, dVk0, Q_COL_DP, dp_full);
     }
+    // Round j: S_{j+1} as soon as the compute warps hold S_j in registers,
+    // then dQ += dS_j Kⱼ and dP_{j+1}; S_{j+1} keeps the tensor pipe busy
+    // while dS_j is formed.
     for (int j = 0; j < n_kv && ok; ++j) {
       const int s = j % KST;
       const int s1 = (j + 1) % KST;
@@ -584,11 +622,13 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         ok = mbar_wait_warp(&kv_full[s1], ((j + 1) / KST) & 1, err);
         if (!ok) break;
       }
+      ok = mbar_wait_warp(s_free, j & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      if (more) issue_ab(Q_COL_Q, sel(s1, dKk0, dKk1, dKk2), Q_COL_S, s_full);
       ok = mbar_wait_warp(ds_ready, j & 1, err);
       if (!ok) break;
       tc_fence_after();
-      // S_{j+1}: the compute warps have read S_j (ds_ready).
-      if (more) issue_ab(Q_COL_Q, sel(s1, dKk0, dKk1, dKk2), Q_COL_S, s_full);
       // dQ += dS_j Kⱼ: A = dS in TMEM (bf16 in the dP columns, halves at
       // offsets 0 and 64), B = Kⱼ MN-major; then K_j and V_j are free.
       const uint64_t bk = sel(s, dKm0, dKm1, dKm2);
@@ -654,13 +694,18 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       const uint32_t dp_addr = tmem + lane_addr + Q_COL_DP + half * 64;
       float p[64];
       const bool masked = (kb0 + 64 > N) || (CAUSAL && kb0 + 63 > q0);
+      uint32_t raw_s[64];
+      tmem_ld64(s_addr, raw_s);
+      tmem_ld_wait();
+      // S_j is in registers: the next S may overwrite its columns.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t raw[32];
-        tmem_ld32(s_addr + 32 * h2, raw);
-        tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) p[32 * h2 + c] = ex2(fmaf(__uint_as_float(raw[c]), scale_log2, -lse2));
+        for (int c = 0; c < 32; ++c)
+          p[32 * h2 + c] = ex2(fmaf(__uint_as_float(raw_s[32 * h2 + c]), scale_log2, -lse2));
         if (masked) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
@@ -672,17 +717,17 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       ok = mbar_wait(dp_full, j & 1, err);
       if (!ok) break;
       tc_fence_after();
+      uint32_t raw[64];
+      tmem_ld64(dp_addr, raw);
+      tmem_ld_wait();
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t raw[32];
-        tmem_ld32(dp_addr + 32 * h2, raw);
-        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int t2 = 0; t2 < 16; ++t2) {
           const float* pp = p + 32 * h2 + 2 * t2;
-          pk[t2] = pack_bf16x2(pp[0] * (__uint_as_float(raw[2 * t2]) - Dq),
-                               pp[1] * (__uint_as_float(raw[2 * t2 + 1]) - Dq));
+          const uint32_t* rr = raw + 32 * h2 + 2 * t2;
+          pk[t2] = pack_bf16x2(pp[0] * (__uint_as_float(rr[0]) - Dq), pp[1] * (__uint_as_float(rr[1]) - Dq));
         }
         tmem_st16(dp_addr + 16 * h2, pk);
       }
