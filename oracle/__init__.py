@@ -6,12 +6,15 @@ and by the benchmark's CPU-baseline / reference leg, never by the library.
 from .attention import (  # noqa: F401
     ROW_CHUNK,
     attention_bwd,
+    attention_bwd_gqa,
     attention_bwd_head,
     attention_dq_rows_head,
     attention_flops,
     attention_fwd,
+    attention_fwd_gqa,
     attention_fwd_head,
     attention_pairs,
+    kv_head_of,
     softmax_blocks_naive_sum,
     softmax_online_blocks,
     softmax_safe,

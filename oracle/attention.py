@@ -199,6 +199,56 @@ def attention_dq_rows_head(q, k, v, do, scale, causal, rows):
 
 
 # --------------------------------------------------------------------------
+# grouped-query attention
+# --------------------------------------------------------------------------
+# "07-16 下午" notes, section 自回归语言模型推理 (Prefill、Decode 与推理调度):
+# with grouped-query attention the number of K/V heads is smaller than the
+# number of query heads.  The pages give no head mapping; the reading used
+# here is the usual one: H / Hkv consecutive query heads share one K/V head,
+# query head h reading K/V head h // (H / Hkv).  Attention per query head is
+# then exactly the attention above, and since one K/V head feeds several
+# query heads, its gradient is the sum of theirs.
+
+def kv_head_of(h, H, Hkv):
+    """K/V head read by query head h."""
+    return h // (H // Hkv)
+
+
+def attention_fwd_gqa(q, k, v, scale, causal):
+    """q: [B, H, N, d]; k, v: [B, Hkv, N, d] float64 (Hkv divides H).
+    Returns o [B, H, N, d], lse [B, H, N]."""
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            g = kv_head_of(h, H, Hkv)
+            o[b, h], lse[b, h] = attention_fwd_head(q[b, h], k[b, g], v[b, g], scale, causal)
+    return o, lse
+
+
+def attention_bwd_gqa(q, k, v, do, scale, causal):
+    """Gradients for grouped-query heads: dq [B, H, N, d], dk, dv
+    [B, Hkv, N, d] (each the sum over the query heads sharing that K/V
+    head) and D [B, H, N]."""
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    D = np.empty((B, H, N), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            g = kv_head_of(h, H, Hkv)
+            dq[b, h], dkh, dvh, D[b, h] = attention_bwd_head(q[b, h], k[b, g], v[b, g], do[b, h],
+                                                             scale, causal)
+            dk[b, g] += dkh
+            dv[b, g] += dvh
+    return dq, dk, dv, D
+
+
+# --------------------------------------------------------------------------
 # FLOP convention used when this oracle is timed
 # --------------------------------------------------------------------------
 
