@@ -43,8 +43,10 @@ FA_STATUS = {
 
 EXPORTED_SYMBOLS = (
     "fa_fwd",
+    "fa_fwd_gqa",
     "fa_bwd_workspace_bytes",
     "fa_bwd",
+    "fa_bwd_gqa",
     "fa_bwd_preprocess",
     "fa_bwd_dkdv",
     "fa_bwd_dq",
@@ -75,15 +77,19 @@ def lib() -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd.restype = i
+        L.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_gqa.restype = i
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_bytes.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = i
+        L.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+        L.fa_bwd_gqa.restype = i
         L.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
         L.fa_bwd_preprocess.restype = i
-        L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_bwd_dkdv.restype = i
-        L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_bwd_dq.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
@@ -110,21 +116,28 @@ def _check(status, where):
         raise FAError(status, where)
 
 
-def _check_inputs(*ts):
-    ref = ts[0]
-    if ref.dim() != 4:
+def _check_inputs(q, k, v, *rest):
+    """q (and o, dO in rest): [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H.
+    Returns Hkv."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("expected [B, H, N, d] tensors")
-    for t in ts:
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    for t in (q, k, v) + rest:
         if not t.is_cuda:
             raise ValueError("tensors must be on a CUDA device")
         if t.dtype != torch.bfloat16:
             raise ValueError("tensors must be bfloat16")
-        if t.shape != ref.shape:
-            raise ValueError("q, k, v (and o, dO) must have the same shape")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
-        if t.device != ref.device:
+        if t.device != q.device:
             raise ValueError("tensors must be on one device")
+    for t in rest:
+        if t.shape != q.shape:
+            raise ValueError("o and dO must have q's shape")
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape or Hkv < 1 or H % Hkv:
+        raise ValueError("k and v must be [B, Hkv, N, d] with Hkv dividing q's head count")
+    return Hkv
 
 
 def _scale(d, scale):
@@ -132,13 +145,16 @@ def _scale(d, scale):
 
 
 def fwd(q, k, v, causal=False, scale=None, out=None, lse=None):
-    """o, lse = softmax(scale·q kᵀ [causal]) v and its per-row log-sum-exp."""
-    _check_inputs(q, k, v)
+    """o, lse = softmax(scale·q kᵀ [causal]) v and its per-row log-sum-exp.
+
+    k and v may hold fewer heads than q (grouped-query attention): query head
+    h then uses K/V head h // (H // Hkv)."""
+    Hkv = _check_inputs(q, k, v)
     B, H, N, d = q.shape
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check(lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, N, d,
-                        _scale(d, scale), int(bool(causal)), _stream(q.device)), "fa_fwd")
+    _check(lib().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, Hkv, N, d,
+                            _scale(d, scale), int(bool(causal)), _stream(q.device)), "fa_fwd_gqa")
     return o, lse_t
 
 
@@ -147,16 +163,18 @@ def bwd_workspace_bytes(B, H, N, d) -> int:
 
 
 def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None):
-    """dq, dk, dv of o = softmax(scale·q kᵀ [causal]) v for the output gradient do."""
-    _check_inputs(q, k, v, o, do)
+    """dq, dk, dv of o = softmax(scale·q kᵀ [causal]) v for the output gradient do
+    (dk, dv shaped like k, v; with grouped-query heads they sum over the group)."""
+    Hkv = _check_inputs(q, k, v, o, do)
     B, H, N, d = q.shape
     ws_bytes = bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                        _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                        B, H, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)), "fa_bwd")
+    _check(lib().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                            _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)),
+           "fa_bwd_gqa")
     return dq, dk, dv
 
 
@@ -170,16 +188,18 @@ def bwd_preprocess(o, do, Dvec):
 def bwd_dkdv(q, k, v, do, lse, Dvec, dk, dv, causal=False, scale=None):
     """dk, dv (bf16, written in place) from the recomputed P and dS."""
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     _check(lib().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dk),
-                             _ptr(dv), B, H, N, d, _scale(d, scale), int(bool(causal)),
+                             _ptr(dv), B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)),
                              _stream(q.device)), "fa_bwd_dkdv")
 
 
 def bwd_dq(q, k, v, do, lse, Dvec, dq, causal=False, scale=None):
     """dq (bf16, written in place) from the recomputed dS."""
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     _check(lib().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dq),
-                           B, H, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)),
+                           B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)),
            "fa_bwd_dq")
 
 

@@ -25,6 +25,12 @@ int check_sizes(int B, int H, int N, int d) {
   return FA_OK;
 }
 
+// Grouped-query heads: Hkv K/V heads, each shared by H / Hkv query heads.
+int check_heads(int H, int Hkv) {
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
 int check_scale(float scale) {
   if (!std::isfinite(scale) || scale <= 0.f) return FA_ERR_INVALID_ARG;
   return FA_OK;
@@ -51,16 +57,22 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-           int d, float scale, int causal, void* stream) {
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Hkv, int N, int d, float scale, int causal, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   int st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
-  return map_cuda(fa::launch_fwd(q, k, v, o, lse, B * H, N, d, scale, causal != 0,
+  return map_cuda(fa::launch_fwd(q, k, v, o, lse, B * H, H / Hkv, N, d, scale, causal != 0,
                                  static_cast<cudaStream_t>(stream)));
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, void* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -80,48 +92,58 @@ int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, int H, 
 }
 
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                const float* Dvec, void* dk, void* dv, int B, int H, int N, int d, float scale,
-                int causal, void* stream) {
+                const float* Dvec, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+                float scale, int causal, void* stream) {
   if (!q || !k || !v || !dO || !lse || !Dvec || !dk || !dv) return FA_ERR_INVALID_ARG;
   int st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(Dvec) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
-  return map_cuda(fa::launch_bwd_dkdv(q, k, v, dO, dk, dv, lse, Dvec, B * H, N, d, scale,
+  return map_cuda(fa::launch_bwd_dkdv(q, k, v, dO, dk, dv, lse, Dvec, B * H, H / Hkv, N, d, scale,
                                       causal != 0, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-              const float* Dvec, void* dq, int B, int H, int N, int d, float scale, int causal,
-              void* stream) {
+              const float* Dvec, void* dq, int B, int H, int Hkv, int N, int d, float scale,
+              int causal, void* stream) {
   if (!q || !k || !v || !dO || !lse || !Dvec || !dq) return FA_ERR_INVALID_ARG;
   int st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(Dvec) || !aligned16(dq))
     return FA_ERR_MISALIGNED;
-  return map_cuda(fa::launch_bwd_dq(q, k, v, dO, dq, lse, Dvec, B * H, N, d, scale, causal != 0,
-                                    static_cast<cudaStream_t>(stream)));
+  return map_cuda(fa::launch_bwd_dq(q, k, v, dO, dq, lse, Dvec, B * H, H / Hkv, N, d, scale,
+                                    causal != 0, static_cast<cudaStream_t>(stream)));
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-           const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
-           int B, int H, int N, int d, float scale, int causal, void* stream) {
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+               int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   int st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!workspace || ws_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_WORKSPACE;
   if (!aligned16(workspace) || !aligned16(o) || !aligned16(dq)) return FA_ERR_MISALIGNED;
   float* Dvec = static_cast<float*>(workspace);
   st = fa_bwd_preprocess(o, dO, Dvec, B, H, N, d, stream);
   if (st != FA_OK) return st;
-  st = fa_bwd_dkdv(q, k, v, dO, lse, Dvec, dk, dv, B, H, N, d, scale, causal, stream);
+  st = fa_bwd_dkdv(q, k, v, dO, lse, Dvec, dk, dv, B, H, Hkv, N, d, scale, causal, stream);
   if (st != FA_OK) return st;
-  return fa_bwd_dq(q, k, v, dO, lse, Dvec, dq, B, H, N, d, scale, causal, stream);
+  return fa_bwd_dq(q, k, v, dO, lse, Dvec, dq, B, H, Hkv, N, d, scale, causal, stream);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+           int B, int H, int N, int d, float scale, int causal, void* stream) {
+  return fa_bwd_gqa(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, H, N, d, scale,
+                    causal, stream);
 }
 
 int fa_last_device_error(void* stream) {

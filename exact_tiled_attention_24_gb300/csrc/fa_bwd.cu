@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tdk,
                     const __grid_constant__ CUtensorMap tdv, const float* __restrict__ lse,
-                    const float* __restrict__ Dvec, int BH, int N, float scale, float scale_log2) {
+                    const float* __restrict__ Dvec, int BHkv, int G, int N, float scale, float scale_log2) {
   using L = DkdvSmem<D>;
   using T = Tiles<D>;
   constexpr int QST = L::QST;
@@ -196,11 +196,14 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (N + TILE - 1) / TILE;
-  int kt, bh;  // causal: heaviest key tile (kt = 0) first within each head group
-  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_t, HEAD_GROUP, &kt, &bh);
+  int kt, bkv;  // causal: heaviest key tile (kt = 0) first within each head group
+  grouped_tile_order(static_cast<int>(blockIdx.x), BHkv, n_t, HEAD_GROUP, &kt, &bkv);
   const int k0 = kt * TILE;
   const int qt_begin = CAUSAL ? kt : 0;  // first query tile with a visible pair
-  const int n_it = n_t - qt_begin;
+  const int n_q = n_t - qt_begin;        // query tiles swept per query head
+  // Sweep tile it = (query head bkv·G + it / n_q, query tile qt_begin + it % n_q):
+  // dK and dV of a shared K/V head sum over every query head of its group.
+  const int n_it = G * n_q;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -235,14 +238,20 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       prefetch_tmap(&tdo);
       mbar_arrive_expect_tx(kv_full, 2 * T::BYTES);
       for (int p = 0; p < T::PANELS; ++p) {
-        tma_load_3d(sK + p * T::PANEL, &tk, kv_full, p * 64, k0, bh);
-        tma_load_3d(sV + p * T::PANEL, &tv, kv_full, p * 64, k0, bh);
+        tma_load_3d(sK + p * T::PANEL, &tk, kv_full, p * 64, k0, bkv);
+        tma_load_3d(sV + p * T::PANEL, &tv, kv_full, p * 64, k0, bkv);
       }
       // Q_i and dO_i complete on one barrier, so the issuer waits once per
       // tile for its inputs.
       int issued = 0;
+      int gq = 0, qi = 0;  // query head within the group, query tile index
       for (int it = 0; it < n_it; ++it) {
-        const int q0 = (qt_begin + it) * TILE;
+        const int q0 = (qt_begin + qi) * TILE;
+        const int bh = bkv * G + gq;
+        if (++qi == n_q) {
+          qi = 0;
+          ++gq;
+        }
         const int sq = it % QST, so = it % OST;
         if (!mbar_wait(&q_empty[sq], ((it / QST) & 1) ^ 1, err)) break;
         if (!mbar_wait(&o_empty[so], ((it / OST) & 1) ^ 1, err)) break;
@@ -345,8 +354,6 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     const int key = k0 + r;
     const bool key_ok = key < N;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const float* lse_h = lse + static_cast<size_t>(bh) * N;
-    const float* D_h = Dvec + static_cast<size_t>(bh) * N;
     constexpr float LOG2E = 1.4426950408889634f;
     // Per-tile (lse·log2 e, D) of the 128 queries, double-buffered in shared
     // memory: compute thread ct fills entry ct % 128 of lse (ct < 128) or of
@@ -354,16 +361,21 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     // reads the loaded register, so no warp waits on the load.
     const float stat_mul = ct < 128 ? LOG2E : 1.f;
     auto load_stat = [&](int tile) -> float {
-      const int q = (qt_begin + tile) * TILE + (ct & 127);
-      if (ct < 128) return (tile < n_it && q < N) ? lse_h[q] : INFINITY;
-      return (tile < n_it && q < N) ? D_h[q] : 0.f;
+      if (tile >= n_it) return ct < 128 ? INFINITY : 0.f;
+      const int gq = tile / n_q;
+      const int q = (qt_begin + tile - gq * n_q) * TILE + (ct & 127);
+      const size_t row = static_cast<size_t>(bkv * G + gq) * N + q;
+      if (ct < 128) return q < N ? lse[row] : INFINITY;
+      return q < N ? Dvec[row] : 0.f;
     };
     sStat[ct] = load_stat(0) * stat_mul;  // buffer 0: lse[0..127], D[128..255]
     float stat_nx = load_stat(1);
     named_bar_sync(1, 256);
     bool ok = true;
+    int qi = 0;  // query tile index of sweep tile i within its query head
     for (int i = 0; i < n_it; ++i) {
-      const int q0 = (qt_begin + i) * TILE + half * 64;  // first query of this warp's half
+      const int q0 = (qt_begin + qi) * TILE + half * 64;  // first query of this warp's half
+      if (++qi == n_q) qi = 0;
       const float* s_lse = sStat + (i & 1) * 256 + half * 64;
       const float* s_D = s_lse + 128;
       ok = mbar_wait(s_full, i & 1, err);
@@ -448,8 +460,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     named_bar_sync(1, 256);
     if (ok && warp == 2 && lane == 0) {
       for (int p = 0; p < T::PANELS; ++p) {
-        tma_store_3d(&tdk, sQ + p * T::PANEL, p * 64, k0, bh);
-        tma_store_3d(&tdv, sdO + p * T::PANEL, p * 64, k0, bh);
+        tma_store_3d(&tdk, sQ + p * T::PANEL, p * 64, k0, bkv);
+        tma_store_3d(&tdv, sdO + p * T::PANEL, p * 64, k0, bkv);
       }
       tma_store_commit();
       tma_store_wait_all();
@@ -492,7 +504,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdq, const float* __restrict__ lse,
-                  const float* __restrict__ Dvec, int BH, int N, float scale, float scale_log2) {
+                  const float* __restrict__ Dvec, int BH, int G, int N, float scale, float scale_log2) {
   using L = DqSmem<D>;
   using T = Tiles<D>;
   constexpr int KST = L::KST;
@@ -523,6 +535,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_t, HEAD_GROUP, &t, &bh);
   const int qt = n_t - 1 - t;
   const int q0 = qt * TILE;
+  const int bkv = bh / G;  // K/V head shared by G consecutive query heads
   const int n_kv = CAUSAL ? qt + 1 : n_t;
 
   if (threadIdx.x == 0) {
@@ -571,8 +584,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         uint8_t* kd = kst(s);
         uint8_t* vd = vst(s);
         for (int p = 0; p < T::PANELS; ++p) {
-          tma_load_3d(kd + p * T::PANEL, &tk, &kv_full[s], p * 64, j * TILE, bh);
-          tma_load_3d(vd + p * T::PANEL, &tv, &kv_full[s], p * 64, j * TILE, bh);
+          tma_load_3d(kd + p * T::PANEL, &tk, &kv_full[s], p * 64, j * TILE, bkv);
+          tma_load_3d(vd + p * T::PANEL, &tv, &kv_full[s], p * 64, j * TILE, bkv);
         }
         issued = j + 1;
       }
@@ -762,15 +775,15 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
 template <int D, bool CAUSAL>
 static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdk,
-                                 const CUtensorMap& tdv, const float* lse, const float* Dvec, int BH,
-                                 int N, float scale, cudaStream_t stream) {
+                                 const CUtensorMap& tdv, const float* lse, const float* Dvec, int BHkv,
+                                 int G, int N, float scale, cudaStream_t stream) {
   auto kern = bwd_dkdv_kernel<D, CAUSAL>;
   const int smem = DkdvSmem<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_t = (N + TILE - 1) / TILE;
-  dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BH));
-  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale,
+  dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BHkv));
+  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BHkv, G, N, scale,
                                                scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
@@ -778,14 +791,14 @@ static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
 template <int D, bool CAUSAL>
 static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse,
-                               const float* Dvec, int BH, int N, float scale, cudaStream_t stream) {
+                               const float* Dvec, int BH, int G, int N, float scale, cudaStream_t stream) {
   auto kern = bwd_dq_kernel<D, CAUSAL>;
   const int smem = DqSmem<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_t = (N + TILE - 1) / TILE;
   dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BH));
-  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale,
+  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale,
                                                scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
@@ -806,35 +819,37 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* d
 }
 
 cudaError_t launch_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
-                            void* dv, const float* lse, const float* Dvec, int BH, int N, int d,
+                            void* dv, const float* lse, const float* Dvec, int BH, int G, int N, int d,
                             float scale, bool causal, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   const int T = bwd::TILE;
+  const int BHkv = BH / G;
   if (!make_tmap_bf16(&tq, q, BH, N, d, T) || !make_tmap_bf16(&tdo, dO, BH, N, d, T) ||
-      !make_tmap_bf16(&tk, k, BH, N, d, T) || !make_tmap_bf16(&tv, v, BH, N, d, T) ||
-      !make_tmap_bf16(&tdk, dk, BH, N, d, T) || !make_tmap_bf16(&tdv, dv, BH, N, d, T))
+      !make_tmap_bf16(&tk, k, BHkv, N, d, T) || !make_tmap_bf16(&tv, v, BHkv, N, d, T) ||
+      !make_tmap_bf16(&tdk, dk, BHkv, N, d, T) || !make_tmap_bf16(&tdv, dv, BHkv, N, d, T))
     return cudaErrorInvalidValue;
   if (d == 64)
-    return causal ? bwd::launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream)
-                  : bwd::launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream);
-  return causal ? bwd::launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream)
-                : bwd::launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BH, N, scale, stream);
+    return causal ? bwd::launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BHkv, G, N, scale, stream)
+                  : bwd::launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BHkv, G, N, scale, stream);
+  return causal ? bwd::launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BHkv, G, N, scale, stream)
+                : bwd::launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BHkv, G, N, scale, stream);
 }
 
 cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
-                          const float* lse, const float* Dvec, int BH, int N, int d, float scale,
+                          const float* lse, const float* Dvec, int BH, int G, int N, int d, float scale,
                           bool causal, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tdo, tdq;
   const int T = bwd::TILE;
+  const int BHkv = BH / G;
   if (!make_tmap_bf16(&tq, q, BH, N, d, T) || !make_tmap_bf16(&tdo, dO, BH, N, d, T) ||
-      !make_tmap_bf16(&tk, k, BH, N, d, T) || !make_tmap_bf16(&tv, v, BH, N, d, T) ||
+      !make_tmap_bf16(&tk, k, BHkv, N, d, T) || !make_tmap_bf16(&tv, v, BHkv, N, d, T) ||
       !make_tmap_bf16(&tdq, dq, BH, N, d, T))
     return cudaErrorInvalidValue;
   if (d == 64)
-    return causal ? bwd::launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream)
-                  : bwd::launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream);
-  return causal ? bwd::launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream)
-                : bwd::launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, N, scale, stream);
+    return causal ? bwd::launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream)
+                  : bwd::launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream);
+  return causal ? bwd::launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream)
+                : bwd::launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream);
 }
 
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream) {

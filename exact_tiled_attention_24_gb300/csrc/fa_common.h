@@ -10,18 +10,19 @@
 namespace fa {
 
 // Kernel launchers. Pointers are device pointers to contiguous [BH][N][d]
-// bf16 tensors (lse, Dvec: [BH][N] fp32); each
-// launcher builds the TMA descriptors its kernel needs. Arguments are assumed
-// validated by the caller. Return the launch (or descriptor) error.
+// bf16 tensors (lse, Dvec: [BH][N] fp32); k, v, dk and dv hold BH / G heads,
+// query head h reading K/V head h / G (G = 1: one K/V head per query head).
+// Each launcher builds the TMA descriptors its kernel needs. Arguments are
+// assumed validated by the caller. Return the launch (or descriptor) error.
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
-                       int N, int d, float scale, bool causal, cudaStream_t stream);
+                       int G, int N, int d, float scale, bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dO, float* Dvec,
                                   int BH, int N, int d, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
-                            void* dv, const float* lse, const float* Dvec, int BH, int N, int d,
+                            void* dv, const float* lse, const float* Dvec, int BH, int G, int N, int d,
                             float scale, bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
-                          const float* lse, const float* Dvec, int BH, int N, int d, float scale,
+                          const float* lse, const float* Dvec, int BH, int G, int N, int d, float scale,
                           bool causal, cudaStream_t stream);
 
 // Device error words (one per translation unit): read, then clear.

@@ -74,7 +74,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                  float* __restrict__ lse, int BH, int N, float scale_log2) {
+                  float* __restrict__ lse, int BH, int G, int N, float scale_log2) {
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   int t, bh;
   grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_qb, HEAD_GROUP, &t, &bh);
   const int qb = n_qb - 1 - t;
+  const int bkv = bh / G;  // K/V head shared by G consecutive query heads
   const int qrow0 = qb * 2 * BM;
   const int n_kt_all = (N + BN - 1) / BN;
   // key tiles per group: group g covers rows qrow0 + 128g .. + 127
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&k_empty[s], ph, err)) break;
         mbar_arrive_expect_tx(&k_full[s], L::TILE_BYTES);
         for (int p = 0; p < L::PANELS; ++p)
-          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &k_full[s], p * 64, j * BN, bh);
+          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &k_full[s], p * 64, j * BN, bkv);
         k_issued = j + 1;
         // V_{j-1} after K_j: V is needed one softmax later than K.
         if (j >= 1) {
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!mbar_wait(&v_empty[sv], ((jv / L::STAGES) & 1) ^ 1, err)) break;
           mbar_arrive_expect_tx(&v_full[sv], L::TILE_BYTES);
           for (int p = 0; p < L::PANELS; ++p)
-            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bh);
+            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bkv);
           v_issued = jv + 1;
         }
       }
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (mbar_wait(&v_empty[sv], ((jv / L::STAGES) & 1) ^ 1, err)) {
           mbar_arrive_expect_tx(&v_full[sv], L::TILE_BYTES);
           for (int p = 0; p < L::PANELS; ++p)
-            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bh);
+            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bkv);
           v_issued = n_kt;
         }
       }
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& to, float* lse, int BH, int N, float scale,
+                            const CUtensorMap& to, float* lse, int BH, int G, int N, float scale,
                             cudaStream_t stream) {
   auto kern = fa_fwd_kernel<D, CAUSAL>;
   const int smem = Smem<D>::ALLOC;
@@ -415,23 +416,24 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
   const int n_qb = (N + 2 * BM - 1) / (2 * BM);
   dim3 grid(static_cast<unsigned>(n_qb) * static_cast<unsigned>(BH));
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, to, lse, BH, N, scale_log2);
+  kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, to, lse, BH, G, N, scale_log2);
   return cudaGetLastError();
 }
 
 }  // namespace fwd
 
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
-                       int N, int d, float scale, bool causal, cudaStream_t stream) {
+                       int G, int N, int d, float scale, bool causal, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_bf16(&tq, q, BH, N, d, fwd::BM) || !make_tmap_bf16(&tk, k, BH, N, d, fwd::BN) ||
-      !make_tmap_bf16(&tv, v, BH, N, d, fwd::BN) || !make_tmap_bf16(&to, o, BH, N, d, fwd::BM))
+  const int BHkv = BH / G;
+  if (!make_tmap_bf16(&tq, q, BH, N, d, fwd::BM) || !make_tmap_bf16(&tk, k, BHkv, N, d, fwd::BN) ||
+      !make_tmap_bf16(&tv, v, BHkv, N, d, fwd::BN) || !make_tmap_bf16(&to, o, BH, N, d, fwd::BM))
     return cudaErrorInvalidValue;
   if (d == 64)
-    return causal ? fwd::launch_t<64, true>(tq, tk, tv, to, lse, BH, N, scale, stream)
-                  : fwd::launch_t<64, false>(tq, tk, tv, to, lse, BH, N, scale, stream);
-  return causal ? fwd::launch_t<128, true>(tq, tk, tv, to, lse, BH, N, scale, stream)
-                : fwd::launch_t<128, false>(tq, tk, tv, to, lse, BH, N, scale, stream);
+    return causal ? fwd::launch_t<64, true>(tq, tk, tv, to, lse, BH, G, N, scale, stream)
+                  : fwd::launch_t<64, false>(tq, tk, tv, to, lse, BH, G, N, scale, stream);
+  return causal ? fwd::launch_t<128, true>(tq, tk, tv, to, lse, BH, G, N, scale, stream)
+                : fwd::launch_t<128, false>(tq, tk, tv, to, lse, BH, G, N, scale, stream);
 }
 
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream) {

@@ -76,10 +76,10 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                                 static_cast<const __nv_bfloat16*>(dO), Dvec, BH, N, d,
                                 s) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (fa::launch_bwd_dkdv(q, k, v, dO, dk, dv, lse, Dvec, BH, N, d, scale, causal != 0, s) !=
+  if (fa::launch_bwd_dkdv(q, k, v, dO, dk, dv, lse, Dvec, BH, 1, N, d, scale, causal != 0, s) !=
       cudaSuccess)
     return FA_ERR_CUDA;
-  if (fa::launch_bwd_dq(q, k, v, dO, dq, lse, Dvec, BH, N, d, scale, causal != 0, s) !=
+  if (fa::launch_bwd_dq(q, k, v, dO, dq, lse, Dvec, BH, 1, N, d, scale, causal != 0, s) !=
       cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;

@@ -35,6 +35,7 @@ class Workload:
     q_std: float = 1.0
     kv_std: float = 1.0
     seed: int = 1000
+    Hkv: int = 0  # K/V heads (grouped-query attention); 0 means H
 
     @property
     def scale(self) -> float:
@@ -44,6 +45,10 @@ class Workload:
     def shape(self):
         return (self.B, self.H, self.N, self.d)
 
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
+
 
 WORKLOADS = {
     "c1": Workload("c1", 1, 1, 256, 64, (False,), ("fwd",), seed=1001),
@@ -51,6 +56,9 @@ WORKLOADS = {
     "c3": Workload("c3", 4, 12, 1028, 64, (False, True), ("fwd",), seed=1003),
     "c4": Workload("c4", 2, 32, 8192, 128, (True,), ("fwd", "bwd"), seed=1004),
     "c5": Workload("c5", 1, 16, 32768, 128, (True,), ("fwd",), q_std=4.0, seed=1005),
+    # grouped-query heads: 32 query heads over 8 K/V heads (Llama-3-8B's head
+    # layout), otherwise the c4 shape
+    "g4": Workload("g4", 2, 32, 8192, 128, (True,), ("fwd", "bwd"), seed=1006, Hkv=8),
 }
 
 WORKLOAD_TITLES = {
@@ -59,16 +67,19 @@ WORKLOAD_TITLES = {
     "c3": "ragged-tile attention fwd B=4 H=12 N=1028 d=64 non-causal and causal",
     "c4": "Llama-shaped attention fwd+bwd B=2 H=32 N=8192 d=128 causal",
     "c5": "long-context attention fwd B=1 H=16 N=32768 d=128 causal, Q ~ N(0, 4^2)",
+    "g4": "grouped-query attention fwd+bwd B=2 H=32 Hkv=8 N=8192 d=128 causal",
 }
 
 
-def make_inputs(B, H, N, d, seed, q_std=1.0, kv_std=1.0, do_std=1.0, with_do=True):
-    """Draw q, k, v (and dO) as bf16 CPU tensors of shape [B, H, N, d]."""
+def make_inputs(B, H, N, d, seed, q_std=1.0, kv_std=1.0, do_std=1.0, with_do=True, Hkv=None):
+    """Draw q, k, v (and dO) as bf16 CPU tensors: q and dO [B, H, N, d], k and
+    v [B, Hkv, N, d] (Hkv = H unless given)."""
     g = torch.Generator().manual_seed(int(seed))
     shape = (B, H, N, d)
+    kv_shape = (B, H if Hkv is None else Hkv, N, d)
     q = (torch.randn(shape, generator=g, dtype=torch.float32) * q_std).to(torch.bfloat16)
-    k = (torch.randn(shape, generator=g, dtype=torch.float32) * kv_std).to(torch.bfloat16)
-    v = (torch.randn(shape, generator=g, dtype=torch.float32) * kv_std).to(torch.bfloat16)
+    k = (torch.randn(kv_shape, generator=g, dtype=torch.float32) * kv_std).to(torch.bfloat16)
+    v = (torch.randn(kv_shape, generator=g, dtype=torch.float32) * kv_std).to(torch.bfloat16)
     out = [q, k, v]
     if with_do:
         do = (torch.randn(shape, generator=g, dtype=torch.float32) * do_std).to(torch.bfloat16)
@@ -80,7 +91,8 @@ def workload_inputs(name: str, with_do=None):
     w = WORKLOADS[name]
     if with_do is None:
         with_do = "bwd" in w.directions
-    return make_inputs(w.B, w.H, w.N, w.d, w.seed, q_std=w.q_std, kv_std=w.kv_std, with_do=with_do)
+    return make_inputs(w.B, w.H, w.N, w.d, w.seed, q_std=w.q_std, kv_std=w.kv_std, with_do=with_do,
+                       Hkv=w.kv_heads)
 
 
 def to_f64(t: torch.Tensor):

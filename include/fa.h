@@ -25,6 +25,8 @@
  * Conventions shared by every entry point
  *   Tensors   q, k, v, o, dO, dq, dk, dv: bf16, contiguous, row-major
  *             [B][H][N][d]; d must be 64 or 128. lse, D: fp32 [B][H][N].
+ *             The _gqa forms (and the backward stages) take k, v, dk, dv as
+ *             [B][Hkv][N][d] (see fa_fwd_gqa).
  *   Pointers  device pointers, each 16-byte aligned. The caller owns every
  *             buffer; the library allocates no memory, never synchronises
  *             the stream (except fa_last_device_error), and launches on
@@ -50,7 +52,7 @@ extern "C" {
 
 typedef enum {
   FA_OK = 0,
-  FA_ERR_INVALID_ARG = 1, /* null pointer, B/H/N < 1, scale not finite or <= 0 */
+  FA_ERR_INVALID_ARG = 1, /* null pointer, B/H/N < 1, Hkv not dividing H, bad scale */
   FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or sizes past 2^31 elements */
   FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch error) */
@@ -69,6 +71,19 @@ typedef enum {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, float scale, int causal, void* stream);
+
+/*
+ * Grouped-query attention forward. k and v hold Hkv heads, [B][Hkv][N][d];
+ * q, o and lse keep H heads. Query head h attends with K/V head h / (H/Hkv):
+ * H/Hkv consecutive query heads share one K/V head. ("07-16 下午" notes,
+ * section 自回归语言模型推理, Prefill、Decode 与推理调度: with grouped-query
+ * attention kv_heads is smaller than the number of query heads, which
+ * shrinks the KV cache; the pages give no head mapping, and consecutive
+ * groups are the usual one.) Hkv must be >= 1 and divide H, else
+ * FA_ERR_INVALID_ARG. fa_fwd is this call with Hkv = H.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Hkv, int N, int d, float scale, int causal, void* stream);
 
 /*
  * Bytes of device workspace fa_bwd needs: the fp32 row vector D [B][H][N]
@@ -92,9 +107,23 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
- * The three backward stages as separate calls (fa_bwd runs all three, in
- * this order, on one stream). They share fa_bwd's argument rules; `Dvec` is
- * fp32 [B][H][N] caller-owned device memory.
+ * Grouped-query attention backward (head mapping and Hkv rules as in
+ * fa_fwd_gqa). k, v, dk, dv are [B][Hkv][N][d]; dk and dv of a K/V head sum
+ * the gradients of every query head that shares it (the dK/dV sweep of one
+ * K/V head runs over all query tiles of its H/Hkv query heads, so the sum
+ * stays in fp32 on chip and needs no atomics). Workspace as for fa_bwd
+ * (fa_bwd_workspace_bytes(B, H, N, d): D has one entry per query row).
+ * fa_bwd is this call with Hkv = H.
+ */
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+               int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * The three backward stages as separate calls (fa_bwd_gqa runs all three,
+ * in this order, on one stream). They share fa_bwd_gqa's argument rules
+ * (Hkv = H for plain multi-head attention); `Dvec` is fp32 [B][H][N]
+ * caller-owned device memory.
  *   fa_bwd_preprocess : Dvec_i = Σ_c dO_ic·O_ic.
  *   fa_bwd_dkdv       : dk = scale·dSᵀ q and dv = Pᵀ dO (bf16, final).
  *   fa_bwd_dq         : dq = scale·dS k (bf16, final).
@@ -102,11 +131,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, int H, int N, int d,
                       void* stream);
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                const float* Dvec, void* dk, void* dv, int B, int H, int N, int d, float scale,
-                int causal, void* stream);
+                const float* Dvec, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+                float scale, int causal, void* stream);
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-              const float* Dvec, void* dq, int B, int H, int N, int d, float scale, int causal,
-              void* stream);
+              const float* Dvec, void* dq, int B, int H, int Hkv, int N, int d, float scale,
+              int causal, void* stream);
 
 /* Size in bytes of the static scratch area behind fa_bwd_noalloc (32 MiB). */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

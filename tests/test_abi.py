@@ -88,10 +88,31 @@ def test_bwd_argument_errors(L):
     assert call(workspace=MIS) == 3
     # stage entry points
     assert L.fa_bwd_preprocess(FAKE, FAKE, NUL, 1, 1, 16, 64, NUL) == 1
-    assert L.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MIS, 1, 1, 16, 64,
+    assert L.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MIS, 1, 1, 1, 16, 64,
                          0.125, 0, NUL) == 3
-    assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0.0, 1, NUL) == 1
-    assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 96, 0.1, 1, NUL) == 2
+    assert L.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 3, 16, 64,
+                         0.125, 0, NUL) == 1  # 3 K/V heads cannot serve 4 query heads
+    assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 16, 64, 0.0, 1, NUL) == 1
+    assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 16, 96, 0.1, 1, NUL) == 2
+    assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 0, 16, 64, 0.1, 1, NUL) == 1
+
+
+def test_gqa_argument_errors(L):
+    def fwd(H=8, Hkv=2, k=FAKE):
+        return L.fa_fwd_gqa(FAKE, k, FAKE, FAKE, FAKE, 1, H, Hkv, 16, 64, 0.125, 1, NUL)
+
+    def bwd(H=8, Hkv=2, dk=FAKE):
+        ws = L.fa_bwd_workspace_bytes(1, H, 16, 64)
+        return L.fa_bwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dk, FAKE, FAKE, ws,
+                            1, H, Hkv, 16, 64, 0.125, 1, NUL)
+
+    for call in (fwd, bwd):
+        assert call(Hkv=0) == 1
+        assert call(Hkv=3) == 1       # does not divide H
+        assert call(Hkv=16) == 1      # more K/V heads than query heads
+        assert call(H=8, Hkv=-8) == 1
+    assert fwd(k=NUL) == 1 and fwd(k=MIS) == 3
+    assert bwd(dk=NUL) == 1
 
 
 def test_product_path_does_not_import_the_oracle():
