@@ -24,6 +24,8 @@ __all__ = [
     "bwd_dq",
     "bwd_workspace_bytes",
     "last_device_error",
+    "softmax_safe",
+    "softmax_online",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -54,6 +56,8 @@ EXPORTED_SYMBOLS = (
     "fa_status_string",
     "fa_version",
     "fa_bwd_noalloc",
+    "fa_softmax_safe",
+    "fa_softmax_online",
 )
 
 
@@ -93,6 +97,10 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_dq.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
+        L.fa_softmax_safe.argtypes = [vp, vp, ctypes.c_longlong, i, vp]
+        L.fa_softmax_safe.restype = i
+        L.fa_softmax_online.argtypes = [vp, vp, ctypes.c_longlong, i, vp]
+        L.fa_softmax_online.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
         L.fa_status_string.argtypes = [i]
@@ -207,3 +215,23 @@ def last_device_error(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device error status."""
     dev = torch.device("cuda") if device is None else device
     return int(lib().fa_last_device_error(_stream(dev)))
+
+
+def _softmax(fn, name, x, out):
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous() or x.dim() < 1:
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    n = x.shape[-1]
+    rows = x.numel() // n if n else 0
+    y = torch.empty_like(x) if out is None else out
+    _check(fn(_ptr(x), _ptr(y), rows, n, _stream(x.device)), name)
+    return y
+
+
+def softmax_safe(x, out=None):
+    """Softmax over the last dimension of fp32 x, three passes per row."""
+    return _softmax(lib().fa_softmax_safe, "fa_softmax_safe", x, out)
+
+
+def softmax_online(x, out=None):
+    """Softmax over the last dimension of fp32 x, two passes per row (online)."""
+    return _softmax(lib().fa_softmax_online, "fa_softmax_online", x, out)

@@ -146,6 +146,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
                     causal, stream);
 }
 
+static int softmax_rows(const float* x, float* y, long long rows, int n, bool online, void* stream) {
+  if (!x || !y || rows < 1 || n < 1) return FA_ERR_INVALID_ARG;
+  if (rows > INT_MAX) return FA_ERR_UNSUPPORTED;  // one CTA per row in a 1-D grid
+  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  return map_cuda(fa::launch_softmax(x, y, rows, n, online, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_softmax_safe(const float* x, float* y, long long rows, int n, void* stream) {
+  return softmax_rows(x, y, rows, n, false, stream);
+}
+
+int fa_softmax_online(const float* x, float* y, long long rows, int n, void* stream) {
+  return softmax_rows(x, y, rows, n, true, stream);
+}
+
 int fa_last_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t ef = 0, eb = 0;

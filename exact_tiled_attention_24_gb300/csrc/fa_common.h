@@ -25,6 +25,11 @@ cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const voi
                           const float* lse, const float* Dvec, int BH, int G, int N, int d, float scale,
                           bool causal, cudaStream_t stream);
 
+// Row softmax of x [rows][n] fp32 into y (may alias x): three passes (safe)
+// or two (online). One CTA per row.
+cudaError_t launch_softmax(const float* x, float* y, long long rows, int n, bool online,
+                           cudaStream_t stream);
+
 // Device error words (one per translation unit): read, then clear.
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream);

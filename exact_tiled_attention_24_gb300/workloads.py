@@ -95,6 +95,33 @@ def workload_inputs(name: str, with_do=None):
                        Hkv=w.kv_heads)
 
 
+@dataclass(frozen=True)
+class RowsWorkload:
+    """Rows for the standalone softmax kernels: x [rows, n] fp32 ~ N(0, std²).
+    rows is a multiple of 608 (152 SMs x 4 resident 512-thread CTAs), so the
+    one-CTA-per-row grid fills whole waves."""
+    name: str
+    rows: int
+    n: int
+    std: float
+    seed: int
+
+
+ROW_WORKLOADS = {
+    # 1 MB rows: 608 rows in flight hold ~600 MB, so a pass's re-read of its
+    # row misses the 126 MB L2 and goes to DRAM
+    "s1": RowsWorkload("s1", 1216, 262144, 4.0, 2001),
+    # 128 KB rows: ~78 MB in flight, so the re-reads can hit L2
+    "s2": RowsWorkload("s2", 9728, 32768, 4.0, 2002),
+}
+
+
+def make_rows(rows, n, seed, std=1.0):
+    """Draw x [rows, n] fp32 on the CPU from the seeded generator."""
+    g = torch.Generator().manual_seed(int(seed))
+    return torch.randn((rows, n), generator=g, dtype=torch.float32) * std
+
+
 def to_f64(t: torch.Tensor):
     """bf16 tensor -> exact float64 numpy array (bf16 values are exact in fp64)."""
     return t.detach().to("cpu").to(torch.float64).numpy()

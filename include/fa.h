@@ -171,6 +171,29 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    float scale, int causal, void* stream);
 
 /*
+ * Row softmax, y_ij = e^(x_ij − m_i) / Σ_j e^(x_ij − m_i) with m_i = max_j
+ * x_ij, over x [rows][n] fp32 (row-major, contiguous) into y [rows][n] fp32.
+ * y may equal x (in place). Two ways of reaching the same result:
+ *   fa_softmax_safe    three passes over each row (maximum; sum of
+ *                      e^(x − m); output), the safe softmax of the dcwnkz.com
+ *                      GPU-tricks article (appendix on softmax) and of the
+ *                      CMU 10-423 L17–L18 notes (section 前置二：online softmax);
+ *   fa_softmax_online  two passes: the running maximum and the running
+ *                      denominator in one pass, the denominator rescaled by
+ *                      e^(m_old − m_new) whenever the maximum grows (same CMU
+ *                      section), then the output pass.
+ * Exponentials use the hardware 2^x approximation; results match the exact
+ * softmax to a few units in the last place of fp32 per element (the sum
+ * adds rounding that grows with n). A row of only -inf gives NaN.
+ * Errors: null pointer, rows < 1 or n < 1 -> FA_ERR_INVALID_ARG; rows >
+ * 2^31 - 1 -> FA_ERR_UNSUPPORTED; x or y not 4-byte aligned ->
+ * FA_ERR_MISALIGNED. 16-byte loads are used when n % 4 == 0 and both
+ * pointers are 16-byte aligned.
+ */
+int fa_softmax_safe(const float* x, float* y, long long rows, int n, void* stream);
+int fa_softmax_online(const float* x, float* y, long long rows, int n, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word set by
  * any kernel of this library on the current device. Returns FA_OK,
  * FA_ERR_TIMEOUT (a pipeline wait gave up; outputs of the calls since the

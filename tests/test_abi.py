@@ -122,3 +122,13 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle", text, flags=re.M), f
+
+
+def test_softmax_argument_errors(L):
+    for fn in (L.fa_softmax_safe, L.fa_softmax_online):
+        assert fn(NUL, FAKE, 4, 16, NUL) == 1
+        assert fn(FAKE, NUL, 4, 16, NUL) == 1
+        assert fn(FAKE, FAKE, 0, 16, NUL) == 1
+        assert fn(FAKE, FAKE, 4, 0, NUL) == 1
+        assert fn(FAKE, FAKE, 2**31, 16, NUL) == 2
+        assert fn(ctypes.c_void_p(0x10001), FAKE, 4, 16, NUL) == 3
