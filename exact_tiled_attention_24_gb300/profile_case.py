@@ -1,7 +1,8 @@
 """Run the forward + backward a few times on one shape, for profiler captures.
 
     python -m exact_tiled_attention_24_gb300.profile_case --B 1 --H 32 --N 4096 --d 128 \
-        --causal --iters 2
+        --causal --iters 2 [--Hkv 8]
+    python -m exact_tiled_attention_24_gb300.profile_case --softmax-rows 1216 --softmax-n 262144
 
 Inputs come from the seeded workload generator; nothing is checked or timed.
 """
@@ -19,17 +20,30 @@ def main():
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--Hkv", type=int, default=0, help="K/V heads (grouped-query); 0 = H")
+    ap.add_argument("--softmax-rows", type=int, default=0, help="run the row softmax kernels instead")
+    ap.add_argument("--softmax-n", type=int, default=262144)
     args = ap.parse_args()
 
     import torch
 
     import exact_tiled_attention_24_gb300 as fa
     from exact_tiled_attention_24_gb300 import build
-    from exact_tiled_attention_24_gb300.workloads import make_inputs
+    from exact_tiled_attention_24_gb300.workloads import make_inputs, make_rows
 
     build.build()
     dev = torch.device("cuda")
-    q, k, v, do = (t.to(dev) for t in make_inputs(args.B, args.H, args.N, args.d, seed=99))
+    if args.softmax_rows:
+        x = make_rows(args.softmax_rows, args.softmax_n, seed=99, std=4.0).to(dev)
+        y = torch.empty_like(x)
+        for _ in range(args.iters):
+            fa.softmax_online(x, out=y)
+            fa.softmax_safe(x, out=y)
+        torch.cuda.synchronize()
+        print("ok")
+        return
+    q, k, v, do = (t.to(dev) for t in make_inputs(args.B, args.H, args.N, args.d, seed=99,
+                                                   Hkv=args.Hkv or None))
     for _ in range(args.iters):
         o, lse = fa.fwd(q, k, v, causal=args.causal)
         if not args.fwd_only:
