@@ -13,6 +13,9 @@ from .attention import (  # noqa: F401
     attention_fwd,
     attention_fwd_gqa,
     attention_fwd_head,
+    attention_merge,
+    decode_paged,
+    gather_paged,
     attention_pairs,
     kv_head_of,
     softmax_blocks_naive_sum,

@@ -249,6 +249,83 @@ def attention_bwd_gqa(q, k, v, do, scale, causal):
 
 
 # --------------------------------------------------------------------------
+# merging partial attention over disjoint key blocks
+# --------------------------------------------------------------------------
+# "07-16 下午" notes, section 长上下文与序列并行: partial softmax results of
+# different K/V blocks cannot be normalised separately and added, because
+# the global denominator depends on every block.  Carry the running maximum
+# m, the normaliser l and the weighted sum u; when a block arrives, rescale
+# the old l and u by e^(m_old - m_new) and add the block's.  A partial result
+# over a block is stored as (o_s, lse_s) with o_s = u_s / l_s and
+# lse_s = m_s + ln l_s, i.e. the block state (m, l, u) = (lse_s, 1, o_s).
+
+def attention_merge(o_parts, lse_parts):
+    """o_parts [S, rows, d], lse_parts [S, rows] (natural log; -inf for a
+    part that saw no key) -> o [rows, d], lse [rows], processing the parts
+    in order with the rescaling recurrence above."""
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    rows, d = o_parts.shape[1], o_parts.shape[2]
+    m = np.full(rows, -np.inf)
+    l = np.zeros(rows)
+    u = np.zeros((rows, d))
+    for o_s, lse_s in zip(o_parts, lse_parts):
+        m_new = np.maximum(m, lse_s)
+        live = np.isfinite(m_new)  # some part so far saw a key
+        with np.errstate(invalid="ignore"):
+            a_old = np.where(live, np.exp(np.where(live, m - m_new, 0.0)), 0.0)
+            a_new = np.where(live, np.exp(np.where(live, lse_s - m_new, 0.0)), 0.0)
+        l = l * a_old + a_new
+        u = u * a_old[:, None] + o_s * a_new[:, None]
+        m = m_new
+    with np.errstate(divide="ignore", invalid="ignore"):
+        o = np.where(l[:, None] > 0, u / np.where(l > 0, l, 1.0)[:, None], 0.0)
+        lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return o, lse
+
+
+# --------------------------------------------------------------------------
+# decode against a paged KV cache
+# --------------------------------------------------------------------------
+# CMU 10-423 L17–L18 notes, section 解碼端：PagedAttention: the KV cache is cut
+# into blocks of a fixed number of tokens stored non-contiguously, and a
+# block table maps a sequence's logical blocks to physical ones.  "07-16
+# 下午" notes, section Prefill、Decode 与推理调度: a decode step feeds one new
+# token per request, whose query attends to the keys and values of every
+# cached token of that request (the new token's own included).
+# Layout read here (the pages fix none): k_cache, v_cache
+# [num_blocks, Hkv, block_size, d]; token t of request b sits in physical
+# block block_table[b, t // block_size], slot t % block_size.
+
+def gather_paged(cache, block_table_row, seq_len):
+    """Contiguous [Hkv, seq_len, d] copy of one request's cached keys or values."""
+    bs = cache.shape[2]
+    t = np.arange(seq_len)
+    blocks = np.asarray(block_table_row)[t // bs]
+    return cache[blocks, :, t % bs, :].transpose(1, 0, 2)
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale):
+    """q [B, H, d] (one query row per request) -> o [B, H, d], lse [B, H].
+    Query head h reads K/V head h // (H / Hkv)."""
+    B, H, d = q.shape
+    Hkv = k_cache.shape[1]
+    o = np.zeros((B, H, d))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        K = gather_paged(k_cache, block_table[b], L)
+        V = gather_paged(v_cache, block_table[b], L)
+        for h in range(H):
+            g = kv_head_of(h, H, Hkv)
+            ob, lb = attention_fwd_head(q[b, h][None, :], K[g], V[g], scale, False)
+            o[b, h], lse[b, h] = ob[0], lb[0]
+    return o, lse
+
+
+# --------------------------------------------------------------------------
 # FLOP convention used when this oracle is timed
 # --------------------------------------------------------------------------
 
