@@ -26,6 +26,9 @@ __all__ = [
     "last_device_error",
     "softmax_safe",
     "softmax_online",
+    "attn_merge",
+    "decode_paged",
+    "decode_workspace_bytes",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -41,6 +44,7 @@ FA_STATUS = {
     4: "FA_ERR_CUDA",
     5: "FA_ERR_TIMEOUT",
     6: "FA_ERR_WORKSPACE",
+    7: "FA_ERR_BAD_INDEX",
 }
 
 EXPORTED_SYMBOLS = (
@@ -58,6 +62,9 @@ EXPORTED_SYMBOLS = (
     "fa_bwd_noalloc",
     "fa_softmax_safe",
     "fa_softmax_online",
+    "fa_attn_merge",
+    "fa_decode_workspace_bytes",
+    "fa_decode_paged",
 )
 
 
@@ -101,6 +108,12 @@ def lib() -> ctypes.CDLL:
         L.fa_softmax_safe.restype = i
         L.fa_softmax_online.argtypes = [vp, vp, ctypes.c_longlong, i, vp]
         L.fa_softmax_online.restype = i
+        L.fa_attn_merge.argtypes = [vp, vp, i, vp, vp, ctypes.c_longlong, i, vp]
+        L.fa_attn_merge.restype = i
+        L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
+        L.fa_decode_workspace_bytes.restype = sz
+        L.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, i, f, i, vp]
+        L.fa_decode_paged.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
         L.fa_status_string.argtypes = [i]
@@ -235,3 +248,51 @@ def softmax_safe(x, out=None):
 def softmax_online(x, out=None):
     """Softmax over the last dimension of fp32 x, two passes per row (online)."""
     return _softmax(lib().fa_softmax_online, "fa_softmax_online", x, out)
+
+
+def attn_merge(o_parts, lse_parts, out=None, lse=None):
+    """Combine partial attention results: o_parts [S, rows, d] fp32, lse_parts
+    [S, rows] fp32 -> (o [rows, d] bf16, lse [rows] fp32)."""
+    S, rows, d = o_parts.shape
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise ValueError("o_parts and lse_parts must be float32")
+    if lse_parts.shape != (S, rows) or not (o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("lse_parts must be a contiguous [S, rows] tensor beside contiguous o_parts")
+    o = torch.empty((rows, d), dtype=torch.bfloat16, device=o_parts.device) if out is None else out
+    lse_t = torch.empty((rows,), dtype=torch.float32, device=o_parts.device) if lse is None else lse
+    _check(lib().fa_attn_merge(_ptr(o_parts), _ptr(lse_parts), S, _ptr(o), _ptr(lse_t), rows, d,
+                               _stream(o_parts.device)), "fa_attn_merge")
+    return o, lse_t
+
+
+def decode_workspace_bytes(B, H, d, n_splits) -> int:
+    return int(lib().fa_decode_workspace_bytes(B, H, d, n_splits))
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, n_splits=1, scale=None, workspace=None,
+                 out=None, lse=None):
+    """One decode step: q [B, H, d] bf16 against the paged cache k_cache,
+    v_cache [num_blocks, Hkv, block_size, d] bf16, with block_table
+    [B, max_blocks] int32 and seq_lens [B] int32. Returns (o [B, H, d] bf16,
+    lse [B, H] fp32)."""
+    B, H, d = q.shape
+    num_blocks, Hkv, bs, dk = k_cache.shape
+    for t in (q, k_cache, v_cache):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k_cache, v_cache must be contiguous bfloat16 CUDA tensors")
+    if v_cache.shape != k_cache.shape or dk != d:
+        raise ValueError("k_cache and v_cache must be [num_blocks, Hkv, block_size, d]")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32 or block_table.dim() != 2 \
+            or block_table.shape[0] != B or seq_lens.shape != (B,) or not block_table.is_contiguous():
+        raise ValueError("block_table [B, max_blocks] and seq_lens [B] must be int32")
+    ws_bytes = decode_workspace_bytes(B, H, d, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+                                 _ptr(o), _ptr(lse_t), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), B, H, Hkv, d, num_blocks, bs,
+                                 block_table.shape[1], _scale(d, scale), n_splits, _stream(q.device)),
+           "fa_decode_paged")
+    return o, lse_t

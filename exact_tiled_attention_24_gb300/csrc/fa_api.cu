@@ -53,6 +53,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_BAD_INDEX: return "FA_ERR_BAD_INDEX";
     default: return "FA_ERR_UNKNOWN";
   }
 }
@@ -162,12 +163,71 @@ int fa_softmax_online(const float* x, float* y, long long rows, int n, void* str
   return softmax_rows(x, y, rows, n, true, stream);
 }
 
+// ------------------------------------------------------------------ decode
+
+size_t fa_decode_workspace_bytes(int B, int H, int d, int n_splits) {
+  if (B < 1 || H < 1 || n_splits < 1 || (d != 64 && d != 128)) return 0;
+  const size_t rows = static_cast<size_t>(n_splits) * B * H;
+  const size_t o_bytes = (rows * d * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  return o_bytes + rows * sizeof(float);
+}
+
+int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                    const int* seq_lens, void* o, float* lse, void* workspace, size_t ws_bytes, int B,
+                    int H, int Hkv, int d, int num_blocks, int block_size, int max_blocks_per_seq,
+                    float scale, int n_splits, void* stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || num_blocks < 1 || block_size < 1 || max_blocks_per_seq < 1 || n_splits < 1)
+    return FA_ERR_INVALID_ARG;
+  int st = check_heads(H, Hkv);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (H / Hkv > 16 || B > 65535 || Hkv > 65535 || n_splits > 4096) return FA_ERR_UNSUPPORTED;
+  const long long ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+  if (ctx > INT_MAX / 2 || static_cast<long long>(num_blocks) * Hkv * block_size * d > (1ll << 40))
+    return FA_ERR_UNSUPPORTED;
+  // Block-table entries one split can touch.
+  const long long T = fa::kDecodeTileKeys;
+  const long long tiles = (ctx + T - 1) / T;
+  const long long per_split = (tiles + n_splits - 1) / n_splits * T;
+  if ((per_split + block_size - 1) / block_size + 1 > fa::kDecodeMaxTable) return FA_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < fa_decode_workspace_bytes(B, H, d, n_splits)) return FA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return FA_ERR_MISALIGNED;
+  const size_t rows = static_cast<size_t>(n_splits) * B * H;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             ((rows * d * sizeof(float) + 255) & ~static_cast<size_t>(255)));
+  return map_cuda(fa::launch_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, o_part,
+                                          lse_part, B, H, Hkv, d, num_blocks, block_size,
+                                          max_blocks_per_seq, scale, n_splits,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int fa_attn_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse,
+                  long long rows, int d, void* stream) {
+  if (!o_parts || !lse_parts || !o || !lse || n_parts < 1 || rows < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((rows + 7) / 8 > INT_MAX) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(o_parts) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_MISALIGNED;
+  return map_cuda(fa::launch_attn_merge(o_parts, lse_parts, n_parts, o, lse, rows, d,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 int fa_last_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t ef = 0, eb = 0;
+  uint32_t ef = 0, eb = 0, ed = 0;
   if (fa::read_and_clear_fwd_error(&ef, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_and_clear_bwd_error(&eb, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (ef || eb) return FA_ERR_TIMEOUT;
+  if (fa::read_and_clear_decode_error(&ed, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (ef == 1 || eb == 1 || ed == 1) return FA_ERR_TIMEOUT;
+  if (ed == 2) return FA_ERR_BAD_INDEX;
+  if (ef || eb || ed) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
 

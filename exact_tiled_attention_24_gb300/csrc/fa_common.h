@@ -30,8 +30,28 @@ cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const voi
 cudaError_t launch_softmax(const float* x, float* y, long long rows, int n, bool online,
                            cudaStream_t stream);
 
+// Block-table entries one decode split may use (its slice is staged in
+// shared memory); the host rejects splits that could need more.
+constexpr int kDecodeMaxTable = 1024;
+constexpr int kDecodeTileKeys = 64;
+
+// Decode of one new query row per request against a paged KV cache
+// (k_cache, v_cache [num_blocks][Hkv][block_size][d] bf16), split over the
+// context into S parts, partial results in o_part [S][B*H][d] fp32 and
+// lse_part [S][B*H], then merged into o [B*H][d] bf16 and lse [B*H].
+cudaError_t launch_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int* block_table, const int* seq_lens, void* o, float* lse,
+                                float* o_part, float* lse_part, int B, int H, int Hkv, int d,
+                                int num_blocks, int block_size, int max_blocks, float scale, int S,
+                                cudaStream_t stream);
+// Merge S partial attention results per row: o_parts [S][rows][d] fp32,
+// lse_parts [S][rows] -> o [rows][d] bf16, lse [rows].
+cudaError_t launch_attn_merge(const float* o_parts, const float* lse_parts, int S, void* o, float* lse,
+                              long long rows, int d, cudaStream_t stream);
+
 // Device error words (one per translation unit): read, then clear.
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream);
+cudaError_t read_and_clear_decode_error(uint32_t* out, cudaStream_t stream);
 
 }  // namespace fa

@@ -14,7 +14,7 @@
 namespace fa {
 
 // Error word values written by device code (host maps them to fa_status).
-enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1 };
+enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 
 // Upper bound on any single mbarrier wait, in nanoseconds of %globaltimer.
 // No wait in these kernels legitimately takes more than microseconds.
@@ -120,6 +120,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
       "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Non-tensor bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing its bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 

@@ -57,7 +57,8 @@ typedef enum {
   FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch error) */
   FA_ERR_TIMEOUT = 5,     /* device pipeline wait exceeded its limit */
-  FA_ERR_WORKSPACE = 6    /* workspace pointer null or smaller than required */
+  FA_ERR_WORKSPACE = 6,   /* workspace pointer null or smaller than required */
+  FA_ERR_BAD_INDEX = 7    /* (device) a block-table entry outside [0, num_blocks) */
 } fa_status;
 
 /*
@@ -194,10 +195,69 @@ int fa_softmax_safe(const float* x, float* y, long long rows, int n, void* strea
 int fa_softmax_online(const float* x, float* y, long long rows, int n, void* stream);
 
 /*
+ * Merge of partial attention results over disjoint key blocks ("07-16 下午"
+ * notes, section 长上下文与序列并行: blocks are not normalised separately and
+ * added; each block's normaliser and weighted sum are rescaled by
+ * e^(m_block − m_global) first). For each row r:
+ *     lse_r = ln Σ_s e^(lse_parts[s][r]),
+ *     o_r   = Σ_s e^(lse_parts[s][r] − lse_r) · o_parts[s][r][:]
+ *   o_parts    [n_parts][rows][d] fp32, each part normalised within its own
+ *              keys (o_s = Σ_j e^(x_j − lse_s) v_j over the part's keys);
+ *   lse_parts  [n_parts][rows] fp32 natural log; -inf marks a part with no
+ *              key (weight 0);
+ *   o          [rows][d] bf16 output, lse [rows] fp32 output. A row whose
+ *              parts are all -inf gets o = 0, lse = -inf.
+ * Errors: null pointer, n_parts or rows < 1 -> FA_ERR_INVALID_ARG; d not 64
+ * or 128 -> FA_ERR_UNSUPPORTED; o_parts or o not 16-byte aligned, lse_parts
+ * or lse not 4-byte aligned -> FA_ERR_MISALIGNED.
+ */
+int fa_attn_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse,
+                  long long rows, int d, void* stream);
+
+/*
+ * Decode step against a paged KV cache. A paged cache (CMU 10-423 notes,
+ * section 解碼端：PagedAttention) cuts each request's keys and values into
+ * blocks of block_size tokens stored anywhere; a block table maps the
+ * request's logical block i to a physical block. In a decode step ("07-16
+ * 下午" notes, section Prefill、Decode 与推理调度) each request brings one new
+ * token whose query attends to all of that request's cached tokens; the
+ * caller has already written the new token's key and value into the cache.
+ *   q            [B][H][d] bf16: the new token's query rows.
+ *   k_cache,     [num_blocks][Hkv][block_size][d] bf16 each: token t of
+ *   v_cache      request b is in block block_table[b][t / block_size], slot
+ *                t % block_size (layout chosen here; the pages fix none).
+ *   block_table  [B][max_blocks_per_seq] int32 device array.
+ *   seq_lens     [B] int32 device array: cached tokens per request (clamped
+ *                to [0, max_blocks_per_seq·block_size]; 0 gives o = 0,
+ *                lse = -inf).
+ *   o, lse       [B][H][d] bf16 and [B][H] fp32 outputs: attention of each
+ *                query row over its request's tokens (no mask beyond the
+ *                context length); query head h reads K/V head h / (H/Hkv).
+ *   workspace    device buffer of fa_decode_workspace_bytes(B, H, d,
+ *                n_splits) bytes (16-byte aligned), for the partial results.
+ *   n_splits     the context of every request is cut into n_splits parts of
+ *                whole 64-token tiles, processed in parallel and combined
+ *                as in fa_attn_merge (two kernels on `stream`).
+ * Errors: null pointer, sizes < 1, Hkv not dividing H, bad scale ->
+ * FA_ERR_INVALID_ARG; d not 64/128, H/Hkv > 16, B or Hkv > 65535, a split
+ * that could span more than 1024 cache blocks (use more splits) ->
+ * FA_ERR_UNSUPPORTED; short workspace -> FA_ERR_WORKSPACE; misaligned ->
+ * FA_ERR_MISALIGNED. A block-table entry outside [0, num_blocks) is never
+ * dereferenced: the tokens it maps are skipped (the results are then
+ * undefined) and fa_last_device_error reports FA_ERR_BAD_INDEX.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int d, int n_splits);
+int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                    const int* seq_lens, void* o, float* lse, void* workspace, size_t ws_bytes, int B,
+                    int H, int Hkv, int d, int num_blocks, int block_size, int max_blocks_per_seq,
+                    float scale, int n_splits, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word set by
  * any kernel of this library on the current device. Returns FA_OK,
  * FA_ERR_TIMEOUT (a pipeline wait gave up; outputs of the calls since the
- * last check are undefined) or FA_ERR_CUDA.
+ * last check are undefined), FA_ERR_BAD_INDEX (a decode block table pointed
+ * outside the cache) or FA_ERR_CUDA.
  */
 int fa_last_device_error(void* stream);
 

@@ -132,3 +132,38 @@ def test_softmax_argument_errors(L):
         assert fn(FAKE, FAKE, 4, 0, NUL) == 1
         assert fn(FAKE, FAKE, 2**31, 16, NUL) == 2
         assert fn(ctypes.c_void_p(0x10001), FAKE, 4, 16, NUL) == 3
+
+
+def test_decode_and_merge_argument_errors(L):
+    ws = L.fa_decode_workspace_bytes(2, 8, 128, 4)
+    assert ws >= 4 * 2 * 8 * 128 * 4 + 4 * 2 * 8 * 4
+    assert L.fa_decode_workspace_bytes(2, 8, 96, 4) == 0
+
+    def dec(q=FAKE, table=FAKE, ws_ptr=FAKE, ws_bytes=ws, B=2, H=8, Hkv=2, d=128, num_blocks=10, bs=16,
+            max_blocks=8, scale=0.1, S=4):
+        return L.fa_decode_paged(q, FAKE, FAKE, table, FAKE, FAKE, FAKE, ws_ptr, ws_bytes, B, H, Hkv, d,
+                                 num_blocks, bs, max_blocks, scale, S, NUL)
+
+    assert dec(q=NUL) == 1
+    assert dec(table=NUL) == 1
+    assert dec(Hkv=3) == 1
+    assert dec(S=0) == 1
+    assert dec(bs=0) == 1
+    assert dec(scale=-1.0) == 1
+    assert dec(d=96) == 2
+    assert dec(H=32, Hkv=1) == 2              # 32 query heads on one K/V head
+    assert dec(max_blocks=100000, S=1) == 2   # a split could span > 1024 blocks
+    assert dec(ws_ptr=NUL) == 6
+    assert dec(ws_bytes=ws - 1) == 6
+    assert dec(q=MIS) == 3
+    assert dec(table=ctypes.c_void_p(0x10002)) == 3
+
+    def merge(o_parts=FAKE, n=3, rows=10, d=64):
+        return L.fa_attn_merge(o_parts, FAKE, n, FAKE, FAKE, rows, d, NUL)
+
+    assert merge(o_parts=NUL) == 1
+    assert merge(n=0) == 1
+    assert merge(rows=0) == 1
+    assert merge(d=80) == 2
+    assert merge(o_parts=MIS) == 3
+    assert L.fa_status_string(7) == b"FA_ERR_BAD_INDEX"

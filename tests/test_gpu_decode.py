@@ -1,0 +1,105 @@
+"""Paged-KV decode and partial-attention merge: CUDA kernels (through the C
+ABI) against the fp64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+from exact_tiled_attention_24_gb300.workloads import to_f64
+from oracle import attention_merge, decode_paged
+from gpu_helpers import assert_lse, assert_o
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from exact_tiled_attention_24_gb300 import build
+    build.build()
+    import exact_tiled_attention_24_gb300 as m
+    return m
+
+
+def paged_case(B, H, Hkv, d, bs, seq_lens, seed, spare_blocks=3):
+    """Seeded bf16 q and a paged cache with a random physical placement of
+    every request's blocks (unused slots hold other random values)."""
+    g = torch.Generator().manual_seed(seed)
+    nb = [(L + bs - 1) // bs for L in seq_lens]
+    total = sum(nb) + spare_blocks
+    q = torch.randn((B, H, d), generator=g).to(torch.bfloat16)
+    kc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16)
+    perm = torch.randperm(total, generator=g)
+    table = torch.zeros((B, max(max(nb), 1)), dtype=torch.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :nb[b]] = perm[pos:pos + nb[b]].to(torch.int32)
+        pos += nb[b]
+    return q, kc, vc, table, torch.tensor(seq_lens, dtype=torch.int32)
+
+
+def run_case(fa, q, kc, vc, table, lens, n_splits, scale):
+    o, lse = fa.decode_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), lens.cuda(),
+                             n_splits=n_splits, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("B,H,Hkv,d,bs,seq_lens,n_splits", [
+    (3, 4, 4, 64, 16, [1, 17, 100], 1),
+    (3, 8, 2, 128, 16, [1, 64, 1000], 4),
+    (2, 8, 1, 128, 32, [5000, 333], 8),
+    (2, 4, 2, 64, 1, [50, 7], 2),           # one token per block
+    (2, 32, 8, 128, 128, [4097, 256], 3),
+    (1, 16, 1, 128, 16, [777], 5),           # 16 query heads on one K/V head
+    (3, 4, 2, 128, 16, [0, 1, 129], 2),      # an empty context
+    (1, 2, 1, 64, 48, [2000], 7),            # block size not a power of two
+])
+def test_decode_paged_vs_oracle(fa, B, H, Hkv, d, bs, seq_lens, n_splits):
+    q, kc, vc, table, lens = paged_case(B, H, Hkv, d, bs, seq_lens, seed=B * 100 + H + bs + sum(seq_lens))
+    scale = d ** -0.5
+    o, lse = run_case(fa, q, kc, vc, table, lens, n_splits, scale)
+    ro, rlse = decode_paged(to_f64(q), to_f64(kc), to_f64(vc), table.numpy(), lens.numpy(), scale)
+    live = lens.numpy() > 0
+    assert_o(o[live], ro[live])
+    assert_lse(lse[live], rlse[live])
+    if not live.all():  # no cached token: o = 0, lse = -inf
+        assert torch.all(o[~torch.from_numpy(live)].float() == 0)
+        assert torch.all(torch.isneginf(lse[~torch.from_numpy(live)]))
+
+
+def test_decode_split_count_does_not_change_the_result(fa):
+    q, kc, vc, table, lens = paged_case(4, 8, 2, 128, 16, [3000, 10, 640, 2049], seed=7)
+    outs = [run_case(fa, q, kc, vc, table, lens, S, 0.1) for S in (1, 2, 7, 40)]
+    for o, lse in outs[1:]:
+        assert (o.float() - outs[0][0].float()).abs().max() <= 2e-2
+        assert (lse - outs[0][1]).abs().max() <= 1e-4
+
+
+def test_decode_bad_block_index_is_reported_not_read(fa):
+    q, kc, vc, table, lens = paged_case(2, 4, 2, 64, 16, [40, 40], seed=9)
+    table[1, 1] = kc.shape[0] + 5  # outside the cache
+    fa.decode_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), lens.cuda(), n_splits=2)
+    assert fa.last_device_error() == 7  # FA_ERR_BAD_INDEX
+    assert fa.last_device_error() == 0  # read and cleared
+    # request 0 does not use the bad entry and is still right
+    o, lse = run_case(fa, q[:1].contiguous(), kc, vc, table[:1].contiguous(), lens[:1].contiguous(), 2, 0.125)
+    ro, rlse = decode_paged(to_f64(q[:1]), to_f64(kc), to_f64(vc), table[:1].numpy(), lens[:1].numpy(), 0.125)
+    assert_o(o, ro)
+
+
+@pytest.mark.parametrize("S,rows,d", [(1, 5, 64), (3, 300, 128), (17, 64, 128)])
+def test_merge_vs_oracle(fa, S, rows, d):
+    g = torch.Generator().manual_seed(S * 1000 + rows + d)
+    o_parts = torch.randn((S, rows, d), generator=g)
+    lse_parts = torch.randn((S, rows), generator=g) * 5
+    lse_parts[0, ::4] = float("-inf")       # parts that saw no key
+    if S > 1:
+        lse_parts[:, 1] = float("-inf")      # a row with no key at all
+    o, lse = fa.attn_merge(o_parts.cuda(), lse_parts.cuda())
+    torch.cuda.synchronize()
+    ro, rlse = attention_merge(o_parts.double().numpy(), lse_parts.double().numpy())
+    np.testing.assert_allclose(o.float().cpu().numpy(), ro, rtol=1e-2, atol=1e-2)
+    fin = np.isfinite(rlse)
+    np.testing.assert_allclose(lse.cpu().numpy()[fin], rlse[fin], rtol=0, atol=1e-4)
+    assert np.all(np.isneginf(lse.cpu().numpy()[~fin]))
