@@ -6,7 +6,7 @@ its grouped-query form with 8 K/V heads), bf16 inputs
 drawn from the seeded generator. Prints one JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c4|c2|c5|c3|c1|g4|s1|s2]
+                    [--workload c4|c2|c5|c3|c1|g4|s1|s2|d1]
 
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (the path shards by independent heads; there is no data exchange), timing
@@ -16,7 +16,8 @@ is max-over-ranks, and ``value`` is the whole-job FLOP rate.
 cores, one bounded sample (one head's forward + backward) per step.
 
 ``--workload s1|s2`` instead times the standalone row softmax kernels (the
-two-pass online form against the three-pass safe form) and reports GB/s.
+two-pass online form against the three-pass safe form) and reports GB/s;
+``--workload d1`` times one paged-KV decode step and reports K/V GB/s.
 """
 from __future__ import annotations
 
@@ -505,6 +506,111 @@ def run_softmax_reference(args, rw, rank):
             "gpu_launches": 0}
 
 
+# -------------------------------------------------------- paged-KV decode
+
+DECODE_METRIC = "paged-KV decode GB/s (K and V bytes read per step)"
+
+
+def run_decode(args, dw, rank, world, dist):
+    """Time one decode step (partial kernel + merge) over the resident cache;
+    value = K/V bytes the step must read ÷ its time."""
+    import torch
+
+    import exact_tiled_attention_24_gb300 as fa
+    from exact_tiled_attention_24_gb300 import build as fabuild
+    from exact_tiled_attention_24_gb300.workloads import make_decode
+
+    fabuild.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    q, kc, vc, table, lens = make_decode(dw, dev)
+    ws = torch.empty(fa.decode_workspace_bytes(dw.B, dw.H, dw.d, dw.n_splits), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((dw.B, dw.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.decode_paged(q, kc, vc, table, lens, n_splits=dw.n_splits, workspace=ws, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.last_device_error(dev) != 0:
+        raise RuntimeError("device error during warm-up")
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(bus_id=bus) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    if fa.last_device_error(dev) != 0:
+        raise RuntimeError("device error during the timed region")
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = int(lens.sum().item())
+    kv_bytes = tokens * dw.Hkv * dw.d * 2 * 2
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    src = ["exact_tiled_attention_24_gb300/csrc/fa_decode.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
+    # end to end: q, table and lengths from pinned host memory, o and lse back
+    hq, ht, hl = (t.cpu().pin_memory() for t in (q, table, lens))
+    ho, hlse = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+    e2e_steps = max(1, min(args.steps, 20))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        q.copy_(hq, non_blocking=True)
+        table.copy_(ht, non_blocking=True)
+        lens.copy_(hl, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, ht, hl))
+    d2h = ho.numel() * ho.element_size() + hlse.numel() * hlse.element_size()
+    res = {
+        "metric": DECODE_METRIC, "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{dw.name}: decode B={dw.B} H={dw.H} Hkv={dw.Hkv} d={dw.d} "
+                               f"block={dw.block_size} context {dw.min_len}-{dw.max_len} "
+                               f"(total {tokens} tokens) splits={dw.n_splits}",
+                   "l2": "K/V %d MB read per step vs 129 MB L2; no flush" % (kv_bytes // 2**20)},
+        "roofline": {"kernel": "decode_partial", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": traffic_for(f"decode_partial_{dw.name}", src)},
+        "clocks": clk.summary(),
+        "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import decode_paged
+        k = 2
+        qs, kcs, vcs = (t.float().cpu().double().numpy() for t in (q[:k], kc, vc))
+        t0 = time.perf_counter()
+        decode_paged(qs, kcs, vcs, table[:k].cpu().numpy(), lens[:k].cpu().numpy(), dw.d ** -0.5)
+        dt = time.perf_counter() - t0
+        sample_bytes = int(lens[:k].sum().item()) * dw.Hkv * dw.d * 4
+        res["cpu_baseline"] = {"value": sample_bytes / dt / 1e9, "unit": "GB/s", "cores": host_cores(),
+                               "kind": "oracle",
+                               "sample": f"{k} requests of {dw.name}, fp64 NumPy oracle, {dt:.2f} s"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -517,13 +623,17 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
 
-    from exact_tiled_attention_24_gb300.workloads import ROW_WORKLOADS, WORKLOADS
+    from exact_tiled_attention_24_gb300.workloads import DECODE_WORKLOADS, ROW_WORKLOADS, WORKLOADS
     rw = ROW_WORKLOADS.get(args.workload)
-    w = WORKLOADS[args.workload] if rw is None else None
+    dw = DECODE_WORKLOADS.get(args.workload)
+    w = WORKLOADS[args.workload] if rw is None and dw is None else None
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None
-    if args.impl == "reference":
+    if args.impl == "reference" and dw is not None:
+        res = {"impl": "reference", "unavailable": "the decode workload has no reference arm; its oracle "
+                                                   "is timed in the GPU run's cpu_baseline"} if rank == 0 else None
+    elif args.impl == "reference":
         res = run_reference(args, w, rank) if rw is None else run_softmax_reference(args, rw, rank)
     else:
         if world > 1:
@@ -532,7 +642,12 @@ def main():
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
             tdist.init_process_group("nccl")
             dist = tdist
-        res = run_ours(args, w, rank, world, dist) if rw is None else run_softmax(args, rw, rank, world, dist)
+        if dw is not None:
+            res = run_decode(args, dw, rank, world, dist)
+        elif rw is not None:
+            res = run_softmax(args, rw, rank, world, dist)
+        else:
+            res = run_ours(args, w, rank, world, dist)
         if dist is not None:
             dist.destroy_process_group()
     if rank == 0 and res is not None:

@@ -21,9 +21,11 @@
 //                   the G query heads that share the K/V head, so each K/V
 //                   byte is read once per step. 64-key tiles of K and V are
 //                   copied into shared memory by bulk copies (one per run of
-//                   consecutive tokens inside a cache block), two tiles in
-//                   flight; scores, the running (m, l) and the fp32 output
-//                   rows stay on chip. Writes o_s (fp32) and lse_s per head.
+//                   consecutive tokens inside a cache block), three tiles in
+//                   flight. Each warp owns 8 keys of every tile and keeps
+//                   its own running (m, l) and fp32 output rows; the warps'
+//                   states are merged once at the end. Writes o_s (fp32)
+//                   and lse_s per head.
 //   merge           one warp per output row: the combination above.
 // The work per byte is a few FMAs (G·d per key and head pair), far below the
 // tensor-core ridge, so the products run on the FMA pipe.
@@ -43,23 +45,31 @@ namespace dec {
 
 constexpr int THREADS = 256;
 constexpr int TK = 64;  // keys per tile
+// Stages of the K/V ring. Two CTAs per SM with three 32 KB stages each keep
+// ~128 KB of loads in flight per SM, what HBM latency under load needs.
+constexpr int NST = 3;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.69314718055994531f;
 
 template <int D, int GM>
 struct Smem {
-  static constexpr int ROW = D * 2;        // bytes of one key (or value) row
-  static constexpr int TILE = TK * ROW;    // one K or V tile
-  static constexpr int K_OFF = 0;          // K stages 0, 1
-  static constexpr int V_OFF = 2 * TILE;   // V stages 0, 1
-  static constexpr int Q_OFF = 4 * TILE;   // q rows fp32 [GM][D], times scale·log2 e
-  static constexpr int P_OFF = Q_OFF + GM * D * 4;        // scores, then P: fp32 [GM][TK]
-  static constexpr int ST_OFF = P_OFF + GM * TK * 4;      // m, l, alpha: fp32 [3][GM]
-  static constexpr int TAB_OFF = ST_OFF + 3 * GM * 4;     // block-table slice, int32
-  static constexpr int O_OFF = TAB_OFF + kDecodeMaxTable * 4;  // partial rows of key parts 1..
-  static constexpr int PARTS = THREADS / D;               // key parts of the output pass
-  static constexpr int BAR_OFF = O_OFF + (PARTS - 1) * GM * D * 4;
-  static constexpr int BYTES = BAR_OFF + 2 * 8 + 16;
+  static constexpr int WARPS = THREADS / 32;
+  static constexpr int ROW = D * 2;             // bytes of one key (or value) row
+  static constexpr int TILE = TK * ROW;         // one K or V tile
+  static constexpr int K_OFF = 0;               // K stages (after the loop: the warps' partial rows)
+  static constexpr int V_OFF = NST * TILE;      // V stages
+  static constexpr int Q_OFF = 2 * NST * TILE;  // q rows fp32 [GM][D], times scale·log2 e
+  // Per-warp scratch: the scores, then the (p, p) pairs, of its 8 keys x 4
+  // heads (64 floats), then the 4 heads' rescale factors.
+  static constexpr int W_OFF = Q_OFF + GM * D * 4;
+  static constexpr int W_BYTES = (8 * 4 * 2 + 4) * 4;
+  static constexpr int ML_OFF = W_OFF + WARPS * W_BYTES;  // per-warp (m, l) per head: [WARPS][2][GM]
+  static constexpr int TAB_OFF = ML_OFF + WARPS * 2 * GM * 4;  // block-table slice, int32
+  static constexpr int BAR_OFF = TAB_OFF + kDecodeMaxTable * 4;
+  // full[NST] mbarriers, then per stage: releases this round, fills so far
+  static constexpr int CNT_OFF = BAR_OFF + NST * 8;
+  static constexpr int BYTES = CNT_OFF + 2 * NST * 4 + 16;
+  static_assert(WARPS * GM * D * 4 <= 2 * NST * TILE, "the warps' partial rows must fit the idle stages");
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -68,12 +78,28 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// Two fp32 multiply-adds in one instruction: d = a * b + c, element-wise.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(*reinterpret_cast<unsigned long long*>(&d))
+      : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
+        "l"(*reinterpret_cast<const unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<const unsigned long long*>(&c)));
+  return d;
 }
 
+// bf16 pair (low half = first element) -> two floats, exactly.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Each warp owns keys 8w .. 8w + 7 of every tile and keeps its own running
+// (m, l) and output rows for the G heads, so the tile loop needs no
+// CTA-wide barrier: a warp waits for the tile's bytes and, when it has read
+// the stage, counts itself out; the last warp out refills the stage with the
+// tile NST further on. The eight warps' states are merged at the end with
+// the same rescaling as the split merge.
 template <int D, int GM>
 __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cache,
@@ -81,10 +107,13 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
     const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B,
     int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale_log2) {
   using L = Smem<D, GM>;
+  constexpr int WARPS = L::WARPS;
+  constexpr int CPL = D / 32;  // output columns per lane
   extern __shared__ __align__(1024) uint8_t smem[];
   const int S = gridDim.x;
   const int s = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int G = H / Hkv;
   uint32_t* err = &g_dec_err;
 
@@ -109,50 +138,45 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
   float* sQ = reinterpret_cast<float*>(smem + L::Q_OFF);
-  float* sP = reinterpret_cast<float*>(smem + L::P_OFF);
-  float* sM = reinterpret_cast<float*>(smem + L::ST_OFF);
-  float* sL = sM + GM;
-  float* sA = sL + GM;
+  float* sW = reinterpret_cast<float*>(smem + L::W_OFF + warp * L::W_BYTES);
+  float* sML = reinterpret_cast<float*>(smem + L::ML_OFF);
   int* sTab = reinterpret_cast<int*>(smem + L::TAB_OFF);
-  float* sO = reinterpret_cast<float*>(smem + L::O_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  int* rel = reinterpret_cast<int*>(smem + L::CNT_OFF);
+  int* fills = rel + NST;
 
   for (int i = tid; i < GM * D; i += THREADS) {
     const int g = i / D;
     sQ[i] = g < G ? __bfloat162float(q[(head0 + g) * D + (i % D)]) * scale_log2 : 0.f;
   }
-  // Zero both stages: the tail rows of a partial tile then read as 0.
-  for (int i = tid; i < 4 * L::TILE / 16; i += THREADS)
-    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = tid; i < nblk; i += THREADS) sTab[i] = block_table[static_cast<size_t>(b) * max_blocks + blk0 + i];
-  if (tid < GM) {
-    sM[tid] = -INFINITY;
-    sL[tid] = 0.f;
+  if (tid < NST) {
+    rel[tid] = 0;
+    fills[tid] = 0;
   }
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int st = 0; st < NST; ++st) mbar_init(&full[st], 1);
     fence_mbar_init();
   }
-  fence_async_smem();  // the zero fill before the bulk copies into the same bytes
   __syncthreads();
 
-  // Thread 0: copy tile `tile` of K and V into stage st, one bulk copy per
+  // One thread: copy tile `tile` of K and V into stage st, one bulk copy per
   // run of consecutive tokens within a cache block. Entries outside
   // [0, num_blocks) are skipped (rows keep their old values) and reported.
   auto issue = [&](int tile, int st) {
+    ++fills[st];
     const int t0 = tile * TK, t1 = min(t_end, t0 + TK);
+    const int bi0 = t0 / bs - blk0, off0 = t0 % bs;  // the only divisions per tile
     uint32_t bytes = 0;
-    for (int t = t0; t < t1;) {
-      const int blk = sTab[t / bs - blk0];
-      const int run = min(bs - t % bs, t1 - t);
+    for (int t = t0, bi = bi0, off = off0; t < t1; ++bi, off = 0) {
+      const int blk = sTab[bi];
+      const int run = min(bs - off, t1 - t);
       if (blk >= 0 && blk < num_blocks) bytes += static_cast<uint32_t>(run) * L::ROW;
       t += run;
     }
     mbar_arrive_expect_tx(&full[st], 2 * bytes);
-    for (int t = t0; t < t1;) {
-      const int blk = sTab[t / bs - blk0];
-      const int off = t % bs;
+    for (int t = t0, bi = bi0, off = off0; t < t1; ++bi, off = 0) {
+      const int blk = sTab[bi];
       const int run = min(bs - off, t1 - t);
       if (blk >= 0 && blk < num_blocks) {
         const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + off) * D;
@@ -166,123 +190,199 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
     }
   };
 
-  constexpr int PARTS = L::PARTS;
-  constexpr int KP = TK / PARTS;  // keys per part in the output pass
-  const int c = tid % D;          // output column of this thread
-  const int part = tid / D;
-  float acc[GM];
+  // Scores: 8 lanes per key (lane = 8·kw + dq); lane dq covers the 16-byte
+  // chunks dq (and dq + 8 when d = 128) of the row, so the 8 lanes of a load
+  // phase hit distinct banks. Four heads at a time; their q slices stay in
+  // registers for the whole sweep when G <= 4.
+  constexpr int CH = D / 64;
+  const int dq = lane & 7, kw = lane >> 3;
+  float2 qr[4][CH * 4];
+  auto load_q = [&](int hg) {
 #pragma unroll
-  for (int g = 0; g < GM; ++g) acc[g] = 0.f;
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) {
+        const float* src = sQ + (hg * 4 + j) * D + (dq + 8 * ch) * 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qr[j][ch * 4 + i] = make_float2(src[2 * i], src[2 * i + 1]);
+      }
+  };
+  if (GM == 4) load_q(0);
 
-  if (tid == 0) issue(tile0, 0);
-  int issued = 1;
-  bool ok = true;
-  int i = 0;
-  for (int tile = tile0; tile < tile1; ++tile, ++i) {
-    const int st = i & 1;
-    if (tid == 0 && tile + 1 < tile1) {
-      issue(tile + 1, st ^ 1);
-      ++issued;
-    }
-    const bool waited = mbar_wait(&full[st], (i >> 1) & 1, err);
-    if (__syncthreads_or(!waited)) {
-      ok = false;
-      break;
-    }
-    const int nk = min(t_end, (tile + 1) * TK) - tile * TK;
-    // Scores (log2 units): thread -> key k, heads g = tid / TK + j·(THREADS / TK).
-    // The 16-byte chunks of a row are visited in a rotated order so that the
-    // threads of a phase hit distinct banks.
-    {
-      const int k = tid % TK;
-      const uint4* kr = reinterpret_cast<const uint4*>(sK + st * L::TILE + k * L::ROW);
-      for (int g = tid / TK; g < G; g += THREADS / TK) {
-        const float* qr = sQ + g * D;
-        float a = 0.f;
-#pragma unroll 4
-        for (int cc = 0; cc < D / 8; ++cc) {
-          const int ch = (cc + k) & (D / 8 - 1);
-          const uint4 kv = kr[ch];
-          const float4 q0 = *reinterpret_cast<const float4*>(qr + ch * 8);
-          const float4 q1 = *reinterpret_cast<const float4*>(qr + ch * 8 + 4);
-          const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
-          const float2 f0 = __bfloat1622float2(k2[0]), f1 = __bfloat1622float2(k2[1]);
-          const float2 f2 = __bfloat1622float2(k2[2]), f3 = __bfloat1622float2(k2[3]);
-          a = fmaf(q0.x, f0.x, a);
-          a = fmaf(q0.y, f0.y, a);
-          a = fmaf(q0.z, f1.x, a);
-          a = fmaf(q0.w, f1.y, a);
-          a = fmaf(q1.x, f2.x, a);
-          a = fmaf(q1.y, f2.y, a);
-          a = fmaf(q1.z, f3.x, a);
-          a = fmaf(q1.w, f3.y, a);
-        }
-        sP[g * TK + k] = k < nk ? a : -INFINITY;
-      }
-    }
-    __syncthreads();
-    // Online softmax per head (warp w takes heads w, w + 8, ...): raise m,
-    // rescale l by 2^(m_old − m_new), P = 2^(s − m_new).
-    {
-      const int warp = tid >> 5, lane = tid & 31;
-      for (int g = warp; g < G; g += THREADS / 32) {
-        const float v0 = sP[g * TK + lane], v1 = sP[g * TK + lane + 32];
-        const float m_old = sM[g];
-        const float m_new = fmaxf(m_old, warp_max(fmaxf(v0, v1)));
-        const float p0 = ex2(v0 - m_new), p1 = ex2(v1 - m_new);
-        sP[g * TK + lane] = p0;
-        sP[g * TK + lane + 32] = p1;
-        const float sum = warp_sum(p0 + p1);
-        if (lane == 0) {
-          const float a = ex2(m_old - m_new);  // 0 on the first tile
-          sA[g] = a;
-          sL[g] = sL[g] * a + sum;
-          sM[g] = m_new;
-        }
-      }
-    }
-    __syncthreads();
-    // Output rows: thread -> column c, keys [part·KP, part·KP + KP).
-    {
-      const __nv_bfloat16* vt = reinterpret_cast<const __nv_bfloat16*>(sV + st * L::TILE);
+  // Per-warp state: lanes 8j .. 8j + 7 hold (m, l) of head 4·hg + j; every
+  // lane holds output columns CPL·lane .. + CPL - 1 of every head.
+  float m_run[GM / 4], l_run[GM / 4];
 #pragma unroll
-      for (int g = 0; g < GM; ++g)
-        if (g < G) acc[g] *= sA[g];
-#pragma unroll 4
-      for (int kk = 0; kk < KP; ++kk) {
-        const int k = part * KP + kk;
-        const float vv = __bfloat162float(vt[k * D + c]);
-#pragma unroll
-        for (int g = 0; g < GM; ++g)
-          if (g < G) acc[g] = fmaf(sP[g * TK + k], vv, acc[g]);
-      }
-    }
-    __syncthreads();  // stage st and sP are free for the next tiles
+  for (int hg = 0; hg < GM / 4; ++hg) {
+    m_run[hg] = -INFINITY;
+    l_run[hg] = 0.f;
   }
-  if (!ok) {
+  float2 acc[GM][CPL / 2];
+#pragma unroll
+  for (int g = 0; g < GM; ++g)
+#pragma unroll
+    for (int c = 0; c < CPL / 2; ++c) acc[g][c] = make_float2(0.f, 0.f);
+
+  // The first NST tiles fill every stage.
+  if (tid == 0)
+    for (int j = 0; j < NST && tile0 + j < tile1; ++j) issue(tile0 + j, j);
+  __syncthreads();
+  bool ok = true;
+  int it = 0;
+  for (int tile = tile0; tile < tile1; ++tile, ++it) {
+    const int st = it % NST;
+    ok = mbar_wait_warp(&full[st], (it / NST) & 1, err);
+    if (!ok) break;
+    const int nk = min(t_end, (tile + 1) * TK) - tile * TK;
+    const uint8_t* kt = sK + st * L::TILE;
+    const uint32_t* vt = reinterpret_cast<const uint32_t*>(sV + st * L::TILE);
+#pragma unroll
+    for (int hg = 0; hg < GM / 4; ++hg) {
+      if (hg * 4 >= G) continue;  // warp-uniform
+      if (GM > 4) load_q(hg);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int kk = p * 4 + kw;  // key within the warp's eight
+        const int k = warp * 8 + kk;
+        float2 a[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(kt + k * L::ROW + (dq + 8 * ch) * 16);
+          const float2 k0 = bf2_to_f2(kv.x), k1 = bf2_to_f2(kv.y), k2 = bf2_to_f2(kv.z), k3 = bf2_to_f2(kv.w);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            a[j] = fma2(k0, qr[j][ch * 4 + 0], a[j]);
+            a[j] = fma2(k1, qr[j][ch * 4 + 1], a[j]);
+            a[j] = fma2(k2, qr[j][ch * 4 + 2], a[j]);
+            a[j] = fma2(k3, qr[j][ch * 4 + 3], a[j]);
+          }
+        }
+        const float s0 = a[0].x + a[0].y, s1 = a[1].x + a[1].y;
+        const float s2 = a[2].x + a[2].y, s3 = a[3].x + a[3].y;
+        // Reduce-scatter over the key's 8 lanes: 4 shuffles leave lane pair
+        // (dq, dq ^ 1) with the full score of head j = 2·bit2 + bit1.
+        const bool hi = dq & 4, mid = dq & 2;
+        const float t0 = __shfl_xor_sync(0xffffffffu, hi ? s0 : s2, 4);
+        const float t1 = __shfl_xor_sync(0xffffffffu, hi ? s1 : s3, 4);
+        const float a0 = (hi ? s2 : s0) + t0, a1 = (hi ? s3 : s1) + t1;
+        float r = (mid ? a1 : a0) + __shfl_xor_sync(0xffffffffu, mid ? a0 : a1, 2);
+        r += __shfl_xor_sync(0xffffffffu, r, 1);
+        const int j = (hi ? 2 : 0) + (mid ? 1 : 0);
+        // Rows past the context end hold stale bytes: their score is -inf
+        // whatever r is.
+        if ((dq & 1) == 0) sW[j * 8 + kk] = (k < nk && hg * 4 + j < G) ? r : -INFINITY;
+      }
+      __syncwarp();
+      // Online softmax of the warp's 8 keys: lane = 8j + kk holds head j, key kk.
+      float pr, al;
+      {
+        const int j = lane >> 3;
+        const float sc = sW[lane];
+        float mx = sc;
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        const float m_new = fmaxf(m_run[hg], mx);
+        if (m_new == -INFINITY) {  // no key of this head seen by the warp yet
+          pr = 0.f;
+          al = 1.f;
+        } else {
+          pr = ex2(sc - m_new);
+          al = ex2(m_run[hg] - m_new);
+        }
+        float sum = pr;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        l_run[hg] = l_run[hg] * al + sum;
+        m_run[hg] = m_new;
+        (void)j;
+      }
+      __syncwarp();
+      // (p, p) pairs, key-major: [kk][head j][2]; alphas of the 4 heads after.
+      sW[((lane & 7) * 4 + (lane >> 3)) * 2] = pr;
+      sW[((lane & 7) * 4 + (lane >> 3)) * 2 + 1] = pr;
+      if ((lane & 7) == 0) sW[64 + (lane >> 3)] = al;
+      __syncwarp();
+      // Output columns: acc_j = α_j·acc_j + Σ_kk P_j,kk · V_kk[cols].
+      {
+        const float4 al4 = *reinterpret_cast<const float4*>(sW + 64);
+        const float alj[4] = {al4.x, al4.y, al4.z, al4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int c = 0; c < CPL / 2; ++c)
+            acc[hg * 4 + j][c] = make_float2(acc[hg * 4 + j][c].x * alj[j], acc[hg * 4 + j][c].y * alj[j]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // Rows past the context end were never copied (P is 0 there, and
+          // their bytes may be anything): skip them, warp-uniformly.
+          if (warp * 8 + kk >= nk) break;
+          const uint32_t* vr = vt + (warp * 8 + kk) * (D / 2) + lane * (CPL / 2);
+          float2 v[CPL / 2];
+#pragma unroll
+          for (int c = 0; c < CPL / 2; ++c) v[c] = bf2_to_f2(vr[c]);
+          const float4 p01 = *reinterpret_cast<const float4*>(sW + kk * 8);
+          const float4 p23 = *reinterpret_cast<const float4*>(sW + kk * 8 + 4);
+          const float2 pp[4] = {make_float2(p01.x, p01.y), make_float2(p01.z, p01.w),
+                                make_float2(p23.x, p23.y), make_float2(p23.z, p23.w)};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int c = 0; c < CPL / 2; ++c) acc[hg * 4 + j][c] = fma2(v[c], pp[j], acc[hg * 4 + j][c]);
+        }
+      }
+      __syncwarp();  // the scratch is rewritten by the next head group
+    }
+    // This warp has read stage st; the last warp out refills it.
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&rel[st], 1) == WARPS - 1) {
+        rel[st] = 0;
+        if (tile + NST < tile1) issue(tile + NST, st);
+      }
+    }
+    __syncwarp();
+  }
+  if (__syncthreads_or(!ok)) {
     // Let copies already issued land before the CTA exits (bounded).
     if (tid == 0)
-      for (int j = i; j < issued; ++j) mbar_wait(&full[j & 1], (j >> 1) & 1, err);
+      for (int st = 0; st < NST; ++st)
+        if (fills[st] > 0) mbar_wait(&full[st], (fills[st] - 1) & 1, err);
     return;
   }
-  // Sum the key parts and write o_s = u / l and lse_s = (m + log2 l)·ln 2.
-  if (part > 0) {
+  // Merge the warps' states per head: M = max_w m_w, L = Σ_w l_w 2^(m_w − M),
+  // o = Σ_w acc_w 2^(m_w − M) / L, lse = (M + log2 L)·ln 2.
+  float* sAcc = reinterpret_cast<float*>(smem + L::K_OFF);  // [WARPS][GM][D]; the stages are idle
 #pragma unroll
-    for (int g = 0; g < GM; ++g)
-      if (g < G) sO[((part - 1) * GM + g) * D + c] = acc[g];
-  }
-  __syncthreads();
-  if (part == 0) {
+  for (int g = 0; g < GM; ++g)
 #pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      if (g < G) {
-        float u = acc[g];
-        for (int p = 1; p < PARTS; ++p) u += sO[((p - 1) * GM + g) * D + c];
-        o_part[(prow + g) * D + c] = u / sL[g];
-      }
+    for (int c = 0; c < CPL / 2; ++c)
+      *reinterpret_cast<float2*>(sAcc + (warp * GM + g) * D + lane * CPL + 2 * c) = acc[g][c];
+#pragma unroll
+  for (int hg = 0; hg < GM / 4; ++hg)
+    if ((lane & 7) == 0) {
+      sML[(warp * 2 + 0) * GM + hg * 4 + (lane >> 3)] = m_run[hg];
+      sML[(warp * 2 + 1) * GM + hg * 4 + (lane >> 3)] = l_run[hg];
     }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += THREADS) {
+    const int g = i / D, c = i % D;
+    float M = -INFINITY;
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sML[(w * 2) * GM + g]);
+    float Ls = 0.f, u = 0.f;
+    for (int w = 0; w < WARPS; ++w) {
+      const float mw = sML[(w * 2) * GM + g];
+      if (mw == -INFINITY) continue;
+      const float f = ex2(mw - M);
+      Ls += sML[(w * 2 + 1) * GM + g] * f;
+      u += sAcc[(w * GM + g) * D + c] * f;
+    }
+    o_part[(prow + g) * D + c] = u / Ls;
+    if (c == 0) lse_part[prow + g] = (M + __log2f(Ls)) * LN2;
   }
-  if (tid < G) lse_part[prow + tid] = (sM[tid] + __log2f(sL[tid])) * LN2;
 }
 
 // One warp per output row: o = Σ_s e^(lse_s − lse) o_s, lse = ln Σ_s e^(lse_s).

@@ -3,6 +3,7 @@
     python -m exact_tiled_attention_24_gb300.profile_case --B 1 --H 32 --N 4096 --d 128 \
         --causal --iters 2 [--Hkv 8]
     python -m exact_tiled_attention_24_gb300.profile_case --softmax-rows 1216 --softmax-n 262144
+    python -m exact_tiled_attention_24_gb300.profile_case --decode d1
 
 Inputs come from the seeded workload generator; nothing is checked or timed.
 """
@@ -23,16 +24,27 @@ def main():
     ap.add_argument("--Hkv", type=int, default=0, help="K/V heads (grouped-query); 0 = H")
     ap.add_argument("--softmax-rows", type=int, default=0, help="run the row softmax kernels instead")
     ap.add_argument("--softmax-n", type=int, default=262144)
+    ap.add_argument("--decode", default="", help="run a decode workload (e.g. d1) instead")
     args = ap.parse_args()
 
     import torch
 
     import exact_tiled_attention_24_gb300 as fa
     from exact_tiled_attention_24_gb300 import build
-    from exact_tiled_attention_24_gb300.workloads import make_inputs, make_rows
+    from exact_tiled_attention_24_gb300.workloads import DECODE_WORKLOADS, make_decode, make_inputs, make_rows
 
     build.build()
     dev = torch.device("cuda")
+    if args.decode:
+        dw = DECODE_WORKLOADS[args.decode]
+        q, kc, vc, table, lens = make_decode(dw, dev)
+        for _ in range(args.iters):
+            fa.decode_paged(q, kc, vc, table, lens, n_splits=dw.n_splits)
+        torch.cuda.synchronize()
+        if fa.last_device_error() != 0:
+            raise SystemExit("device error")
+        print("ok")
+        return
     if args.softmax_rows:
         x = make_rows(args.softmax_rows, args.softmax_n, seed=99, std=4.0).to(dev)
         y = torch.empty_like(x)

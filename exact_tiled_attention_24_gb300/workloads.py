@@ -116,6 +116,51 @@ ROW_WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """One decode step of B requests against a paged KV cache: context
+    lengths drawn uniformly from [min_len, max_len], 16-token blocks placed
+    in a random order, q, K, V ~ N(0, 1) in bf16."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    d: int
+    block_size: int
+    min_len: int
+    max_len: int
+    n_splits: int
+    seed: int
+
+
+DECODE_WORKLOADS = {
+    # 32 requests with 2k-8k cached tokens, Llama-3-8B heads (32 over 8):
+    # about 670 MB of K and V read per step, more than L2
+    "d1": DecodeWorkload("d1", 32, 32, 8, 128, 16, 2048, 8192, 4, 3001),
+}
+
+
+def make_decode(w: DecodeWorkload, device):
+    """Seeded decode inputs, drawn on `device` (the cache is state that lives
+    there): q [B, H, d], k_cache, v_cache [num_blocks, Hkv, bs, d],
+    block_table [B, max_blocks] int32, seq_lens [B] int32."""
+    g = torch.Generator().manual_seed(w.seed)
+    lens = torch.randint(w.min_len, w.max_len + 1, (w.B,), generator=g, dtype=torch.int64)
+    nb = (lens + w.block_size - 1) // w.block_size
+    total = int(nb.sum())
+    perm = torch.randperm(total, generator=g)
+    table = torch.zeros((w.B, int(nb.max())), dtype=torch.int32)
+    pos = 0
+    for b in range(w.B):
+        table[b, :nb[b]] = perm[pos:pos + int(nb[b])].to(torch.int32)
+        pos += int(nb[b])
+    gd = torch.Generator(device=device).manual_seed(w.seed + 1)
+    q = torch.randn((w.B, w.H, w.d), generator=gd, device=device).to(torch.bfloat16)
+    kc = torch.randn((total, w.Hkv, w.block_size, w.d), generator=gd, device=device).to(torch.bfloat16)
+    vc = torch.randn((total, w.Hkv, w.block_size, w.d), generator=gd, device=device).to(torch.bfloat16)
+    return q, kc, vc, table.to(device), lens.to(torch.int32).to(device)
+
+
 def make_rows(rows, n, seed, std=1.0):
     """Draw x [rows, n] fp32 on the CPU from the seeded generator."""
     g = torch.Generator().manual_seed(int(seed))
