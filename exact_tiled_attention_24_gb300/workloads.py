@@ -136,7 +136,7 @@ class DecodeWorkload:
 DECODE_WORKLOADS = {
     # 32 requests with 2k-8k cached tokens, Llama-3-8B heads (32 over 8):
     # about 670 MB of K and V read per step, more than L2
-    "d1": DecodeWorkload("d1", 32, 32, 8, 128, 16, 2048, 8192, 4, 3001),
+    "d1": DecodeWorkload("d1", 32, 32, 8, 128, 16, 2048, 8192, 8, 3001),
 }
 
 
