@@ -61,8 +61,8 @@ struct Smem {
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
   // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  // p_ready[2], pv_done[2], final
-  static constexpr int NBARS = 1 + 4 * STAGES + 6 + 1;
+  // p_ready[2] (keys 0..63 of P), pv_done[2], final, p_hi[2] (keys 64..127)
+  static constexpr int NBARS = 1 + 4 * STAGES + 6 + 1 + 2;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   // Slack for 1024-byte alignment; at least 116 KB so that only one CTA
@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_ready = s_full + 2;           // [2]
   uint64_t* pv_done = p_ready + 2;          // [2]
   uint64_t* final_bar = pv_done + 2;
+  uint64_t* p_hi = final_bar + 1;           // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int g = 0; g < 2; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&p_ready[g], 4);
+      mbar_init(&p_hi[g], 4);
       mbar_init(&pv_done[g], 1);
     }
     mbar_init(final_bar, 1);
@@ -212,16 +214,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       __syncwarp();
     };
-    // O_g += P_g V_j; P_g is bf16 in the first 64 S columns of group g.
-    auto issue_pv = [&](int g, int s, uint32_t acc0) {
+    // O_g += P_g V_j over keys 64·half .. 64·half + 63; P_g is bf16 in the
+    // first 64 S columns of group g. The second half commits pv_done.
+    auto issue_pv = [&](int g, int s, int half, uint32_t acc0) {
       const uint64_t b = s ? dv1 : dv0;
       const uint32_t d = tmem + 256 + g * 128;
       const uint32_t a = tmem + g * BN;
       if (elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
+        for (int k4 = 0; k4 < BN / 32; ++k4) {
+          const int ks = half * (BN / 32) + k4;
           mma_ts(d, a + ks * 8, desc_add(b, mnmajor_step(ks)), idesc_o, ks > 0 ? 1u : acc0);
-        tc_commit(&pv_done[g]);
+        }
+        if (half == 1) tc_commit(&pv_done[g]);
       }
       __syncwarp();
     };
@@ -239,26 +244,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = 0; j < n_kt && ok; ++j) {
       const int s = j % L::STAGES;
       const int s1 = (j + 1) % L::STAGES;
-      bool next_ready = false;
+      // The data waits (V_j, K_{j+1}) come first: they are normally met and
+      // overlap the wait for P_j, so no wait sits between two products.
+      const bool next_ready = j + 1 < n_kt;
       ok = mbar_wait_warp(&v_full[s], (j / L::STAGES) & 1, err);
+      if (ok && next_ready) ok = mbar_wait_warp(&k_full[s1], ((j + 1) / L::STAGES) & 1, err);
       if (!ok) break;
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
         const int n_g = (g == 0) ? n_g0 : n_g1;
         if (j >= n_g) continue;
+        // P·V on keys 0..63 as soon as that half of P is written, then on
+        // keys 64..127: the tensor core starts while the softmax warps are
+        // still on the second half.
         ok = mbar_wait_warp(&p_ready[g], j & 1, err);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(g, s, j > 0 ? 1u : 0u);
-        if (j + 1 < n_g) {
-          if (!next_ready) {
-            ok = mbar_wait_warp(&k_full[s1], ((j + 1) / L::STAGES) & 1, err);
-            if (!ok) break;
-            tc_fence_after();
-            next_ready = true;
-          }
-          issue_s(g, s1);
-        }
+        issue_pv(g, s, 0, j > 0 ? 1u : 0u);
+        ok = mbar_wait_warp(&p_hi[g], j & 1, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(g, s, 1, 1u);
+        if (j + 1 < n_g) issue_s(g, s1);
       }
       if (!ok) break;
       commit(&v_empty[s]);                 // V_j: read by PV_j
@@ -301,15 +308,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (key >= N || (CAUSAL && key > qrow)) x[c] = -INFINITY;
         }
       }
-      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+      // Eight independent max chains (short dependency chains: the softmax
+      // warps have little else to hide latency with).
+      float mx[8];
 #pragma unroll
-      for (int c = 4; c < BN; c += 4) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
-        mx2 = fmaxf(mx2, x[c + 2]);
-        mx3 = fmaxf(mx3, x[c + 3]);
-      }
-      const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+      for (int u = 0; u < 8; ++u) mx[u] = x[u];
+#pragma unroll
+      for (int c = 8; c < BN; c += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], x[c + u]);
+      const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * scale_log2;
       // Raise the reference when the max outgrew it by more than the
       // threshold (always on the first tile, where m = -inf).
       const bool warp_raise = __any_sync(0xffffffffu, tile_max > m + RESCALE_LOG2);
@@ -320,22 +329,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         m = m_new;
         l *= alpha;
       }
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t2 = 0; t2 < 16; ++t2) {
-          const float p0 = ex2(fmaf(x[c + 2 * t2], scale_log2, -m));
-          const float p1 = ex2(fmaf(x[c + 2 * t2 + 1], scale_log2, -m));
-          sum0 += p0;
-          sum1 += p1;
-          pk[t2] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(s_addr + c / 2, pk);  // P (bf16) into the first 64 S columns
-      }
-      l += sum0 + sum1;
-      // O *= alpha once P V_{j-1} has landed (only when this warp raised).
+      // O *= alpha once P V_{j-1} has landed (only when this warp raised);
+      // before any of P_j is released, since P V_j accumulates into O.
       if (warp_raise && j > 0) {
         ok = mbar_wait(&pv_done[g], (j - 1) & 1, err);
         if (!ok) break;
@@ -355,10 +350,29 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st16(o_addr + c + 16, bb);
         }
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[g]);
+      float sum[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum[u] = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2) {
+          const float p0 = ex2(fmaf(x[c + 2 * t2], scale_log2, -m));
+          const float p1 = ex2(fmaf(x[c + 2 * t2 + 1], scale_log2, -m));
+          sum[(2 * t2) & 7] += p0;
+          sum[(2 * t2 + 1) & 7] += p1;
+          pk[t2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + c / 2, pk);  // P (bf16) into the first 64 S columns
+        if (c + 32 == BN / 2 || c + 32 == BN) {  // a half of P is in TMEM: release it
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(c + 32 == BN ? &p_hi[g] : &p_ready[g]);
+        }
+      }
+      l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
     }
     // -------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&pv_done[g], (n_mine - 1) & 1, err);
