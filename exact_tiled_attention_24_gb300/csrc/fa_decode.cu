@@ -160,33 +160,40 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
   }
   __syncthreads();
 
-  // One thread: copy tile `tile` of K and V into stage st, one bulk copy per
-  // run of consecutive tokens within a cache block. Entries outside
-  // [0, num_blocks) are skipped (rows keep their old values) and reported.
+  // One warp: copy tile `tile` of K and V into stage st. Lane r takes the
+  // r-th run of consecutive tokens inside one cache block (r, r + 32, ...)
+  // and issues its K and V bulk copies, so the copies of a tile go out in
+  // parallel. Entries outside [0, num_blocks) are skipped (their rows keep
+  // old bytes, masked later) and reported; only copied bytes are expected.
   auto issue = [&](int tile, int st) {
-    ++fills[st];
     const int t0 = tile * TK, t1 = min(t_end, t0 + TK);
-    const int bi0 = t0 / bs - blk0, off0 = t0 % bs;  // the only divisions per tile
+    const int b0 = t0 / bs;                 // the only division per tile
+    const int nrun = (t1 - 1) / bs - b0 + 1;
     uint32_t bytes = 0;
-    for (int t = t0, bi = bi0, off = off0; t < t1; ++bi, off = 0) {
-      const int blk = sTab[bi];
-      const int run = min(bs - off, t1 - t);
-      if (blk >= 0 && blk < num_blocks) bytes += static_cast<uint32_t>(run) * L::ROW;
-      t += run;
+    for (int r = lane; r < nrun; r += 32) {
+      const int blk = sTab[b0 + r - blk0];
+      const int rs = max(t0, (b0 + r) * bs), re = min(t1, (b0 + r + 1) * bs);
+      if (blk >= 0 && blk < num_blocks) bytes += static_cast<uint32_t>(re - rs) * L::ROW;
     }
-    mbar_arrive_expect_tx(&full[st], 2 * bytes);
-    for (int t = t0, bi = bi0, off = off0; t < t1; ++bi, off = 0) {
-      const int blk = sTab[bi];
-      const int run = min(bs - off, t1 - t);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+    if (lane == 0) {
+      ++fills[st];
+      mbar_arrive_expect_tx(&full[st], 2 * bytes);
+    }
+    __syncwarp();
+    for (int r = lane; r < nrun; r += 32) {
+      const int blk = sTab[b0 + r - blk0];
+      const int rs = max(t0, (b0 + r) * bs), re = min(t1, (b0 + r + 1) * bs);
       if (blk >= 0 && blk < num_blocks) {
-        const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + off) * D;
-        const uint32_t dst = static_cast<uint32_t>(t - t0) * L::ROW;
-        bulk_load(sK + st * L::TILE + dst, k_cache + src, static_cast<uint32_t>(run) * L::ROW, &full[st]);
-        bulk_load(sV + st * L::TILE + dst, v_cache + src, static_cast<uint32_t>(run) * L::ROW, &full[st]);
+        const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + (rs - (b0 + r) * bs)) * D;
+        const uint32_t dst = static_cast<uint32_t>(rs - t0) * L::ROW;
+        const uint32_t nbytes = static_cast<uint32_t>(re - rs) * L::ROW;
+        bulk_load(sK + st * L::TILE + dst, k_cache + src, nbytes, &full[st]);
+        bulk_load(sV + st * L::TILE + dst, v_cache + src, nbytes, &full[st]);
       } else {
         atomicExch(err, DEV_BAD_INDEX);
       }
-      t += run;
     }
   };
 
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
     for (int c = 0; c < CPL / 2; ++c) acc[g][c] = make_float2(0.f, 0.f);
 
   // The first NST tiles fill every stage.
-  if (tid == 0)
+  if (warp == 0)
     for (int j = 0; j < NST && tile0 + j < tile1; ++j) issue(tile0 + j, j);
   __syncthreads();
   bool ok = true;
@@ -337,14 +344,13 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
       __syncwarp();  // the scratch is rewritten by the next head group
     }
     // This warp has read stage st; the last warp out refills it.
+    int last = 0;
     if (lane == 0) {
       __threadfence_block();
-      if (atomicAdd(&rel[st], 1) == WARPS - 1) {
-        rel[st] = 0;
-        if (tile + NST < tile1) issue(tile + NST, st);
-      }
+      last = atomicAdd(&rel[st], 1) == WARPS - 1;
+      if (last) rel[st] = 0;
     }
-    __syncwarp();
+    if (__shfl_sync(0xffffffffu, last, 0) && tile + NST < tile1) issue(tile + NST, st);
   }
   if (__syncthreads_or(!ok)) {
     // Let copies already issued land before the CTA exits (bounded).
