@@ -56,9 +56,12 @@ struct Smem {
   static constexpr int WARPS = THREADS / 32;
   static constexpr int ROW = D * 2;             // bytes of one key (or value) row
   static constexpr int TILE = TK * ROW;         // one K or V tile
-  static constexpr int K_OFF = 0;               // K stages (after the loop: the warps' partial rows)
-  static constexpr int V_OFF = NST * TILE;      // V stages
-  static constexpr int Q_OFF = 2 * NST * TILE;  // q rows fp32 [GM][D], times scale·log2 e
+  // Each warp streams its own 8 keys of every tile: stage st of warp w holds
+  // their K rows then their V rows (after the loop, the stages hold the
+  // warps' partial output rows).
+  static constexpr int WSLOT = 2 * 8 * ROW;
+  static constexpr int SLOT_OFF = 0;
+  static constexpr int Q_OFF = NST * WARPS * WSLOT;  // q rows fp32 [GM][D], times scale·log2 e
   // Per-warp scratch: the scores, then the (p, p) pairs, of its 8 keys x 4
   // heads (64 floats), then the 4 heads' rescale factors.
   static constexpr int W_OFF = Q_OFF + GM * D * 4;
@@ -66,10 +69,10 @@ struct Smem {
   static constexpr int ML_OFF = W_OFF + WARPS * W_BYTES;  // per-warp (m, l) per head: [WARPS][2][GM]
   static constexpr int TAB_OFF = ML_OFF + WARPS * 2 * GM * 4;  // block-table slice, int32
   static constexpr int BAR_OFF = TAB_OFF + kDecodeMaxTable * 4;
-  // full[NST] mbarriers, then per stage: releases this round, fills so far
-  static constexpr int CNT_OFF = BAR_OFF + NST * 8;
-  static constexpr int BYTES = CNT_OFF + 2 * NST * 4 + 16;
-  static_assert(WARPS * GM * D * 4 <= 2 * NST * TILE, "the warps' partial rows must fit the idle stages");
+  // full[NST][WARPS] mbarriers, then fills so far per (stage, warp)
+  static constexpr int CNT_OFF = BAR_OFF + NST * WARPS * 8;
+  static constexpr int BYTES = CNT_OFF + NST * WARPS * 4 + 16;
+  static_assert(WARPS * GM * D * 4 <= NST * WARPS * WSLOT, "the warps' partial rows must fit the idle stages");
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -94,12 +97,12 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Each warp owns keys 8w .. 8w + 7 of every tile and keeps its own running
-// (m, l) and output rows for the G heads, so the tile loop needs no
-// CTA-wide barrier: a warp waits for the tile's bytes and, when it has read
-// the stage, counts itself out; the last warp out refills the stage with the
-// tile NST further on. The eight warps' states are merged at the end with
-// the same rescaling as the split merge.
+// Each warp owns keys 8w .. 8w + 7 of every tile: it streams their K and V
+// rows through its own NST-slot ring (own mbarriers, refilled by itself as
+// soon as it has read a slot) and keeps its own running (m, l) and output
+// rows for the G heads. The warps never wait for one another inside the
+// tile loop; their states are merged at the end with the same rescaling as
+// the split merge.
 template <int D, int GM>
 __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cache,
@@ -135,40 +138,60 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
   const int blk0 = t_begin / bs;
   const int nblk = (t_end - 1) / bs + 1 - blk0;  // <= kDecodeMaxTable (checked on the host)
 
-  uint8_t* sK = smem + L::K_OFF;
-  uint8_t* sV = smem + L::V_OFF;
+  uint8_t* sSlot = smem + L::SLOT_OFF + warp * L::WSLOT;  // this warp's slot of stage 0
   float* sQ = reinterpret_cast<float*>(smem + L::Q_OFF);
   float* sW = reinterpret_cast<float*>(smem + L::W_OFF + warp * L::W_BYTES);
   float* sML = reinterpret_cast<float*>(smem + L::ML_OFF);
   int* sTab = reinterpret_cast<int*>(smem + L::TAB_OFF);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  int* rel = reinterpret_cast<int*>(smem + L::CNT_OFF);
-  int* fills = rel + NST;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp;  // [st * WARPS]
+  int* fills = reinterpret_cast<int*>(smem + L::CNT_OFF) + warp;           // [st * WARPS]
 
   for (int i = tid; i < GM * D; i += THREADS) {
     const int g = i / D;
     sQ[i] = g < G ? __bfloat162float(q[(head0 + g) * D + (i % D)]) * scale_log2 : 0.f;
   }
   for (int i = tid; i < nblk; i += THREADS) sTab[i] = block_table[static_cast<size_t>(b) * max_blocks + blk0 + i];
-  if (tid < NST) {
-    rel[tid] = 0;
-    fills[tid] = 0;
-  }
-  if (tid == 0) {
-    for (int st = 0; st < NST; ++st) mbar_init(&full[st], 1);
+  if (lane == 0) {
+    for (int st = 0; st < NST; ++st) {
+      fills[st * WARPS] = 0;
+      mbar_init(&full[st * WARPS], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  // One warp: copy tile `tile` of K and V into stage st. Lane r takes the
-  // r-th run of consecutive tokens inside one cache block (r, r + 32, ...)
-  // and issues its K and V bulk copies, so the copies of a tile go out in
-  // parallel. Entries outside [0, num_blocks) are skipped (their rows keep
-  // old bytes, masked later) and reported; only copied bytes are expected.
+  // One warp: copy its 8 keys of tile `tile` (K rows, then V rows) into its
+  // slot of stage st. Lane r takes the r-th run of consecutive tokens inside
+  // one cache block. Entries outside [0, num_blocks) are skipped (their rows
+  // keep old bytes, masked later) and reported; only copied bytes are expected.
+  const bool single_run = (bs & 7) == 0;  // a warp's 8 keys never cross a block boundary
   auto issue = [&](int tile, int st) {
-    const int t0 = tile * TK, t1 = min(t_end, t0 + TK);
-    const int b0 = t0 / bs;                 // the only division per tile
-    const int nrun = (t1 - 1) / bs - b0 + 1;
+    const int t0 = tile * TK + warp * 8, t1 = min(t_end, t0 + 8);
+    if (single_run) {  // lane 0 alone: one table entry, two copies
+      if (lane == 0) {
+        ++fills[st * WARPS];
+        uint32_t nbytes = 0;
+        int blk = -1, off = 0;
+        if (t0 < t1) {
+          const int bi = t0 / bs;  // the only division per tile
+          off = t0 - bi * bs;
+          blk = sTab[bi - blk0];
+          if (blk >= 0 && blk < num_blocks) nbytes = static_cast<uint32_t>(t1 - t0) * L::ROW;
+          else atomicExch(err, DEV_BAD_INDEX);
+        }
+        mbar_arrive_expect_tx(&full[st * WARPS], 2 * nbytes);
+        if (nbytes) {
+          uint8_t* slot = sSlot + st * WARPS * L::WSLOT;
+          const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + off) * D;
+          bulk_load(slot, k_cache + src, nbytes, &full[st * WARPS]);
+          bulk_load(slot + 8 * L::ROW, v_cache + src, nbytes, &full[st * WARPS]);
+        }
+      }
+      __syncwarp();
+      return;
+    }
+    const int b0 = t0 / bs;  // the only division per tile
+    const int nrun = t0 < t1 ? (t1 - 1) / bs - b0 + 1 : 0;
     uint32_t bytes = 0;
     for (int r = lane; r < nrun; r += 32) {
       const int blk = sTab[b0 + r - blk0];
@@ -178,10 +201,11 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
     if (lane == 0) {
-      ++fills[st];
-      mbar_arrive_expect_tx(&full[st], 2 * bytes);
+      ++fills[st * WARPS];
+      mbar_arrive_expect_tx(&full[st * WARPS], 2 * bytes);
     }
     __syncwarp();
+    uint8_t* slot = sSlot + st * WARPS * L::WSLOT;
     for (int r = lane; r < nrun; r += 32) {
       const int blk = sTab[b0 + r - blk0];
       const int rs = max(t0, (b0 + r) * bs), re = min(t1, (b0 + r + 1) * bs);
@@ -189,8 +213,8 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
         const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + (rs - (b0 + r) * bs)) * D;
         const uint32_t dst = static_cast<uint32_t>(rs - t0) * L::ROW;
         const uint32_t nbytes = static_cast<uint32_t>(re - rs) * L::ROW;
-        bulk_load(sK + st * L::TILE + dst, k_cache + src, nbytes, &full[st]);
-        bulk_load(sV + st * L::TILE + dst, v_cache + src, nbytes, &full[st]);
+        bulk_load(slot + dst, k_cache + src, nbytes, &full[st * WARPS]);
+        bulk_load(slot + 8 * L::ROW + dst, v_cache + src, nbytes, &full[st * WARPS]);
       } else {
         atomicExch(err, DEV_BAD_INDEX);
       }
@@ -230,19 +254,18 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
 #pragma unroll
     for (int c = 0; c < CPL / 2; ++c) acc[g][c] = make_float2(0.f, 0.f);
 
-  // The first NST tiles fill every stage.
-  if (warp == 0)
-    for (int j = 0; j < NST && tile0 + j < tile1; ++j) issue(tile0 + j, j);
-  __syncthreads();
+  // The first NST tiles fill every slot of this warp.
+  __syncthreads();  // barrier inits and the table slice are visible
+  for (int j = 0; j < NST && tile0 + j < tile1; ++j) issue(tile0 + j, j);
   bool ok = true;
   int it = 0;
   for (int tile = tile0; tile < tile1; ++tile, ++it) {
     const int st = it % NST;
-    ok = mbar_wait_warp(&full[st], (it / NST) & 1, err);
+    ok = mbar_wait_warp(&full[st * WARPS], (it / NST) & 1, err);
     if (!ok) break;
     const int nk = min(t_end, (tile + 1) * TK) - tile * TK;
-    const uint8_t* kt = sK + st * L::TILE;
-    const uint32_t* vt = reinterpret_cast<const uint32_t*>(sV + st * L::TILE);
+    const uint8_t* kt = sSlot + st * WARPS * L::WSLOT;  // this warp's 8 K rows, then its 8 V rows
+    const uint32_t* vt = reinterpret_cast<const uint32_t*>(kt + 8 * L::ROW);
 #pragma unroll
     for (int hg = 0; hg < GM / 4; ++hg) {
       if (hg * 4 >= G) continue;  // warp-uniform
@@ -256,7 +279,7 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
         for (int j = 0; j < 4; ++j) a[j] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < CH; ++ch) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(kt + k * L::ROW + (dq + 8 * ch) * 16);
+          const uint4 kv = *reinterpret_cast<const uint4*>(kt + kk * L::ROW + (dq + 8 * ch) * 16);
           const float2 k0 = bf2_to_f2(kv.x), k1 = bf2_to_f2(kv.y), k2 = bf2_to_f2(kv.z), k3 = bf2_to_f2(kv.w);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -327,7 +350,7 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
           // Rows past the context end were never copied (P is 0 there, and
           // their bytes may be anything): skip them, warp-uniformly.
           if (warp * 8 + kk >= nk) break;
-          const uint32_t* vr = vt + (warp * 8 + kk) * (D / 2) + lane * (CPL / 2);
+          const uint32_t* vr = vt + kk * (D / 2) + lane * (CPL / 2);
           float2 v[CPL / 2];
 #pragma unroll
           for (int c = 0; c < CPL / 2; ++c) v[c] = bf2_to_f2(vr[c]);
@@ -343,25 +366,19 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
       }
       __syncwarp();  // the scratch is rewritten by the next head group
     }
-    // This warp has read stage st; the last warp out refills it.
-    int last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicAdd(&rel[st], 1) == WARPS - 1;
-      if (last) rel[st] = 0;
-    }
-    if (__shfl_sync(0xffffffffu, last, 0) && tile + NST < tile1) issue(tile + NST, st);
+    // This warp has read its slot of stage st: refill it.
+    if (tile + NST < tile1) issue(tile + NST, st);
   }
   if (__syncthreads_or(!ok)) {
     // Let copies already issued land before the CTA exits (bounded).
-    if (tid == 0)
+    if (lane == 0)
       for (int st = 0; st < NST; ++st)
-        if (fills[st] > 0) mbar_wait(&full[st], (fills[st] - 1) & 1, err);
+        if (fills[st * WARPS] > 0) mbar_wait(&full[st * WARPS], (fills[st * WARPS] - 1) & 1, err);
     return;
   }
   // Merge the warps' states per head: M = max_w m_w, L = Σ_w l_w 2^(m_w − M),
   // o = Σ_w acc_w 2^(m_w − M) / L, lse = (M + log2 L)·ln 2.
-  float* sAcc = reinterpret_cast<float*>(smem + L::K_OFF);  // [WARPS][GM][D]; the stages are idle
+  float* sAcc = reinterpret_cast<float*>(smem + L::SLOT_OFF);  // [WARPS][GM][D]; the stages are idle
 #pragma unroll
   for (int g = 0; g < GM; ++g)
 #pragma unroll
