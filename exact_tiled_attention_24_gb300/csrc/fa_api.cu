@@ -183,7 +183,8 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (H / Hkv > 16 || B > 65535 || Hkv > 65535 || n_splits > 4096) return FA_ERR_UNSUPPORTED;
+  if (B > 65535 || static_cast<long long>(Hkv) * ((H / Hkv + 15) / 16) > 65535 || n_splits > 4096)
+    return FA_ERR_UNSUPPORTED;
   const long long ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
   if (ctx > INT_MAX / 2 || static_cast<long long>(num_blocks) * Hkv * block_size * d > (1ll << 40))
     return FA_ERR_UNSUPPORTED;

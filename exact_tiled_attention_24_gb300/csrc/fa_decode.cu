@@ -19,7 +19,8 @@
 // Kernels:
 //   decode_partial  one CTA per (context split, K/V head, request). It serves
 //                   the G query heads that share the K/V head, so each K/V
-//                   byte is read once per step. 64-key tiles of K and V are
+//                   byte is read once per step (G > 16: one CTA per 16 of
+//                   them, each reading the K/V head). 64-key tiles of K and V are
 //                   copied into shared memory by bulk copies (one per run of
 //                   consecutive tokens inside a cache block), three tiles in
 //                   flight. Each warp owns 8 keys of every tile and keeps
@@ -114,10 +115,13 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
   constexpr int CPL = D / 32;  // output columns per lane
   extern __shared__ __align__(1024) uint8_t smem[];
   const int S = gridDim.x;
-  const int s = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  // blockIdx.y = (K/V head, chunk of at most 16 of its query heads)
+  const int G_all = H / Hkv;
+  const int n_chunk = (G_all + 15) / 16;
+  const int s = blockIdx.x, hk = blockIdx.y / n_chunk, chunk = blockIdx.y % n_chunk, b = blockIdx.z;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int G = H / Hkv;
+  const int G = min(16, G_all - 16 * chunk);  // query heads served by this CTA
   uint32_t* err = &g_dec_err;
 
   // Context of request b, clamped to what its block-table row can address.
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(THREADS) decode_partial_kernel(
   const int tps = (n_tiles + S - 1) / S;  // tiles per split
   const int tile0 = s * tps;
   const int tile1 = min(n_tiles, tile0 + tps);
-  const size_t head0 = static_cast<size_t>(b) * H + static_cast<size_t>(hk) * G;  // first query head
+  const size_t head0 = static_cast<size_t>(b) * H + static_cast<size_t>(hk) * G_all + 16 * chunk;  // first query head
   const size_t prow = static_cast<size_t>(s) * B * H + head0;                     // its partial row
   if (tile0 >= tile1) {  // no key in this split: o_s = 0, lse_s = -inf (weight 0 in the merge)
     for (int i = tid; i < G * D; i += THREADS) o_part[prow * D + i] = 0.f;
@@ -451,7 +455,8 @@ static cudaError_t launch_partial_t(const void* q, const void* kc, const void* v
   const int smem = Smem<D, GM>::BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(Hkv), static_cast<unsigned>(B));
+  const int n_chunk = (H / Hkv + 15) / 16;  // CTAs per K/V head (16 query heads each at most)
+  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(Hkv * n_chunk), static_cast<unsigned>(B));
   kern<<<grid, THREADS, smem, stream>>>(static_cast<const __nv_bfloat16*>(q),
                                          static_cast<const __nv_bfloat16*>(kc),
                                          static_cast<const __nv_bfloat16*>(vc), table, seq_lens, o_part,

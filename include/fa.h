@@ -239,8 +239,8 @@ int fa_attn_merge(const float* o_parts, const float* lse_parts, int n_parts, voi
  *                whole 64-token tiles, processed in parallel and combined
  *                as in fa_attn_merge (two kernels on `stream`).
  * Errors: null pointer, sizes < 1, Hkv not dividing H, bad scale ->
- * FA_ERR_INVALID_ARG; d not 64/128, H/Hkv > 16, B or Hkv > 65535, a split
- * that could span more than 1024 cache blocks (use more splits) ->
+ * FA_ERR_INVALID_ARG; d not 64/128, B > 65535, Hkv·ceil(H/Hkv / 16) > 65535,
+ * a split that could span more than 1024 cache blocks (use more splits) ->
  * FA_ERR_UNSUPPORTED; short workspace -> FA_ERR_WORKSPACE; misaligned ->
  * FA_ERR_MISALIGNED. A block-table entry outside [0, num_blocks) is never
  * dereferenced: the tokens it maps are skipped (the results are then

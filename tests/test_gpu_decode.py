@@ -54,6 +54,8 @@ def run_case(fa, q, kc, vc, table, lens, n_splits, scale):
     (1, 16, 1, 128, 16, [777], 5),           # 16 query heads on one K/V head
     (3, 4, 2, 128, 16, [0, 1, 129], 2),      # an empty context
     (1, 2, 1, 64, 48, [2000], 7),            # block size not a power of two
+    (2, 32, 1, 128, 16, [300, 1500], 3),     # 32 query heads on one K/V head: two CTAs of 16
+    (1, 24, 1, 64, 32, [777], 2),            # 24 = 16 + 8
 ])
 def test_decode_paged_vs_oracle(fa, B, H, Hkv, d, bs, seq_lens, n_splits):
     q, kc, vc, table, lens = paged_case(B, H, Hkv, d, bs, seq_lens, seed=B * 100 + H + bs + sum(seq_lens))
