@@ -103,9 +103,11 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
 // soon as it has read a slot) and keeps its own running (m, l) and output
 // rows for the G heads. The warps never wait for one another inside the
 // tile loop; their states are merged at the end with the same rescaling as
-// the split merge.
+// the split merge. Two CTAs share an SM (the ring depth above assumes it),
+// so the kernel is held to 128 registers a thread, except with 16 heads of
+// 128 columns, whose accumulators would then spill.
 template <int D, int GM>
-__global__ void __launch_bounds__(THREADS) decode_partial_kernel(
+__global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cache,
     const __nv_bfloat16* __restrict__ v_cache, const int* __restrict__ block_table,
     const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B,
