@@ -29,6 +29,8 @@ __all__ = [
     "attn_merge",
     "decode_paged",
     "decode_workspace_bytes",
+    "fwd_host",
+    "fwd_bwd_host",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -65,7 +67,14 @@ EXPORTED_SYMBOLS = (
     "fa_attn_merge",
     "fa_decode_workspace_bytes",
     "fa_decode_paged",
+    "fa_fwd_host",
+    "fa_fwd_bwd_host",
 )
+
+
+class Tensors(ctypes.Structure):
+    """fa_tensors: addresses of one problem's q, k, v, dO, o, lse, dq, dk, dv."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "dO", "o", "lse", "dq", "dk", "dv")]
 
 
 class FAError(RuntimeError):
@@ -114,6 +123,11 @@ def lib() -> ctypes.CDLL:
         L.fa_decode_workspace_bytes.restype = sz
         L.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, i, f, i, vp]
         L.fa_decode_paged.restype = i
+        tp = ctypes.POINTER(Tensors)
+        L.fa_fwd_host.argtypes = [tp, tp, i, i, i, i, i, f, i, i, vp]
+        L.fa_fwd_host.restype = i
+        L.fa_fwd_bwd_host.argtypes = [tp, tp, vp, sz, i, i, i, i, i, f, i, i, vp]
+        L.fa_fwd_bwd_host.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
         L.fa_status_string.argtypes = [i]
@@ -296,3 +310,66 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, n_splits=1, scale=N
                                  block_table.shape[1], _scale(d, scale), n_splits, _stream(q.device)),
            "fa_decode_paged")
     return o, lse_t
+
+
+_HOST_NAMES = ("q", "k", "v", "dO", "o", "lse", "dq", "dk", "dv")
+
+
+def _tensors(ts: dict, on_cuda: bool, shapes: dict, names):
+    """Check one side's tensors (shape, dtype, contiguity, device kind) and
+    pack their addresses into a Tensors struct."""
+    st = Tensors()
+    for n in names:
+        t = ts.get(n)
+        if t is None:
+            raise ValueError(f"missing tensor {n!r}")
+        want_dtype = torch.float32 if n == "lse" else torch.bfloat16
+        if tuple(t.shape) != shapes[n] or t.dtype != want_dtype or not t.is_contiguous():
+            raise ValueError(f"{n}: expected a contiguous {want_dtype} tensor of shape {shapes[n]}")
+        if t.is_cuda != on_cuda:
+            raise ValueError(f"{n}: expected a {'CUDA' if on_cuda else 'host'} tensor")
+        setattr(st, n, t.data_ptr())
+    return st
+
+
+def _host_shapes(q, k):
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    qs, kvs = (B, H, N, d), (B, Hkv, N, d)
+    return {"q": qs, "k": kvs, "v": kvs, "dO": qs, "o": qs, "lse": (B, H, N), "dq": qs, "dk": kvs,
+            "dv": kvs}
+
+
+def fwd_host(host: dict, dev: dict, causal=False, scale=None, n_chunks=0):
+    """Forward from host memory: host["q"], ["k"], ["v"] (CPU, ideally
+    pinned) are copied into dev["q"], ["k"], ["v"] (CUDA), the forward runs
+    there, and dev["o"], ["lse"] are copied back into host["o"], ["lse"], in
+    n_chunks pipelined slices (0: the library's default). Asynchronous on the
+    current stream: synchronise it before reading host["o"]."""
+    names = ("q", "k", "v", "o", "lse")
+    q, k = host["q"], host["k"]
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    shapes = _host_shapes(q, k)
+    h = _tensors(host, False, shapes, names)
+    dv = _tensors(dev, True, shapes, names)
+    _check(lib().fa_fwd_host(ctypes.byref(h), ctypes.byref(dv), B, H, Hkv, N, d, _scale(d, scale),
+                             int(bool(causal)), int(n_chunks), _stream(dev["q"].device)), "fa_fwd_host")
+
+
+def fwd_bwd_host(host: dict, dev: dict, workspace, causal=False, scale=None, n_chunks=0):
+    """Forward and backward from host memory: as fwd_host, plus host["dO"]
+    in and host["dq"], ["dk"], ["dv"] out; workspace is a CUDA buffer of
+    bwd_workspace_bytes(B, H, N, d) bytes."""
+    q, k = host["q"], host["k"]
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    shapes = _host_shapes(q, k)
+    h = _tensors(host, False, shapes, _HOST_NAMES)
+    dv = _tensors(dev, True, shapes, _HOST_NAMES)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    _check(lib().fa_fwd_bwd_host(ctypes.byref(h), ctypes.byref(dv), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+                                 _scale(d, scale), int(bool(causal)), int(n_chunks),
+                                 _stream(dev["q"].device)), "fa_fwd_bwd_host")

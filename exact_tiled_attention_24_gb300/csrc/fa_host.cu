@@ -1,0 +1,258 @@
+// Attention steps whose inputs and outputs live in host memory.
+//
+// The (batch, K/V head) pairs are independent problems, so the step is cut
+// into slices of consecutive pairs and run as a three-stage pipeline:
+//   copy-in stream   q, k, v (and dO) of slice c, host -> device
+//   caller's stream  forward (and backward) kernels of slice c
+//   copy-out stream  o, lse (and dq, dk, dv) of slice c, device -> host
+// Events order each slice's stages; slice c's kernels run while slice c+1
+// is copied in and slice c-1 is copied out. In the [B][H][N][d] layout a
+// run of consecutive (b, h) pairs is one contiguous range of every tensor,
+// so each tensor of a slice moves in one copy. The kernels are the device
+// entry points' own, launched on the slice's sub-range; results do not
+// depend on the slicing.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/fa.h"
+#include "fa_common.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxChunks = 64;
+constexpr int kDefaultChunks = 8;
+
+// The copy streams of one host thread on one device, created on first use
+// and kept for the thread's lifetime (non-blocking: they never wait on the
+// legacy default stream).
+struct CopyStreams {
+  cudaStream_t in = nullptr;
+  cudaStream_t out = nullptr;
+};
+
+cudaError_t copy_streams(CopyStreams** out) {
+  thread_local CopyStreams per_device[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CopyStreams& cs = per_device[dev];
+  if (cs.in == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&cs.in, cudaStreamNonBlocking)) != cudaSuccess) {
+      cs.in = nullptr;
+      return e;
+    }
+  }
+  if (cs.out == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&cs.out, cudaStreamNonBlocking)) != cudaSuccess) {
+      cs.out = nullptr;
+      return e;
+    }
+  }
+  *out = &cs;
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Events of one call, released when the call returns (CUDA defers the
+// release until the recorded work has completed).
+struct Events {
+  std::vector<cudaEvent_t> ev;
+  ~Events() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+  cudaError_t make(cudaEvent_t* out) {
+    cudaError_t e = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
+    if (e == cudaSuccess) ev.push_back(*out);
+    return e;
+  }
+};
+
+#define FA_TRY(expr)                         \
+  do {                                       \
+    cudaError_t e_ = (expr);                 \
+    if (e_ != cudaSuccess) return e_;        \
+  } while (0)
+
+// Byte offset of row block [u0, u1) of a tensor with `per_unit` bytes per
+// (batch, K/V head) pair.
+struct Slice {
+  size_t off, bytes;
+};
+Slice slice(long long u0, long long u1, size_t per_unit) {
+  return {static_cast<size_t>(u0) * per_unit, static_cast<size_t>(u1 - u0) * per_unit};
+}
+
+const char* cptr(const void* p, size_t off) { return static_cast<const char*>(p) + off; }
+char* mptr(void* p, size_t off) { return static_cast<char*>(p) + off; }
+
+cudaError_t copy_in(void* dst, const void* src, Slice s, cudaStream_t st) {
+  return cudaMemcpyAsync(mptr(dst, s.off), cptr(src, s.off), s.bytes, cudaMemcpyHostToDevice, st);
+}
+cudaError_t copy_out(void* dst, const void* src, Slice s, cudaStream_t st) {
+  return cudaMemcpyAsync(mptr(dst, s.off), cptr(src, s.off), s.bytes, cudaMemcpyDeviceToHost, st);
+}
+
+// The pipeline; argument checks are done by the callers.
+cudaError_t run_pipeline(const fa_tensors& h, const fa_tensors& dv, float* Dvec, bool with_bwd, int B,
+                         int H, int Hkv, int N, int d, float scale, bool causal, int n_chunks,
+                         cudaStream_t stream) {
+  CopyStreams* cs = nullptr;
+  FA_TRY(copy_streams(&cs));
+  const int G = H / Hkv;
+  const long long units = static_cast<long long>(B) * Hkv;  // (batch, K/V head) pairs
+  const int C = static_cast<int>(n_chunks < units ? n_chunks : units);
+  const size_t row_b = static_cast<size_t>(N) * d * 2;  // one head of a bf16 tensor
+  const size_t q_unit = row_b * G, kv_unit = row_b;     // bytes per pair
+  const size_t r_unit = static_cast<size_t>(N) * G * 4;  // lse, D per pair
+  auto bounds = [&](int c, long long* u0, long long* u1) {
+    *u0 = units * c / C;
+    *u1 = units * (c + 1) / C;
+  };
+
+  Events evs;
+  cudaEvent_t start, done;
+  std::vector<cudaEvent_t> in_ready(C), fwd_done(C), bwd_done(C);
+  FA_TRY(evs.make(&start));
+  FA_TRY(evs.make(&done));
+  for (int c = 0; c < C; ++c) {
+    FA_TRY(evs.make(&in_ready[c]));
+    FA_TRY(evs.make(&fwd_done[c]));
+    if (with_bwd) FA_TRY(evs.make(&bwd_done[c]));
+  }
+  // Both copy streams start after the work already queued on `stream`.
+  FA_TRY(cudaEventRecord(start, stream));
+  FA_TRY(cudaStreamWaitEvent(cs->in, start, 0));
+  FA_TRY(cudaStreamWaitEvent(cs->out, start, 0));
+
+  cudaError_t err = cudaSuccess;
+  // Stage 1: every slice's inputs, back to back.
+  for (int c = 0; c < C && err == cudaSuccess; ++c) {
+    long long u0, u1;
+    bounds(c, &u0, &u1);
+    const Slice sq = slice(u0, u1, q_unit), skv = slice(u0, u1, kv_unit);
+    if ((err = copy_in(const_cast<void*>(dv.q), h.q, sq, cs->in)) != cudaSuccess) break;
+    if ((err = copy_in(const_cast<void*>(dv.k), h.k, skv, cs->in)) != cudaSuccess) break;
+    if ((err = copy_in(const_cast<void*>(dv.v), h.v, skv, cs->in)) != cudaSuccess) break;
+    if (with_bwd && (err = copy_in(const_cast<void*>(dv.dO), h.dO, sq, cs->in)) != cudaSuccess) break;
+    err = cudaEventRecord(in_ready[c], cs->in);
+  }
+  // Stage 2: the kernels of each slice, on the caller's stream.
+  for (int c = 0; c < C && err == cudaSuccess; ++c) {
+    long long u0, u1;
+    bounds(c, &u0, &u1);
+    const int bh = static_cast<int>((u1 - u0) * G);  // query heads in the slice
+    const size_t oq = slice(u0, u1, q_unit).off, okv = slice(u0, u1, kv_unit).off;
+    const size_t orow = slice(u0, u1, r_unit).off;
+    float* lse = reinterpret_cast<float*>(mptr(dv.lse, orow));
+    if ((err = cudaStreamWaitEvent(stream, in_ready[c], 0)) != cudaSuccess) break;
+    err = fa::launch_fwd(cptr(dv.q, oq), cptr(dv.k, okv), cptr(dv.v, okv), mptr(dv.o, oq), lse, bh, G, N, d,
+                         scale, causal, stream);
+    if (err != cudaSuccess) break;
+    if ((err = cudaEventRecord(fwd_done[c], stream)) != cudaSuccess) break;
+    if (!with_bwd) continue;
+    float* D = reinterpret_cast<float*>(mptr(Dvec, orow));
+    err = fa::launch_bwd_preprocess(reinterpret_cast<const __nv_bfloat16*>(cptr(dv.o, oq)),
+                                    reinterpret_cast<const __nv_bfloat16*>(cptr(dv.dO, oq)), D, bh, N, d,
+                                    stream);
+    if (err != cudaSuccess) break;
+    err = fa::launch_bwd_dkdv(cptr(dv.q, oq), cptr(dv.k, okv), cptr(dv.v, okv), cptr(dv.dO, oq),
+                              mptr(dv.dk, okv), mptr(dv.dv, okv), lse, D, bh, G, N, d, scale, causal, stream);
+    if (err != cudaSuccess) break;
+    err = fa::launch_bwd_dq(cptr(dv.q, oq), cptr(dv.k, okv), cptr(dv.v, okv), cptr(dv.dO, oq),
+                            mptr(dv.dq, oq), lse, D, bh, G, N, d, scale, causal, stream);
+    if (err != cudaSuccess) break;
+    err = cudaEventRecord(bwd_done[c], stream);
+  }
+  // Stage 3: every slice's outputs, each as soon as its kernels are done.
+  for (int c = 0; c < C && err == cudaSuccess; ++c) {
+    long long u0, u1;
+    bounds(c, &u0, &u1);
+    const Slice sq = slice(u0, u1, q_unit), skv = slice(u0, u1, kv_unit), sr = slice(u0, u1, r_unit);
+    if ((err = cudaStreamWaitEvent(cs->out, fwd_done[c], 0)) != cudaSuccess) break;
+    if ((err = copy_out(h.o, dv.o, sq, cs->out)) != cudaSuccess) break;
+    if ((err = copy_out(h.lse, dv.lse, sr, cs->out)) != cudaSuccess) break;
+    if (!with_bwd) continue;
+    if ((err = cudaStreamWaitEvent(cs->out, bwd_done[c], 0)) != cudaSuccess) break;
+    if ((err = copy_out(h.dq, dv.dq, sq, cs->out)) != cudaSuccess) break;
+    if ((err = copy_out(h.dk, dv.dk, skv, cs->out)) != cudaSuccess) break;
+    err = copy_out(h.dv, dv.dv, skv, cs->out);
+  }
+  // Join: `stream` passes this point only after both copy streams have
+  // drained what this call queued on them, also after a failure half-way.
+  cudaError_t e1 = cudaEventRecord(done, cs->in);
+  if (e1 == cudaSuccess) e1 = cudaStreamWaitEvent(stream, done, 0);
+  cudaEvent_t done_out;
+  cudaError_t e2 = evs.make(&done_out);
+  if (e2 == cudaSuccess) e2 = cudaEventRecord(done_out, cs->out);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(stream, done_out, 0);
+  if (err != cudaSuccess) return err;
+  return e1 != cudaSuccess ? e1 : e2;
+}
+
+int check_common(const fa_tensors* host, const fa_tensors* dev, bool with_bwd, int B, int H, int Hkv,
+                 int N, int d, float scale, int n_chunks) {
+  if (!host || !dev) return FA_ERR_INVALID_ARG;
+  const void* hp[] = {host->q, host->k, host->v, host->o, host->lse};
+  const void* dp[] = {dev->q, dev->k, dev->v, dev->o, dev->lse};
+  for (const void* p : hp)
+    if (!p) return FA_ERR_INVALID_ARG;
+  for (const void* p : dp) {
+    if (!p) return FA_ERR_INVALID_ARG;
+    if (!aligned16(p)) return FA_ERR_MISALIGNED;
+  }
+  if (with_bwd) {
+    const void* hb[] = {host->dO, host->dq, host->dk, host->dv};
+    const void* db[] = {dev->dO, dev->dq, dev->dk, dev->dv};
+    for (const void* p : hb)
+      if (!p) return FA_ERR_INVALID_ARG;
+    for (const void* p : db) {
+      if (!p) return FA_ERR_INVALID_ARG;
+      if (!aligned16(p)) return FA_ERR_MISALIGNED;
+    }
+  }
+  if (B < 1 || H < 1 || N < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale <= 0.f) return FA_ERR_INVALID_ARG;
+  if (n_chunks < 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * N > INT_MAX) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int chunks_or_default(int n_chunks) {
+  if (n_chunks == 0) return kDefaultChunks;
+  return n_chunks > kMaxChunks ? kMaxChunks : n_chunks;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_host(const fa_tensors* host, const fa_tensors* dev, int B, int H, int Hkv, int N, int d,
+                float scale, int causal, int n_chunks, void* stream) {
+  const int st = check_common(host, dev, false, B, H, Hkv, N, d, scale, n_chunks);
+  if (st != FA_OK) return st;
+  const cudaError_t e = run_pipeline(*host, *dev, nullptr, false, B, H, Hkv, N, d, scale, causal != 0,
+                                     chunks_or_default(n_chunks), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_bwd_host(const fa_tensors* host, const fa_tensors* dev, void* workspace, size_t ws_bytes, int B,
+                    int H, int Hkv, int N, int d, float scale, int causal, int n_chunks, void* stream) {
+  const int st = check_common(host, dev, true, B, H, Hkv, N, d, scale, n_chunks);
+  if (st != FA_OK) return st;
+  if (!workspace || ws_bytes < static_cast<size_t>(B) * H * N * sizeof(float)) return FA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
+  const cudaError_t e = run_pipeline(*host, *dev, static_cast<float*>(workspace), true, B, H, Hkv, N, d,
+                                     scale, causal != 0, chunks_or_default(n_chunks),
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -138,6 +138,60 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const
               const float* Dvec, void* dq, int B, int H, int Hkv, int N, int d, float scale,
               int causal, void* stream);
 
+/*
+ * Addresses of one attention problem's tensors, in host or in device
+ * memory depending on the argument they are passed as. Shapes and types as
+ * in fa_fwd_gqa / fa_bwd_gqa: q, dO, o, dq [B][H][N][d] bf16; k, v, dk, dv
+ * [B][Hkv][N][d] bf16; lse [B][H][N] fp32. dO, dq, dk, dv are unused (may
+ * be NULL) in fa_fwd_host.
+ */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dO;
+  void* o;
+  float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+} fa_tensors;
+
+/*
+ * Attention from host memory: copies q, k, v (and dO) from `host` to the
+ * device buffers in `dev`, runs fa_fwd_gqa (and fa_bwd_gqa, its D vector
+ * in `workspace`, fa_bwd_workspace_bytes(B, H, N, d) bytes) on them, and
+ * copies o, lse (and dq, dk, dv) back into `host`. The results are those
+ * of the device calls, bit for bit, and are also left in `dev`.
+ *
+ * The (batch, K/V head) pairs are independent problems, so the work is cut
+ * into n_chunks slices of consecutive pairs (0 = 8; more than B·Hkv or 64
+ * is clamped), and each slice's copies overlap other slices' kernels: its
+ * inputs go in on a copy-in stream, its kernels run on `stream`, its
+ * outputs come out on a copy-out stream as soon as they are ready. Host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister), else
+ * the copies are staged by the driver and do not overlap.
+ *
+ *   Ordering   the call starts after the work already queued on `stream`,
+ *              and work queued on `stream` after it starts after every
+ *              copy of this call has finished: synchronise `stream`
+ *              before reading the host outputs or reusing the host inputs.
+ *   Resources  the first call on a host thread and device creates two
+ *              non-blocking CUDA streams, kept until the thread exits;
+ *              each call creates and releases a few CUDA events. No
+ *              memory is allocated.
+ * Errors: as fa_fwd_gqa / fa_bwd_gqa for sizes, heads, scale, alignment of
+ * the device pointers and the workspace (host pointers have no alignment
+ * rule); a NULL struct or a NULL pointer it must hold, or n_chunks < 0 ->
+ * FA_ERR_INVALID_ARG. FA_ERR_CUDA when a copy, event or launch fails after
+ * part of the work was queued; `stream` is still ordered after whatever was.
+ */
+int fa_fwd_host(const fa_tensors* host, const fa_tensors* dev, int B, int H, int Hkv, int N, int d,
+                float scale, int causal, int n_chunks, void* stream);
+int fa_fwd_bwd_host(const fa_tensors* host, const fa_tensors* dev, void* workspace, size_t ws_bytes,
+                    int B, int H, int Hkv, int N, int d, float scale, int causal, int n_chunks,
+                    void* stream);
+
 /* Size in bytes of the static scratch area behind fa_bwd_noalloc (32 MiB). */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -167,3 +167,41 @@ def test_decode_and_merge_argument_errors(L):
     assert merge(d=80) == 2
     assert merge(o_parts=MIS) == 3
     assert L.fa_status_string(7) == b"FA_ERR_BAD_INDEX"
+
+
+def test_host_pipeline_argument_errors(L):
+    def ts(**over):
+        t = fa.Tensors(*([0x10000] * 9))
+        for k, val in over.items():
+            setattr(t, k, val)
+        return t
+
+    def fwd_h(host=None, dev=None, B=1, H=4, Hkv=2, N=16, d=64, scale=0.125, chunks=0):
+        h = ctypes.byref(host if host is not None else ts())
+        dv = ctypes.byref(dev if dev is not None else ts())
+        return L.fa_fwd_host(h, dv, B, H, Hkv, N, d, scale, 0, chunks, NUL)
+
+    def fb_h(host=None, dev=None, ws=FAKE, ws_bytes=4 * 4 * 16, B=1, H=4, Hkv=2, N=16, d=64, chunks=0):
+        h = ctypes.byref(host if host is not None else ts())
+        dv = ctypes.byref(dev if dev is not None else ts())
+        return L.fa_fwd_bwd_host(h, dv, ws, ws_bytes, B, H, Hkv, N, d, 0.125, 1, chunks, NUL)
+
+    tp = ctypes.POINTER(fa.Tensors)
+    assert L.fa_fwd_host(tp(), ctypes.byref(ts()), 1, 4, 2, 16, 64, 0.125, 0, 0, NUL) == 1
+    assert fwd_h(host=ts(q=None)) == 1
+    assert fwd_h(dev=ts(lse=None)) == 1
+    assert fwd_h(Hkv=3) == 1
+    assert fwd_h(N=0) == 1
+    assert fwd_h(scale=float("inf")) == 1
+    assert fwd_h(chunks=-1) == 1
+    assert fwd_h(d=96) == 2
+    assert fwd_h(dev=ts(o=0x10004)) == 3
+    # forward-only calls ignore the gradient slots
+    assert fwd_h(host=ts(dO=None, dq=None, dk=None, dv=None), d=96) == 2
+    assert fb_h(host=ts(dO=None)) == 1
+    assert fb_h(dev=ts(dk=None)) == 1
+    assert fb_h(dev=ts(dv=0x10008)) == 3
+    assert fb_h(ws=NUL) == 6
+    assert fb_h(ws_bytes=4 * 4 * 16 - 1) == 6
+    assert fb_h(ws=MIS) == 3
+    assert fb_h(d=80) == 2
