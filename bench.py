@@ -293,6 +293,15 @@ def run_ours(args, w, rank, world, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
+    # Distribution of the per-step device time (first kernel start to last
+    # kernel end of each timed step).
+    last = 4 if has_bwd else 1
+    per_step = sorted(e[0].elapsed_time(e[last]) for e in evs)
+
+    def pct(q):
+        return per_step[min(len(per_step) - 1, int(q * (len(per_step) - 1) + 0.5))]
+
+    step_stats = {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9), "n": len(per_step)}
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     if has_bwd:
         pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
@@ -368,6 +377,7 @@ def run_ours(args, w, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(args, w),
+        "step_ms": step_stats,
         "fwd_tflops": F_fwd / (fwd_ms * 1e-3) / 1e12,
         "fwd_ms": fwd_ms,
         "frac_of_peak": {"fwd_bwd": value / world / peak, "fwd": F_fwd / (fwd_ms * 1e-3) / 1e12 / peak,

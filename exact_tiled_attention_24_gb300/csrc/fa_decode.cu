@@ -351,11 +351,7 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
 #pragma unroll
           for (int c = 0; c < CPL / 2; ++c)
             acc[hg * 4 + j][c] = make_float2(acc[hg * 4 + j][c].x * alj[j], acc[hg * 4 + j][c].y * alj[j]);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // Rows past the context end were never copied (P is 0 there, and
-          // their bytes may be anything): skip them, warp-uniformly.
-          if (warp * 8 + kk >= nk) break;
+        auto pv_key = [&](int kk) {
           const uint32_t* vr = vt + kk * (D / 2) + lane * (CPL / 2);
           float2 v[CPL / 2];
 #pragma unroll
@@ -368,6 +364,20 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
           for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int c = 0; c < CPL / 2; ++c) acc[hg * 4 + j][c] = fma2(v[c], pp[j], acc[hg * 4 + j][c]);
+        };
+        if (warp * 8 + 8 <= nk) {
+          // All 8 rows hold copied keys (every tile but a context's last):
+          // a branch-free loop whose shared-memory loads can be hoisted.
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) pv_key(kk);
+        } else {
+          // Rows past the context end were never copied (P is 0 there, and
+          // their bytes may be anything): skip them, warp-uniformly.
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            if (warp * 8 + kk >= nk) break;
+            pv_key(kk);
+          }
         }
       }
       __syncwarp();  // the scratch is rewritten by the next head group

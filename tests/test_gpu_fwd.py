@@ -138,3 +138,21 @@ def test_fwd_misaligned_pointer_rejected(fa):
     with pytest.raises(fa.FAError) as e:
         fa.fwd(qm, k.to(dev), v.to(dev))
     assert e.value.status == 3
+
+
+def test_fwd_long_context_sampled_rows(fa):
+    """N = 131072 (four times the longest benchmark context) on two heads:
+    TMA coordinates, tile counts and the causal bound at the largest N the
+    tests reach; sampled rows against the oracle."""
+    B, H, N, d = 1, 2, 131072, 128
+    q, k, v = make_inputs(B, H, N, d, seed=1313, with_do=False)
+    dev = torch.device("cuda")
+    o, lse = fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    rows = np.array(sorted({0, 1, 127, 128, 65535, 65536, 100001, N - 129, N - 128, N - 2, N - 1}))
+    for h in range(H):
+        ro, rlse = attention_fwd_head(to_f64(q[0, h]), to_f64(k[0, h]), to_f64(v[0, h]), 1.0 / d ** 0.5,
+                                      True, rows=rows)
+        assert_o(o[0, h, rows].cpu(), ro, what=f"o[0,{h}]")
+        assert_lse(lse[0, h, rows].cpu(), rlse)
