@@ -46,6 +46,31 @@ def flops(w, direction):
     return per_pair * w.B * w.H * pairs
 
 
+def barrier(dist):
+    """Line the ranks up (no-op at world size 1)."""
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(values, dist, device):
+    """Each value's maximum over the ranks: the slowest rank's time sets
+    the job's time. The values themselves at world size 1."""
+    values = [float(x) for x in values]
+    if dist is None:
+        return values
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units per second over the whole job: every rank runs the same
+    workload on its own GPU (weak scaling) and `ms` is the max-over-ranks
+    time of one step."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -274,8 +299,7 @@ def run_ours(args, w, rank, world, dist):
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
     except Exception:
         bus = None
-    if dist is not None:
-        dist.barrier()
+    barrier(dist)
     torch.cuda.synchronize(dev)
     with ClockSampler(bus_id=bus) as clk:
         t_start.record(stream)
@@ -283,15 +307,11 @@ def run_ours(args, w, rank, world, dist):
             step(evs[i])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
-    if dist is not None:
-        dist.barrier()
+    barrier(dist)
     elapsed_ms = t_start.elapsed_time(t_end)
     if fa.last_device_error(dev) != 0:
         raise RuntimeError("device error during the timed region")
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, = max_over_ranks([elapsed_ms], dist, dev)
 
     # Distribution of the per-step device time (first kernel start to last
     # kernel end of each timed step).
@@ -311,7 +331,7 @@ def run_ours(args, w, rank, world, dist):
     F_bwd = flops(w, "bwd") if has_bwd else 0
     F_step = F_fwd + F_bwd
     ms_per_step = elapsed_ms / args.steps
-    value = F_step * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_rate(F_step, world, ms_per_step) / 1e12
     peaks, peak_kind = load_peaks()
 
     # Dominant kernel: the one with the largest share of the step. Its
@@ -366,11 +386,8 @@ def run_ours(args, w, rank, world, dist):
     if fa.last_device_error(dev) != 0:
         raise RuntimeError("device error during the end-to-end steps")
     e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = F_step * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms, = max_over_ranks([e2e_ms], dist, dev)
+    e2e_value = whole_job_rate(F_step, world, e2e_ms) / 1e12
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -439,8 +456,7 @@ def run_softmax(args, rw, rank, world, dist):
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
     except Exception:
         pass
-    if dist is not None:
-        dist.barrier()
+    barrier(dist)
     ms = {}
     with ClockSampler(bus_id=bus) as clk:
         for name, fn in fns.items():
@@ -451,10 +467,9 @@ def run_softmax(args, rw, rank, world, dist):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             ms[name] = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms["online"], ms["safe"]], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = {"online": float(t[0]), "safe": float(t[1])}
+    barrier(dist)
+    m_on, m_safe = max_over_ranks([ms["online"], ms["safe"]], dist, dev)
+    ms = {"online": m_on, "safe": m_safe}
     alg_bytes = 8 * rw.rows * rw.n
     gbs = {k: alg_bytes / (v * 1e-3) / 1e9 for k, v in ms.items()}
     peaks, peak_kind = load_peaks()
@@ -471,7 +486,7 @@ def run_softmax(args, rw, rank, world, dist):
         y_host.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms, = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], dist, dev)
     res = {
         "metric": SOFTMAX_METRIC, "value": gbs["online"] * world, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms["online"],
@@ -563,8 +578,7 @@ def run_decode(args, dw, rank, world, dist):
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
     except Exception:
         pass
-    if dist is not None:
-        dist.barrier()
+    barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(bus_id=bus) as clk:
         e0.record(stream)
@@ -575,10 +589,8 @@ def run_decode(args, dw, rank, world, dist):
     ms = e0.elapsed_time(e1) / args.steps
     if fa.last_device_error(dev) != 0:
         raise RuntimeError("device error during the timed region")
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    barrier(dist)
+    ms, = max_over_ranks([ms], dist, dev)
     tokens = int(lens.sum().item())
     kv_bytes = tokens * dw.Hkv * dw.d * 2 * 2
     gbs = kv_bytes / (ms * 1e-3) / 1e9
@@ -599,7 +611,7 @@ def run_decode(args, dw, rank, world, dist):
         hlse.copy_(lse, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms, = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, ht, hl))
     d2h = ho.numel() * ho.element_size() + hlse.numel() * hlse.element_size()
     res = {
