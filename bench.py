@@ -402,7 +402,7 @@ def run_ours(args, w, rank, world, dist):
                          "nominal_2250": value / world / 2250.0},
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "host_chunks": args.host_chunks or "library default (8)"},
+                "ms_per_step": e2e_ms, "host_chunks": args.host_chunks or "library default"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
     }
@@ -653,7 +653,7 @@ def main():
     ap.add_argument("--workload", default="c4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-chunks", type=int, default=0,
-                    help="slices of the end-to-end host pipeline (0: the library default)")
+                    help="slices of the end-to-end host pipeline (0: the library's choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -225,9 +225,19 @@ int check_common(const fa_tensors* host, const fa_tensors* dev, bool with_bwd, i
   return FA_OK;
 }
 
-int chunks_or_default(int n_chunks) {
-  if (n_chunks == 0) return kDefaultChunks;
-  return n_chunks > kMaxChunks ? kMaxChunks : n_chunks;
+// Slices when the caller leaves the choice (n_chunks = 0): up to 8, but no
+// more than keep every slice's dK/dV sweep (one CTA per K/V head and
+// 128-key tile) at two or more CTAs per SM. Smaller slices leave SMs idle;
+// their kernels lose more than the finer pipeline gains.
+int chunks_or_default(int n_chunks, int B, int Hkv, int N) {
+  if (n_chunks > 0) return n_chunks > kMaxChunks ? kMaxChunks : n_chunks;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return kDefaultChunks;
+  const long long ctas = static_cast<long long>(B) * Hkv * ((N + 127) / 128);
+  const long long c = ctas / (2LL * sms);
+  return static_cast<int>(c < 1 ? 1 : (c > kDefaultChunks ? kDefaultChunks : c));
 }
 
 }  // namespace
@@ -239,7 +249,7 @@ int fa_fwd_host(const fa_tensors* host, const fa_tensors* dev, int B, int H, int
   const int st = check_common(host, dev, false, B, H, Hkv, N, d, scale, n_chunks);
   if (st != FA_OK) return st;
   const cudaError_t e = run_pipeline(*host, *dev, nullptr, false, B, H, Hkv, N, d, scale, causal != 0,
-                                     chunks_or_default(n_chunks), static_cast<cudaStream_t>(stream));
+                                     chunks_or_default(n_chunks, B, Hkv, N), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -250,7 +260,7 @@ int fa_fwd_bwd_host(const fa_tensors* host, const fa_tensors* dev, void* workspa
   if (!workspace || ws_bytes < static_cast<size_t>(B) * H * N * sizeof(float)) return FA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
   const cudaError_t e = run_pipeline(*host, *dev, static_cast<float*>(workspace), true, B, H, Hkv, N, d,
-                                     scale, causal != 0, chunks_or_default(n_chunks),
+                                     scale, causal != 0, chunks_or_default(n_chunks, B, Hkv, N),
                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -165,8 +165,10 @@ typedef struct {
  * of the device calls, bit for bit, and are also left in `dev`.
  *
  * The (batch, K/V head) pairs are independent problems, so the work is cut
- * into n_chunks slices of consecutive pairs (0 = 8; more than B·Hkv or 64
- * is clamped), and each slice's copies overlap other slices' kernels: its
+ * into n_chunks slices of consecutive pairs (more than B·Hkv or 64 is
+ * clamped; 0 lets the library choose: up to 8, as long as each slice's
+ * dK/dV sweep keeps two CTAs per SM), and each slice's copies overlap
+ * other slices' kernels: its
  * inputs go in on a copy-in stream, its kernels run on `stream`, its
  * outputs come out on a copy-out stream as soon as they are ready. Host
  * buffers should be page-locked (cudaHostAlloc / cudaHostRegister), else
