@@ -167,7 +167,7 @@ typedef struct {
  * The (batch, K/V head) pairs are independent problems, so the work is cut
  * into n_chunks slices of consecutive pairs (more than B·Hkv or 64 is
  * clamped; 0 lets the library choose: up to 8, as long as each slice's
- * dK/dV sweep keeps two CTAs per SM), and each slice's copies overlap
+ * dK/dV sweep keeps 1.5 CTAs per SM), and each slice's copies overlap
  * other slices' kernels: its
  * inputs go in on a copy-in stream, its kernels run on `stream`, its
  * outputs come out on a copy-out stream as soon as they are ready. Host
