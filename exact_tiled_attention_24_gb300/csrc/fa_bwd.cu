@@ -355,11 +355,13 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     const bool key_ok = key < N;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr float LOG2E = 1.4426950408889634f;
-    // Per-tile (lse·log2 e, D) of the 128 queries, double-buffered in shared
+    // Per-tile (−lse·log2 e, −D) of the 128 queries, double-buffered in shared
     // memory: compute thread ct fills entry ct % 128 of lse (ct < 128) or of
     // D. A value is loaded one tile before it is stored, and only the store
     // reads the loaded register, so no warp waits on the load.
-    const float stat_mul = ct < 128 ? LOG2E : 1.f;
+    // Stored negated (−lse·log2 e, −D) so that the packed pair arithmetic
+    // below adds them; the products are the same as subtracting.
+    const float stat_mul = ct < 128 ? -LOG2E : -1.f;
     auto load_stat = [&](int tile) -> float {
       if (tile >= n_it) return ct < 128 ? INFINITY : 0.f;
       const int gq = tile / n_q;
@@ -389,13 +391,18 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         uint32_t raw[64];
         tmem_ld64(s_addr, raw);
         tmem_ld_wait();
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + c);
-          p[c + 0] = ex2(fmaf(__uint_as_float(raw[c + 0]), scale_log2, -l4.x));
-          p[c + 1] = ex2(fmaf(__uint_as_float(raw[c + 1]), scale_log2, -l4.y));
-          p[c + 2] = ex2(fmaf(__uint_as_float(raw[c + 2]), scale_log2, -l4.z));
-          p[c + 3] = ex2(fmaf(__uint_as_float(raw[c + 3]), scale_log2, -l4.w));
+          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + c);  // −lse·log2 e
+          const float2 e01 = ffma2(make_float2(__uint_as_float(raw[c + 0]), __uint_as_float(raw[c + 1])), sc2,
+                                   make_float2(l4.x, l4.y));
+          const float2 e23 = ffma2(make_float2(__uint_as_float(raw[c + 2]), __uint_as_float(raw[c + 3])), sc2,
+                                   make_float2(l4.z, l4.w));
+          p[c + 0] = ex2(e01.x);
+          p[c + 1] = ex2(e01.y);
+          p[c + 2] = ex2(e23.x);
+          p[c + 3] = ex2(e23.y);
         }
       }
 #pragma unroll
@@ -427,12 +434,17 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(s_D + 32 * h2 + c);
+            const float4 d4 = *reinterpret_cast<const float4*>(s_D + 32 * h2 + c);  // −D
             const float* pp = p + 32 * h2 + c;
             const uint32_t* rr = raw + 32 * h2 + c;
-            pk[c / 2] = pack_bf16x2(pp[0] * (__uint_as_float(rr[0]) - d4.x), pp[1] * (__uint_as_float(rr[1]) - d4.y));
-            pk[c / 2 + 1] =
-                pack_bf16x2(pp[2] * (__uint_as_float(rr[2]) - d4.z), pp[3] * (__uint_as_float(rr[3]) - d4.w));
+            const float2 ds01 = fmul2(make_float2(pp[0], pp[1]),
+                                      fadd2(make_float2(__uint_as_float(rr[0]), __uint_as_float(rr[1])),
+                                            make_float2(d4.x, d4.y)));
+            const float2 ds23 = fmul2(make_float2(pp[2], pp[3]),
+                                      fadd2(make_float2(__uint_as_float(rr[2]), __uint_as_float(rr[3])),
+                                            make_float2(d4.z, d4.w)));
+            pk[c / 2] = pack_bf16x2(ds01.x, ds01.y);
+            pk[c / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
           }
           tmem_st16(dp_addr + 16 * h2, pk);
         }
@@ -717,8 +729,13 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          p[32 * h2 + c] = ex2(fmaf(__uint_as_float(raw_s[32 * h2 + c]), scale_log2, -lse2));
+        for (int c = 0; c < 32; c += 2) {
+          const float2 e = ffma2(make_float2(__uint_as_float(raw_s[32 * h2 + c]),
+                                             __uint_as_float(raw_s[32 * h2 + c + 1])),
+                                 make_float2(scale_log2, scale_log2), make_float2(-lse2, -lse2));
+          p[32 * h2 + c] = ex2(e.x);
+          p[32 * h2 + c + 1] = ex2(e.y);
+        }
         if (masked) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
@@ -740,7 +757,10 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         for (int t2 = 0; t2 < 16; ++t2) {
           const float* pp = p + 32 * h2 + 2 * t2;
           const uint32_t* rr = raw + 32 * h2 + 2 * t2;
-          pk[t2] = pack_bf16x2(pp[0] * (__uint_as_float(rr[0]) - Dq), pp[1] * (__uint_as_float(rr[1]) - Dq));
+          const float2 ds = fmul2(make_float2(pp[0], pp[1]),
+                                  fadd2(make_float2(__uint_as_float(rr[0]), __uint_as_float(rr[1])),
+                                        make_float2(-Dq, -Dq)));
+          pk[t2] = pack_bf16x2(ds.x, ds.y);
         }
         tmem_st16(dp_addr + 16 * h2, pk);
       }

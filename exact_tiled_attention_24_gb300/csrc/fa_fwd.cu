@@ -309,16 +309,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       // Eight independent max chains (short dependency chains: the softmax
-      // warps have little else to hide latency with).
+      // warps have little else to hide latency with), two new scores per
+      // three-input max.
       float mx[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = x[u];
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(x[u], x[8 + u]);
 #pragma unroll
-      for (int c = 8; c < BN; c += 8)
+      for (int c = 16; c < BN; c += 16)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], x[c + u]);
-      const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * scale_log2;
+        for (int u = 0; u < 8; ++u) mx[u] = fmax3(mx[u], x[c + u], x[c + 8 + u]);
+      const float tile_max = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                   fmaxf(mx[6], mx[7])) * scale_log2;
       // Raise the reference when the max outgrew it by more than the
       // threshold (always on the first tile, where m = -inf).
       const bool warp_raise = __any_sync(0xffffffffu, tile_max > m + RESCALE_LOG2);
@@ -350,18 +351,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st16(o_addr + c + 16, bb);
         }
       }
-      float sum[8];
+      // Pairs of scores through packed fp32 arithmetic: the scale-and-shift
+      // and the running sums take one instruction per two scores. Four
+      // packed sums = eight independent chains.
+      float2 sum[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sum[u] = 0.f;
+      for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m, -m);
 #pragma unroll
       for (int c = 0; c < BN; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int t2 = 0; t2 < 16; ++t2) {
-          const float p0 = ex2(fmaf(x[c + 2 * t2], scale_log2, -m));
-          const float p1 = ex2(fmaf(x[c + 2 * t2 + 1], scale_log2, -m));
-          sum[(2 * t2) & 7] += p0;
-          sum[(2 * t2 + 1) & 7] += p1;
+          const float2 e = ffma2(make_float2(x[c + 2 * t2], x[c + 2 * t2 + 1]), sc2, nm2);
+          const float p0 = ex2(e.x);
+          const float p1 = ex2(e.y);
+          sum[t2 & 3] = fadd2(sum[t2 & 3], make_float2(p0, p1));
           pk[t2] = pack_bf16x2(p0, p1);
         }
         tmem_st16(s_addr + c / 2, pk);  // P (bf16) into the first 64 S columns
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0) mbar_arrive(c + 32 == BN ? &p_hi[g] : &p_ready[g]);
         }
       }
-      l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+      l += ((sum[0].x + sum[0].y) + (sum[1].x + sum[1].y)) + ((sum[2].x + sum[2].y) + (sum[3].x + sum[3].y));
     }
     // -------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&pv_done[g], (n_mine - 1) & 1, err);
