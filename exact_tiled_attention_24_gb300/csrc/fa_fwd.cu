@@ -308,9 +308,43 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (key >= N || (CAUSAL && key > qrow)) x[c] = -INFINITY;
         }
       }
-      // Eight independent max chains (short dependency chains: the softmax
-      // warps have little else to hide latency with), two new scores per
-      // three-input max.
+      // P for 32 columns from c on, relative to the reference -nm.x; bf16
+      // into the S columns (P_j is read by the P·V product only after its
+      // release), the fp32 values into the running sums. Packed fp32 pairs:
+      // the scale-and-shift and the sums take one instruction per two
+      // scores; four packed sums = eight independent chains.
+      float2 sum[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      auto p_chunk = [&](int c, float2 nm2) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2) {
+          const float2 e = ffma2(make_float2(x[c + 2 * t2], x[c + 2 * t2 + 1]), sc2, nm2);
+          const float p0 = ex2(e.x);
+          const float p1 = ex2(e.y);
+          sum[t2 & 3] = fadd2(sum[t2 & 3], make_float2(p0, p1));
+          pk[t2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + c / 2, pk);  // P (bf16) into the first 64 S columns
+      };
+      auto release = [&](uint64_t* bar) {  // this half of P is in TMEM
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+      };
+      // The first half of P is formed against the current reference before
+      // the tile maximum is known (the maximum is computed alongside); it
+      // stands unless the maximum outgrew the reference by more than the
+      // threshold, which is rare after the first tile. The first tile has
+      // no reference yet.
+      if (j > 0) {
+        p_chunk(0, make_float2(-m, -m));
+        p_chunk(32, make_float2(-m, -m));
+      }
+      // Eight independent max chains, two new scores per three-input max.
       float mx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx[u] = fmaxf(x[u], x[8 + u]);
@@ -323,60 +357,42 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Raise the reference when the max outgrew it by more than the
       // threshold (always on the first tile, where m = -inf).
       const bool warp_raise = __any_sync(0xffffffffu, tile_max > m + RESCALE_LOG2);
-      float alpha = 1.f;
       if (warp_raise) {
         const float m_new = fmaxf(m, tile_max);
-        alpha = ex2(m - m_new);  // 0 on the first tile
+        const float alpha = ex2(m - m_new);  // 0 on the first tile
         m = m_new;
         l *= alpha;
-      }
-      // O *= alpha once P V_{j-1} has landed (only when this warp raised);
-      // before any of P_j is released, since P V_j accumulates into O.
-      if (warp_raise && j > 0) {
-        ok = mbar_wait(&pv_done[g], (j - 1) & 1, err);
-        if (!ok) break;
-        tc_fence_after();
+        // O *= alpha once P V_{j-1} has landed, before any of P_j is
+        // released, since P V_j accumulates into O.
+        if (j > 0) {
+          ok = mbar_wait(&pv_done[g], (j - 1) & 1, err);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + c, o);
-          tmem_ld_wait();
-          uint32_t a[16], bb[16];
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + c, o);
+            tmem_ld_wait();
+            uint32_t a[16], bb[16];
 #pragma unroll
-          for (int t2 = 0; t2 < 16; ++t2) {
-            a[t2] = __float_as_uint(__uint_as_float(o[t2]) * alpha);
-            bb[t2] = __float_as_uint(__uint_as_float(o[16 + t2]) * alpha);
+            for (int t2 = 0; t2 < 16; ++t2) {
+              a[t2] = __float_as_uint(__uint_as_float(o[t2]) * alpha);
+              bb[t2] = __float_as_uint(__uint_as_float(o[16 + t2]) * alpha);
+            }
+            tmem_st16(o_addr + c, a);
+            tmem_st16(o_addr + c + 16, bb);
           }
-          tmem_st16(o_addr + c, a);
-          tmem_st16(o_addr + c + 16, bb);
         }
+        // The first half again, against the new reference.
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
+        p_chunk(0, make_float2(-m, -m));
+        p_chunk(32, make_float2(-m, -m));
       }
-      // Pairs of scores through packed fp32 arithmetic: the scale-and-shift
-      // and the running sums take one instruction per two scores. Four
-      // packed sums = eight independent chains.
-      float2 sum[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
-      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m, -m);
-#pragma unroll
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t2 = 0; t2 < 16; ++t2) {
-          const float2 e = ffma2(make_float2(x[c + 2 * t2], x[c + 2 * t2 + 1]), sc2, nm2);
-          const float p0 = ex2(e.x);
-          const float p1 = ex2(e.y);
-          sum[t2 & 3] = fadd2(sum[t2 & 3], make_float2(p0, p1));
-          pk[t2] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(s_addr + c / 2, pk);  // P (bf16) into the first 64 S columns
-        if (c + 32 == BN / 2 || c + 32 == BN) {  // a half of P is in TMEM: release it
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(c + 32 == BN ? &p_hi[g] : &p_ready[g]);
-        }
-      }
+      release(&p_ready[g]);
+      p_chunk(64, make_float2(-m, -m));
+      p_chunk(96, make_float2(-m, -m));
+      release(&p_hi[g]);
       l += ((sum[0].x + sum[0].y) + (sum[1].x + sum[1].y)) + ((sum[2].x + sum[2].y) + (sum[3].x + sum[3].y));
     }
     // -------------------------------------------------------------- epilogue
