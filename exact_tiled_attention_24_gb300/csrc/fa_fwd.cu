@@ -13,7 +13,8 @@
 // key/value tiles once for both ("ping-pong"): while one softmax group
 // exponentiates its S tile, the tensor core runs the other group's products.
 // Roles (320 threads):
-//   warp 0      TMA producer: Q0, Q1 once, then K_j and V_j into 2-stage rings
+//   warp 0      TMA producer: Q0, Q1 and K_0 once, then V_j with K_{j+1}
+//               into 2-stage rings (one full and one empty barrier per pair)
 //   warp 1      TMEM owner and MMA issuer (warp-uniform, one elected lane issues)
 //   warps 2..5  softmax group 0 (Q0), one thread per query row (TMEM lane)
 //   warps 6..9  softmax group 1 (Q1)
@@ -60,9 +61,9 @@ struct Smem {
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  // p_ready[2] (keys 0..63 of P), pv_done[2], final, p_hi[2] (keys 64..127)
-  static constexpr int NBARS = 1 + 4 * STAGES + 6 + 1 + 2;
+  // q_full, k0_full, kv_full[2], kv_empty[2], s_full[2], p_ready[2] (keys
+  // 0..63 of P), pv_done[2], final, p_hi[2] (keys 64..127)
+  static constexpr int NBARS = 2 + 2 * STAGES + 6 + 1 + 2;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   // Slack for 1024-byte alignment; at least 116 KB so that only one CTA
@@ -83,12 +84,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  // Step j of the sweep reads V_j and K_{j+1} (for S_{j+1}); the two are
+  // loaded together and released together, so one full and one empty
+  // barrier per slot serve both rings: slot j % 2 holds V_j in V stage
+  // j % 2 and K_{j+1} in K stage (j + 1) % 2. K_0 has its own barrier.
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + L::STAGES;
-  uint64_t* v_full = k_empty + L::STAGES;
-  uint64_t* v_empty = v_full + L::STAGES;
-  uint64_t* s_full = v_empty + L::STAGES;   // [2], one per group
+  uint64_t* k0_full = bars + 1;
+  uint64_t* kv_full = bars + 2;                // [2]
+  uint64_t* kv_empty = kv_full + L::STAGES;    // [2]
+  uint64_t* s_full = kv_empty + L::STAGES;     // [2], one per group
   uint64_t* p_ready = s_full + 2;           // [2]
   uint64_t* pv_done = p_ready + 2;          // [2]
   uint64_t* final_bar = pv_done + 2;
@@ -114,11 +118,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(k0_full, 1);
     for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&s_full[g], 1);
@@ -149,43 +152,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int g = 0; g < 2; ++g)
         for (int p = 0; p < L::PANELS; ++p)
           tma_load_3d(sQ + g * L::TILE_BYTES + p * L::PANEL, &tq, q_full, p * 64, qrow0 + g * BM, bh);
-      // K_j is read only by the S products and its stage is released right
-      // after them; V_j is released after the P·V products. K loads therefore
-      // run ahead of V loads.
-      int k_issued = 0, v_issued = 0;
+      mbar_arrive_expect_tx(k0_full, L::TILE_BYTES);
+      for (int p = 0; p < L::PANELS; ++p)
+        tma_load_3d(sK + p * L::PANEL, &tk, k0_full, p * 64, 0, bkv);
+      // Slot j: V_j and K_{j+1}, issued once step j - 2 (the prologue for
+      // j = 1, whose S_0 read K_0) has released their stages.
+      int issued = 0;
       for (int j = 0; j < n_kt; ++j) {
-        const int s = j % L::STAGES;
-        const uint32_t ph = ((j / L::STAGES) & 1) ^ 1;
-        if (!mbar_wait(&k_empty[s], ph, err)) break;
-        mbar_arrive_expect_tx(&k_full[s], L::TILE_BYTES);
+        const int sv = j % L::STAGES, sk = (j + 1) % L::STAGES;
+        const bool has_k = j + 1 < n_kt;
+        if (j >= 1 && !mbar_wait(&kv_empty[sv], ((j - 1) / 2) & 1, err)) break;
+        mbar_arrive_expect_tx(&kv_full[sv], L::TILE_BYTES * (has_k ? 2 : 1));
         for (int p = 0; p < L::PANELS; ++p)
-          tma_load_3d(sK + s * L::TILE_BYTES + p * L::PANEL, &tk, &k_full[s], p * 64, j * BN, bkv);
-        k_issued = j + 1;
-        // V_{j-1} after K_j: V is needed one softmax later than K.
-        if (j >= 1) {
-          const int jv = j - 1, sv = jv % L::STAGES;
-          if (!mbar_wait(&v_empty[sv], ((jv / L::STAGES) & 1) ^ 1, err)) break;
-          mbar_arrive_expect_tx(&v_full[sv], L::TILE_BYTES);
+          tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &kv_full[sv], p * 64, j * BN, bkv);
+        if (has_k)
           for (int p = 0; p < L::PANELS; ++p)
-            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bkv);
-          v_issued = jv + 1;
-        }
-      }
-      if (v_issued == n_kt - 1 && k_issued == n_kt) {
-        const int jv = n_kt - 1, sv = jv % L::STAGES;
-        if (mbar_wait(&v_empty[sv], ((jv / L::STAGES) & 1) ^ 1, err)) {
-          mbar_arrive_expect_tx(&v_full[sv], L::TILE_BYTES);
-          for (int p = 0; p < L::PANELS; ++p)
-            tma_load_3d(sV + sv * L::TILE_BYTES + p * L::PANEL, &tv, &v_full[sv], p * 64, jv * BN, bkv);
-          v_issued = n_kt;
-        }
+            tma_load_3d(sK + sk * L::TILE_BYTES + p * L::PANEL, &tk, &kv_full[sv], p * 64, (j + 1) * BN, bkv);
+        issued = j + 1;
       }
       // Drain: never leave the CTA with copies still landing in its smem.
       mbar_wait(q_full, 0, err);
-      for (int j = max(0, k_issued - L::STAGES); j < k_issued; ++j)
-        mbar_wait(&k_full[j % L::STAGES], (j / L::STAGES) & 1, err);
-      for (int j = max(0, v_issued - L::STAGES); j < v_issued; ++j)
-        mbar_wait(&v_full[j % L::STAGES], (j / L::STAGES) & 1, err);
+      mbar_wait(k0_full, 0, err);
+      for (int j = max(0, issued - L::STAGES); j < issued; ++j)
+        mbar_wait(&kv_full[j % L::STAGES], (j / L::STAGES) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -234,21 +223,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (elect_one()) tc_commit(bar);
       __syncwarp();
     };
-    bool ok = mbar_wait_warp(q_full, 0, err) && mbar_wait_warp(&k_full[0], 0, err);
+    bool ok = mbar_wait_warp(q_full, 0, err) && mbar_wait_warp(k0_full, 0, err);
     if (ok) {
       tc_fence_after();
       issue_s(0, 0);
       issue_s(1, 0);
-      commit(&k_empty[0]);
+      commit(&kv_empty[1]);  // K_0 read: slot 1 (V_1, K_2) may load
     }
     for (int j = 0; j < n_kt && ok; ++j) {
       const int s = j % L::STAGES;
       const int s1 = (j + 1) % L::STAGES;
-      // The data waits (V_j, K_{j+1}) come first: they are normally met and
-      // overlap the wait for P_j, so no wait sits between two products.
-      const bool next_ready = j + 1 < n_kt;
-      ok = mbar_wait_warp(&v_full[s], (j / L::STAGES) & 1, err);
-      if (ok && next_ready) ok = mbar_wait_warp(&k_full[s1], ((j + 1) / L::STAGES) & 1, err);
+      // The data wait (V_j and K_{j+1}) comes first: it is normally met and
+      // overlaps the wait for P_j, so no wait sits between two products.
+      ok = mbar_wait_warp(&kv_full[s], (j / L::STAGES) & 1, err);
       if (!ok) break;
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
@@ -268,8 +255,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (j + 1 < n_g) issue_s(g, s1);
       }
       if (!ok) break;
-      commit(&v_empty[s]);                 // V_j: read by PV_j
-      if (next_ready) commit(&k_empty[s1]);  // K_{j+1}: read by S_{j+1}
+      commit(&kv_empty[s]);  // V_j read by PV_j, K_{j+1} by S_{j+1}
     }
     commit(final_bar);
     mbar_wait_warp(final_bar, 0, err);
