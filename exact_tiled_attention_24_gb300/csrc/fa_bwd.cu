@@ -502,9 +502,9 @@ struct DqSmem {
   static constexpr int K_OFF = DO_OFF + T::BYTES;  // K of stages 0, 1
   static constexpr int V_OFF = K_OFF + 2 * T::BYTES;  // V of stages 0, 1
   static constexpr int BAR_OFF = V_OFF + 2 * T::BYTES;
-  // q_full, kv_full[KST], kv_empty[KST], a_ready, s_full, s_free, dp_full,
-  // ds_ready, final
-  static constexpr int NBARS = 1 + 2 * KST + 6;
+  // q_full, s_go[KST], kv_empty[KST], a_ready, s_full, dp_full, ds_ready,
+  // final
+  static constexpr int NBARS = 1 + 2 * KST + 5;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   static constexpr int ALLOC = alloc_for(BYTES);
@@ -529,13 +529,16 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   auto kst = [&](int st) { return st < 2 ? smem + L::K_OFF + st * T::BYTES : sQ; };
   auto vst = [&](int st) { return st < 2 ? smem + L::V_OFF + st * T::BYTES : sdO; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  // s_go[j % KST]: the two things S_j waits for, in one barrier — K_j and
+  // V_j have landed (the producer's byte-counted arrival) and the compute
+  // warps hold S_{j-1} in registers, so S_j may overwrite its columns
+  // (their 8 arrivals; for j = 0, made once Q and dO are in TMEM).
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;       // K_j and V_j of one stage
-  uint64_t* kv_empty = kv_full + KST;
+  uint64_t* s_go = bars + 1;
+  uint64_t* kv_empty = s_go + KST;
   uint64_t* a_ready = kv_empty + KST;  // Q and dO copied into TMEM
   uint64_t* s_full = a_ready + 1;
-  uint64_t* s_free = s_full + 1;  // the compute warps hold S_j in registers
-  uint64_t* dp_full = s_free + 1;
+  uint64_t* dp_full = s_full + 1;
   uint64_t* ds_ready = dp_full + 1;
   uint64_t* final_bar = ds_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
@@ -553,12 +556,11 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < KST; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&s_go[s], 1 + 8);
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(a_ready, 8);
     mbar_init(s_full, 1);
-    mbar_init(s_free, 8);
     mbar_init(dp_full, 1);
     mbar_init(ds_ready, 8);
     mbar_init(final_bar, 1);
@@ -592,18 +594,18 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         if (!mbar_wait(&kv_empty[s], ((j / KST) & 1) ^ 1, err)) break;
         // Stage 2 overlays Q and dO: first use waits for their copy to TMEM.
         if (j == 2 && !mbar_wait(a_ready, 0, err)) break;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * T::BYTES);
+        mbar_arrive_expect_tx(&s_go[s], 2 * T::BYTES);
         uint8_t* kd = kst(s);
         uint8_t* vd = vst(s);
         for (int p = 0; p < T::PANELS; ++p) {
-          tma_load_3d(kd + p * T::PANEL, &tk, &kv_full[s], p * 64, j * TILE, bkv);
-          tma_load_3d(vd + p * T::PANEL, &tv, &kv_full[s], p * 64, j * TILE, bkv);
+          tma_load_3d(kd + p * T::PANEL, &tk, &s_go[s], p * 64, j * TILE, bkv);
+          tma_load_3d(vd + p * T::PANEL, &tv, &s_go[s], p * 64, j * TILE, bkv);
         }
         issued = j + 1;
       }
       mbar_wait(q_full, 0, err);
       for (int j = max(0, issued - KST); j < issued; ++j)
-        mbar_wait(&kv_full[j % KST], (j / KST) & 1, err);
+        mbar_wait(&s_go[j % KST], (j / KST) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       }
       __syncwarp();
     };
-    bool ok = mbar_wait_warp(a_ready, 0, err) && mbar_wait_warp(&kv_full[0], 0, err);
+    bool ok = mbar_wait_warp(&s_go[0], 0, err);  // K_0, V_0 landed; Q, dO in TMEM
     if (ok) {
       tc_fence_after();
       issue_ab(Q_COL_Q, dKk0, Q_COL_S, s_full);
@@ -644,13 +646,11 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       const int s1 = (j + 1) % KST;
       const bool more = j + 1 < n_kv;
       if (more) {
-        ok = mbar_wait_warp(&kv_full[s1], ((j + 1) / KST) & 1, err);
+        ok = mbar_wait_warp(&s_go[s1], ((j + 1) / KST) & 1, err);
         if (!ok) break;
+        tc_fence_after();
+        issue_ab(Q_COL_Q, sel(s1, dKk0, dKk1, dKk2), Q_COL_S, s_full);
       }
-      ok = mbar_wait_warp(s_free, j & 1, err);
-      if (!ok) break;
-      tc_fence_after();
-      if (more) issue_ab(Q_COL_Q, sel(s1, dKk0, dKk1, dKk2), Q_COL_S, s_full);
       ok = mbar_wait_warp(ds_ready, j & 1, err);
       if (!ok) break;
       tc_fence_after();
@@ -709,7 +709,10 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       tc_fence_before();
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(a_ready);
+    if (lane == 0) {
+      mbar_arrive(a_ready);
+      mbar_arrive(&s_go[0]);
+    }
     for (int j = 0; j < n_kv && ok; ++j) {
       const int kb0 = j * TILE + half * 64;  // first key of this warp's half
       ok = mbar_wait(s_full, j & 1, err);
@@ -725,7 +728,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       // S_j is in registers: the next S may overwrite its columns.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
+      if (lane == 0) mbar_arrive(&s_go[(j + 1) % KST]);
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
