@@ -112,3 +112,26 @@ def test_host_call_is_ordered_on_the_stream(fa):
     torch.cuda.synchronize()
     assert torch.equal(o2, o)
     assert torch.equal(host["o"], o.cpu())
+
+
+def test_fwd_bwd_host_with_pageable_memory(fa):
+    """Host buffers that are not page-locked: the copies are staged by the
+    driver (no overlap) but the results are the same."""
+    B, H, Hkv, N, d = 1, 4, 2, 257, 64
+    q, k, v, do = make_inputs(B, H, N, d, seed=808, Hkv=Hkv)
+    host = {"q": q.clone(), "k": k.clone(), "v": v.clone(), "dO": do.clone()}
+    for n, shp, dt in (("o", (B, H, N, d), torch.bfloat16), ("lse", (B, H, N), torch.float32),
+                       ("dq", (B, H, N, d), torch.bfloat16), ("dk", (B, Hkv, N, d), torch.bfloat16),
+                       ("dv", (B, Hkv, N, d), torch.bfloat16)):
+        host[n] = torch.full(shp, float("nan"), dtype=dt)
+    assert not host["q"].is_pinned() and not host["o"].is_pinned()
+    dev = dev_bufs(q, k, True)
+    ws = torch.empty(fa.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    fa.fwd_bwd_host(host, dev, ws, causal=True, n_chunks=2)
+    torch.cuda.synchronize()
+    qg, kg, vg, dog = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qg, kg, vg, causal=True)
+    dq, dk, dv = fa.bwd(qg, kg, vg, o, lse, dog, causal=True)
+    torch.cuda.synchronize()
+    for name, ref in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.equal(host[name], ref.cpu()), name
