@@ -163,22 +163,26 @@ class ClockSampler:
 
 # -------------------------------------------------------------- oracle leg
 
-def oracle_sample(w, q, k, v, do, heads):
-    """Time the fp64 oracle's forward + backward on the given heads.
+def oracle_sample(w, q, k, v, do, heads, n=None):
+    """Time the fp64 oracle's forward + backward on the given heads, each
+    restricted to its first n queries and keys (all N when n is None: a
+    prefix of a head is itself a complete attention problem of length n).
     Returns (seconds, algorithmic FLOPs of the sample)."""
     from exact_tiled_attention_24_gb300.workloads import to_f64
     from oracle import attention_bwd_head, attention_fwd_head
     causal = True in w.causal
+    n = w.N if n is None else n
     t0 = time.perf_counter()
     for (b, h) in heads:
         hk = h // (w.H // w.kv_heads)  # the K/V head query head h reads
-        qq, dd = to_f64(q[b, h]), (to_f64(do[b, h]) if do is not None else None)
-        kk, vv = to_f64(k[b, hk]), to_f64(v[b, hk])
+        qq, dd = to_f64(q[b, h, :n]), (to_f64(do[b, h, :n]) if do is not None else None)
+        kk, vv = to_f64(k[b, hk, :n]), to_f64(v[b, hk, :n])
         attention_fwd_head(qq, kk, vv, w.scale, causal)
         if do is not None:
             attention_bwd_head(qq, kk, vv, dd, w.scale, causal)
     dt = time.perf_counter() - t0
-    per_head = (flops(w, "fwd") + (flops(w, "bwd") if do is not None else 0)) // (w.B * w.H)
+    pairs = n * (n + 1) // 2 if causal else n * n
+    per_head = (4 * w.d + (10 * w.d if do is not None else 0)) * pairs
     return dt, per_head * len(heads)
 
 
@@ -189,14 +193,21 @@ def run_reference(args, w, rank):
     q, k, v, *rest = workload_inputs(args.workload, with_do=True)
     do = rest[0] if rest else None
     heads = [(0, 0)]
-    oracle_sample(w, q, k, v, do, heads)  # one untimed call (BLAS thread start-up)
+    # One head per step for up to 30 steps; beyond that, each step takes the
+    # head's first n queries and keys with n shrunk so that the whole run
+    # costs about as much as 30 full-head steps (the rate is per FLOP).
+    n = w.N if args.steps <= 30 else max(128, int(w.N * (30 / args.steps) ** 0.5) // 128 * 128)
+    n = min(n, w.N)
+    oracle_sample(w, q, k, v, do, heads, n)  # one untimed call (BLAS thread start-up)
     times, fl = [], 0
     for _ in range(args.steps):
-        dt, fl = oracle_sample(w, q, k, v, do, heads)
+        dt, fl = oracle_sample(w, q, k, v, do, heads, n)
         times.append(dt)
     total = sum(times)
     value = fl * args.steps / total / 1e12
-    sample = f"one head (b=0,h=0) of {args.workload} forward+backward per step, fp64 NumPy oracle"
+    part = "" if n == w.N else f" (its first {n} queries and keys)"
+    sample = (f"one head (b=0,h=0){part} of {args.workload} forward"
+              f"{'+backward' if do is not None else ''} per step, fp64 NumPy oracle")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
