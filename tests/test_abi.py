@@ -205,3 +205,39 @@ def test_host_pipeline_argument_errors(L):
     assert fb_h(ws_bytes=4 * 4 * 16 - 1) == 6
     assert fb_h(ws=MIS) == 3
     assert fb_h(d=80) == 2
+
+
+def test_plain_c_program_compiles_links_and_runs(L, tmp_path):
+    """The header is C99 and libfa.so links into a plain C program; the entry
+    points that need no GPU (version, status names, argument checks) run."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_fa.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "fa.h"
+int main(void) {
+  fa_tensors host, dev;
+  memset(&host, 0, sizeof host);
+  memset(&dev, 0, sizeof dev);
+  if (fa_fwd(NULL, NULL, NULL, NULL, NULL, 1, 1, 16, 64, 0.125f, 0, NULL) != FA_ERR_INVALID_ARG) return 1;
+  if (fa_fwd_host(&host, &dev, 1, 1, 1, 16, 64, 0.125f, 0, 0, NULL) != FA_ERR_INVALID_ARG) return 2;
+  if (fa_bwd_workspace_bytes(2, 3, 5, 64) != 2 * 3 * 5 * sizeof(float)) return 3;
+  if (strcmp(fa_status_string(FA_ERR_WORKSPACE), "FA_ERR_WORKSPACE") != 0) return 4;
+  printf("%s\n", fa_version());
+  return 0;
+}
+''')
+    lib_dir = os.path.dirname(fa.lib_path())
+    exe = tmp_path / "use_fa"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", lib_dir, "-lfa", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert re.match(r"^\d+\.\d+\.\d+$", r.stdout.strip())
