@@ -139,18 +139,6 @@ __device__ __forceinline__ void tma_store_commit() {
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-// Bulk (non-tensor) reduction: global[dst .. dst+bytes) += shared[src ..]
-// element-wise in fp32. Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
-  asm volatile(
-      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
-      "r"(smem_u32(src)), "r"(bytes)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // Make generic-proxy shared-memory writes visible to the async (TMA/MMA) proxy.
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
