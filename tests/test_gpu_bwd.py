@@ -115,3 +115,27 @@ def test_bwd_c4_sampled(fa):
         rq, _ = attention_dq_rows_head(to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h]),
                                        to_f64(do[b, h]), w.scale, True, rows)
         assert_grad(dq[b, h, rows].cpu(), rq, f"dq[{b},{h}]")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_heads_one_ragged_tile(fa, d):
+    """2048 (batch, head) pairs of N = 70 (one ragged tile each), with K/V
+    heads shared by pairs of query heads: head indexing over a large grid."""
+    from oracle import attention_bwd_gqa, attention_fwd_gqa
+    B, H, Hkv, N = 64, 32, 16, 70
+    q, k, v, do = make_inputs(B, H, N, d, seed=2048 + d, Hkv=Hkv)
+    dev = torch.device("cuda")
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    scale = 1.0 / d ** 0.5
+    for causal in (False, True):
+        o, lse = fa.fwd(qg, kg, vg, causal=causal)
+        dq, dk, dv = fa.bwd(qg, kg, vg, o, lse, dog, causal=causal)
+        torch.cuda.synchronize()
+        assert fa.last_device_error() == 0
+        ro, rlse = attention_fwd_gqa(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+        assert_o(o, ro)
+        assert_lse(lse, rlse)
+        rdq, rdk, rdv, _ = attention_bwd_gqa(to_f64(q), to_f64(k), to_f64(v), to_f64(do), scale, causal)
+        assert_grad(dq, rdq, "dq")
+        assert_grad(dk, rdk, "dk")
+        assert_grad(dv, rdv, "dv")
