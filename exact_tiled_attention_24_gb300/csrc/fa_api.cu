@@ -135,9 +135,32 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
   float* Dvec = static_cast<float*>(workspace);
   st = fa_bwd_preprocess(o, dO, Dvec, B, H, N, d, stream);
   if (st != FA_OK) return st;
-  st = fa_bwd_dkdv(q, k, v, dO, lse, Dvec, dk, dv, B, H, Hkv, N, d, scale, causal, stream);
-  if (st != FA_OK) return st;
-  return fa_bwd_dq(q, k, v, dO, lse, Dvec, dq, B, H, Hkv, N, d, scale, causal, stream);
+  // The dQ sweep needs only D: it runs on the library's side stream, forked
+  // from `stream` after the preprocess and joined back at the end, beside
+  // the dK/dV sweep (the two grids then share one tail).
+  cudaStream_t cs = static_cast<cudaStream_t>(stream), side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool forked = fa::side_stream(&side) == cudaSuccess &&
+                cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventRecord(fork, cs) == cudaSuccess && cudaStreamWaitEvent(side, fork, 0) == cudaSuccess;
+  if (!forked) {  // no side stream: the three stages in order on `stream`
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+    st = fa_bwd_dkdv(q, k, v, dO, lse, Dvec, dk, dv, B, H, Hkv, N, d, scale, causal, stream);
+    if (st != FA_OK) return st;
+    return fa_bwd_dq(q, k, v, dO, lse, Dvec, dq, B, H, Hkv, N, d, scale, causal, stream);
+  }
+  const int st_dkdv = fa_bwd_dkdv(q, k, v, dO, lse, Dvec, dk, dv, B, H, Hkv, N, d, scale, causal, stream);
+  const int st_dq = fa_bwd_dq(q, k, v, dO, lse, Dvec, dq, B, H, Hkv, N, d, scale, causal, side);
+  // Join even after a failed launch, so `stream` stays ordered after the side work.
+  cudaError_t ej = cudaEventRecord(join, side);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(cs, join, 0);
+  cudaEventDestroy(fork);
+  cudaEventDestroy(join);
+  if (st_dkdv != FA_OK) return st_dkdv;
+  if (st_dq != FA_OK) return st_dq;
+  return map_cuda(ej);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,

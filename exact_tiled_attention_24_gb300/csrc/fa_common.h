@@ -49,6 +49,10 @@ cudaError_t launch_decode_paged(const void* q, const void* k_cache, const void* 
 cudaError_t launch_attn_merge(const float* o_parts, const float* lse_parts, int S, void* o, float* lse,
                               long long rows, int d, cudaStream_t stream);
 
+// The calling host thread's side stream on the current device (a
+// non-blocking stream the library creates on first use and keeps).
+cudaError_t side_stream(cudaStream_t* out);
+
 // Device error words (one per translation unit): read, then clear.
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream);

@@ -27,13 +27,22 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxChunks = 64;
 constexpr int kDefaultChunks = 8;
 
-// The copy streams of one host thread on one device, created on first use
-// and kept for the thread's lifetime (non-blocking: they never wait on the
-// legacy default stream).
+// The library's own streams for one host thread on one device, created on
+// first use and kept for the thread's lifetime (non-blocking: they never
+// wait on the legacy default stream): copy-in, copy-out, and a side stream
+// for the dQ sweep, which runs beside the dK/dV sweep.
 struct CopyStreams {
   cudaStream_t in = nullptr;
   cudaStream_t out = nullptr;
+  cudaStream_t side = nullptr;
 };
+
+cudaError_t make_stream(cudaStream_t* s) {
+  if (*s != nullptr) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) *s = nullptr;
+  return e;
+}
 
 cudaError_t copy_streams(CopyStreams** out) {
   thread_local CopyStreams per_device[kMaxDevices];
@@ -42,18 +51,9 @@ cudaError_t copy_streams(CopyStreams** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   CopyStreams& cs = per_device[dev];
-  if (cs.in == nullptr) {
-    if ((e = cudaStreamCreateWithFlags(&cs.in, cudaStreamNonBlocking)) != cudaSuccess) {
-      cs.in = nullptr;
-      return e;
-    }
-  }
-  if (cs.out == nullptr) {
-    if ((e = cudaStreamCreateWithFlags(&cs.out, cudaStreamNonBlocking)) != cudaSuccess) {
-      cs.out = nullptr;
-      return e;
-    }
-  }
+  if ((e = make_stream(&cs.in)) != cudaSuccess) return e;
+  if ((e = make_stream(&cs.out)) != cudaSuccess) return e;
+  if ((e = make_stream(&cs.side)) != cudaSuccess) return e;
   *out = &cs;
   return cudaSuccess;
 }
@@ -118,13 +118,17 @@ cudaError_t run_pipeline(const fa_tensors& h, const fa_tensors& dv, float* Dvec,
 
   Events evs;
   cudaEvent_t start, done;
-  std::vector<cudaEvent_t> in_ready(C), fwd_done(C), bwd_done(C);
+  std::vector<cudaEvent_t> in_ready(C), fwd_done(C), pre_done(C), bwd_done(C), dq_done(C);
   FA_TRY(evs.make(&start));
   FA_TRY(evs.make(&done));
   for (int c = 0; c < C; ++c) {
     FA_TRY(evs.make(&in_ready[c]));
     FA_TRY(evs.make(&fwd_done[c]));
-    if (with_bwd) FA_TRY(evs.make(&bwd_done[c]));
+    if (with_bwd) {
+      FA_TRY(evs.make(&pre_done[c]));
+      FA_TRY(evs.make(&bwd_done[c]));
+      FA_TRY(evs.make(&dq_done[c]));
+    }
   }
   // Both copy streams start after the work already queued on `stream`.
   FA_TRY(cudaEventRecord(start, stream));
@@ -162,13 +166,18 @@ cudaError_t run_pipeline(const fa_tensors& h, const fa_tensors& dv, float* Dvec,
                                     reinterpret_cast<const __nv_bfloat16*>(cptr(dv.dO, oq)), D, bh, N, d,
                                     stream);
     if (err != cudaSuccess) break;
+    // The dQ sweep needs only D: it runs on the side stream beside the
+    // dK/dV sweep (and the next slice's kernels).
+    if ((err = cudaEventRecord(pre_done[c], stream)) != cudaSuccess) break;
+    if ((err = cudaStreamWaitEvent(cs->side, pre_done[c], 0)) != cudaSuccess) break;
     err = fa::launch_bwd_dkdv(cptr(dv.q, oq), cptr(dv.k, okv), cptr(dv.v, okv), cptr(dv.dO, oq),
                               mptr(dv.dk, okv), mptr(dv.dv, okv), lse, D, bh, G, N, d, scale, causal, stream);
     if (err != cudaSuccess) break;
+    if ((err = cudaEventRecord(bwd_done[c], stream)) != cudaSuccess) break;
     err = fa::launch_bwd_dq(cptr(dv.q, oq), cptr(dv.k, okv), cptr(dv.v, okv), cptr(dv.dO, oq),
-                            mptr(dv.dq, oq), lse, D, bh, G, N, d, scale, causal, stream);
+                            mptr(dv.dq, oq), lse, D, bh, G, N, d, scale, causal, cs->side);
     if (err != cudaSuccess) break;
-    err = cudaEventRecord(bwd_done[c], stream);
+    err = cudaEventRecord(dq_done[c], cs->side);
   }
   // Stage 3: every slice's outputs, each as soon as its kernels are done.
   for (int c = 0; c < C && err == cudaSuccess; ++c) {
@@ -180,21 +189,43 @@ cudaError_t run_pipeline(const fa_tensors& h, const fa_tensors& dv, float* Dvec,
     if ((err = copy_out(h.lse, dv.lse, sr, cs->out)) != cudaSuccess) break;
     if (!with_bwd) continue;
     if ((err = cudaStreamWaitEvent(cs->out, bwd_done[c], 0)) != cudaSuccess) break;
-    if ((err = copy_out(h.dq, dv.dq, sq, cs->out)) != cudaSuccess) break;
     if ((err = copy_out(h.dk, dv.dk, skv, cs->out)) != cudaSuccess) break;
-    err = copy_out(h.dv, dv.dv, skv, cs->out);
+    if ((err = copy_out(h.dv, dv.dv, skv, cs->out)) != cudaSuccess) break;
+    if ((err = cudaStreamWaitEvent(cs->out, dq_done[c], 0)) != cudaSuccess) break;
+    err = copy_out(h.dq, dv.dq, sq, cs->out);
   }
-  // Join: `stream` passes this point only after both copy streams have
-  // drained what this call queued on them, also after a failure half-way.
+  // Join: `stream` passes this point only after the copy streams and the
+  // side stream have drained what this call queued on them, also after a
+  // failure half-way.
   cudaError_t e1 = cudaEventRecord(done, cs->in);
   if (e1 == cudaSuccess) e1 = cudaStreamWaitEvent(stream, done, 0);
-  cudaEvent_t done_out;
-  cudaError_t e2 = evs.make(&done_out);
-  if (e2 == cudaSuccess) e2 = cudaEventRecord(done_out, cs->out);
-  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(stream, done_out, 0);
+  cudaError_t e2 = cudaSuccess;
+  for (cudaStream_t side : {cs->out, cs->side}) {
+    cudaEvent_t ev;
+    cudaError_t e = evs.make(&ev);
+    if (e == cudaSuccess) e = cudaEventRecord(ev, side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev, 0);
+    if (e2 == cudaSuccess) e2 = e;
+  }
   if (err != cudaSuccess) return err;
   return e1 != cudaSuccess ? e1 : e2;
 }
+
+}  // namespace
+
+namespace fa {
+
+// The calling thread's side stream on the current device (see CopyStreams).
+cudaError_t side_stream(cudaStream_t* out) {
+  CopyStreams* cs = nullptr;
+  cudaError_t e = copy_streams(&cs);
+  if (e == cudaSuccess) *out = cs->side;
+  return e;
+}
+
+}  // namespace fa
+
+namespace {
 
 int check_common(const fa_tensors* host, const fa_tensors* dev, bool with_bwd, int B, int H, int Hkv,
                  int N, int d, float scale, int n_chunks) {

@@ -100,8 +100,12 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   dq, dk, dv      [B][H][N][d] bf16 outputs.
  *   workspace       device buffer of at least fa_bwd_workspace_bytes(...)
  *                   bytes, 16-byte aligned; contents on entry are ignored.
- * Launches three kernels in order on `stream`: preprocess (D), the dK/dV
- * sweep over query tiles, and the dQ sweep over key tiles.
+ * Launches three kernels: preprocess (D) on `stream`, then the dK/dV sweep
+ * over query tiles on `stream` and, beside it, the dQ sweep over key tiles
+ * on a side stream the library forks from `stream` after the preprocess and
+ * joins back to it (work queued on `stream` afterwards sees all three; the
+ * call is capturable into a CUDA graph). The first call on a host thread
+ * and device creates that side stream, kept until the thread exits.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
@@ -121,8 +125,8 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream);
 
 /*
- * The three backward stages as separate calls (fa_bwd_gqa runs all three,
- * in this order, on one stream). They share fa_bwd_gqa's argument rules
+ * The three backward stages as separate calls, each on `stream` (fa_bwd_gqa
+ * runs all three, the dQ sweep beside the dK/dV sweep). They share fa_bwd_gqa's argument rules
  * (Hkv = H for plain multi-head attention); `Dvec` is fp32 [B][H][N]
  * caller-owned device memory.
  *   fa_bwd_preprocess : Dvec_i = Σ_c dO_ic·O_ic.

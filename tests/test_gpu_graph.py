@@ -80,3 +80,31 @@ def test_host_pipeline_graph_replay_matches_eager(fa):
     assert fa.last_device_error() == 0
     for n, want in ref.items():
         assert torch.equal(host[n], want), n
+
+
+def test_fused_backward_graph_replay_matches_eager(fa):
+    """fa.bwd forks the dQ sweep onto the library's side stream and joins it
+    back; captured, it replays to the eager result."""
+    B, H, Hkv, N, d = 1, 4, 2, 500, 128
+    q, k, v, do = (t.cuda() for t in make_inputs(B, H, N, d, seed=31, Hkv=Hkv))
+    o, lse = fa.fwd(q, k, v, causal=True)
+    ws = torch.empty(fa.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    ref = fa.bwd(q, k, v, o, lse, do, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    outs = {}
+    with torch.cuda.stream(s):
+        outs["warm"] = fa.bwd(q, k, v, o, lse, do, causal=True, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs["graph"] = fa.bwd(q, k, v, o, lse, do, causal=True, workspace=ws)
+    for t in outs["graph"]:
+        t.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    for name, got, want in zip(("dq", "dk", "dv"), outs["graph"], ref):
+        assert torch.equal(got, want), name
