@@ -105,7 +105,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  * on a side stream the library forks from `stream` after the preprocess and
  * joins back to it (work queued on `stream` afterwards sees all three; the
  * call is capturable into a CUDA graph). The first call on a host thread
- * and device creates that side stream, kept until the thread exits.
+ * and device creates that side stream, kept until the thread exits. Calls
+ * from one host thread share it, so their dQ sweeps run in call order even
+ * when the calls are on different streams.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
