@@ -31,6 +31,7 @@ __all__ = [
     "decode_workspace_bytes",
     "fwd_host",
     "fwd_bwd_host",
+    "softmax_host",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -69,6 +70,7 @@ EXPORTED_SYMBOLS = (
     "fa_decode_paged",
     "fa_fwd_host",
     "fa_fwd_bwd_host",
+    "fa_softmax_host",
 )
 
 
@@ -128,6 +130,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_host.restype = i
         L.fa_fwd_bwd_host.argtypes = [tp, tp, vp, sz, i, i, i, i, i, f, i, i, vp]
         L.fa_fwd_bwd_host.restype = i
+        L.fa_softmax_host.argtypes = [vp, vp, vp, vp, ctypes.c_longlong, i, i, i, vp]
+        L.fa_softmax_host.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
         L.fa_status_string.argtypes = [i]
@@ -373,3 +377,18 @@ def fwd_bwd_host(host: dict, dev: dict, workspace, causal=False, scale=None, n_c
                                  workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
                                  _scale(d, scale), int(bool(causal)), int(n_chunks),
                                  _stream(dev["q"].device)), "fa_fwd_bwd_host")
+
+
+def softmax_host(x_host, y_host, x_dev, y_dev, online=True, n_chunks=0):
+    """Row softmax from host memory: x_host (CPU fp32, ideally pinned) is
+    copied into x_dev, normalised into y_dev and copied back into y_host, in
+    n_chunks pipelined slices of rows (0: the library's default).
+    Asynchronous on the current stream: synchronise it before reading y_host."""
+    for t, cuda in ((x_host, False), (y_host, False), (x_dev, True), (y_dev, True)):
+        if t.is_cuda != cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.shape != x_host.shape:
+            raise ValueError("x_host, y_host (CPU) and x_dev, y_dev (CUDA) must be contiguous float32 "
+                             "tensors of one shape")
+    n = x_host.shape[-1]
+    rows = x_host.numel() // n if n else 0
+    _check(lib().fa_softmax_host(_ptr(x_host), _ptr(y_host), _ptr(x_dev), _ptr(y_dev), rows, n,
+                                 int(bool(online)), int(n_chunks), _stream(x_dev.device)), "fa_softmax_host")

@@ -211,6 +211,63 @@ cudaError_t run_pipeline(const fa_tensors& h, const fa_tensors& dv, float* Dvec,
   return e1 != cudaSuccess ? e1 : e2;
 }
 
+// Row softmax of x [rows][n] fp32 from host memory, pipelined like the
+// attention calls: slices of consecutive rows (each one contiguous range)
+// are copied in, normalised and copied out on the three streams.
+cudaError_t run_softmax_pipeline(const float* xh, float* yh, float* xd, float* yd, long long rows, int n,
+                                 bool online, int n_chunks, cudaStream_t stream) {
+  CopyStreams* cs = nullptr;
+  FA_TRY(copy_streams(&cs));
+  const int C = static_cast<int>(n_chunks < rows ? n_chunks : rows);
+  const size_t row_bytes = static_cast<size_t>(n) * sizeof(float);
+  Events evs;
+  cudaEvent_t start, done;
+  std::vector<cudaEvent_t> in_ready(C), out_ready(C);
+  FA_TRY(evs.make(&start));
+  FA_TRY(evs.make(&done));
+  for (int c = 0; c < C; ++c) {
+    FA_TRY(evs.make(&in_ready[c]));
+    FA_TRY(evs.make(&out_ready[c]));
+  }
+  FA_TRY(cudaEventRecord(start, stream));
+  FA_TRY(cudaStreamWaitEvent(cs->in, start, 0));
+  FA_TRY(cudaStreamWaitEvent(cs->out, start, 0));
+  auto bounds = [&](int c, long long* r0, long long* r1) {
+    *r0 = rows * c / C;
+    *r1 = rows * (c + 1) / C;
+  };
+  cudaError_t err = cudaSuccess;
+  for (int c = 0; c < C && err == cudaSuccess; ++c) {
+    long long r0, r1;
+    bounds(c, &r0, &r1);
+    const Slice sl = slice(r0, r1, row_bytes);
+    if ((err = copy_in(xd, xh, sl, cs->in)) != cudaSuccess) break;
+    err = cudaEventRecord(in_ready[c], cs->in);
+  }
+  for (int c = 0; c < C && err == cudaSuccess; ++c) {
+    long long r0, r1;
+    bounds(c, &r0, &r1);
+    if ((err = cudaStreamWaitEvent(stream, in_ready[c], 0)) != cudaSuccess) break;
+    err = fa::launch_softmax(xd + r0 * n, yd + r0 * n, r1 - r0, n, online, stream);
+    if (err != cudaSuccess) break;
+    err = cudaEventRecord(out_ready[c], stream);
+  }
+  for (int c = 0; c < C && err == cudaSuccess; ++c) {
+    long long r0, r1;
+    bounds(c, &r0, &r1);
+    if ((err = cudaStreamWaitEvent(cs->out, out_ready[c], 0)) != cudaSuccess) break;
+    err = copy_out(yh, yd, slice(r0, r1, row_bytes), cs->out);
+  }
+  cudaError_t e1 = cudaEventRecord(done, cs->in);
+  if (e1 == cudaSuccess) e1 = cudaStreamWaitEvent(stream, done, 0);
+  cudaEvent_t done_out;
+  cudaError_t e2 = evs.make(&done_out);
+  if (e2 == cudaSuccess) e2 = cudaEventRecord(done_out, cs->out);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(stream, done_out, 0);
+  if (err != cudaSuccess) return err;
+  return e1 != cudaSuccess ? e1 : e2;
+}
+
 }  // namespace
 
 namespace fa {
@@ -294,6 +351,18 @@ int fa_fwd_bwd_host(const fa_tensors* host, const fa_tensors* dev, void* workspa
   const cudaError_t e = run_pipeline(*host, *dev, static_cast<float*>(workspace), true, B, H, Hkv, N, d,
                                      scale, causal != 0, chunks_or_default(n_chunks, B, Hkv, N),
                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_softmax_host(const float* x_host, float* y_host, float* x_dev, float* y_dev, long long rows, int n,
+                    int online, int n_chunks, void* stream) {
+  if (!x_host || !y_host || !x_dev || !y_dev || rows < 1 || n < 1 || n_chunks < 0) return FA_ERR_INVALID_ARG;
+  if (rows > INT_MAX) return FA_ERR_UNSUPPORTED;
+  if (((reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(y_dev)) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  const int C = n_chunks == 0 ? kDefaultChunks : (n_chunks > kMaxChunks ? kMaxChunks : n_chunks);
+  const cudaError_t e = run_softmax_pipeline(x_host, y_host, x_dev, y_dev, rows, n, online != 0, C,
+                                             static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -257,6 +257,21 @@ int fa_softmax_safe(const float* x, float* y, long long rows, int n, void* strea
 int fa_softmax_online(const float* x, float* y, long long rows, int n, void* stream);
 
 /*
+ * Row softmax from host memory: copies x_host [rows][n] fp32 into x_dev,
+ * runs fa_softmax_online (online != 0) or fa_softmax_safe on the device
+ * buffers, and copies y_dev into y_host, in n_chunks pipelined slices of
+ * consecutive rows (0 = 8; clamped to rows and 64) so that the copies of
+ * one slice overlap another's kernel. Results equal the device call's bit
+ * for bit. Ordering, resources and page-locking as in fa_fwd_host.
+ * Errors: a NULL pointer, rows or n < 1, n_chunks < 0 -> FA_ERR_INVALID_ARG;
+ * rows > 2^31 - 1 -> FA_ERR_UNSUPPORTED; x_dev or y_dev not 4-byte aligned
+ * -> FA_ERR_MISALIGNED; FA_ERR_CUDA when a copy, event or launch fails
+ * after part of the work was queued.
+ */
+int fa_softmax_host(const float* x_host, float* y_host, float* x_dev, float* y_dev, long long rows, int n,
+                    int online, int n_chunks, void* stream);
+
+/*
  * Merge of partial attention results over disjoint key blocks ("07-16 下午"
  * notes, section 长上下文与序列并行: blocks are not normalised separately and
  * added; each block's normaliser and weighted sum are rescaled by

@@ -241,3 +241,16 @@ int main(void) {
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stderr)
     assert re.match(r"^\d+\.\d+\.\d+$", r.stdout.strip())
+
+
+def test_softmax_host_argument_errors(L):
+    def call(xh=FAKE, yh=FAKE, xd=FAKE, yd=FAKE, rows=4, n=16, chunks=0):
+        return L.fa_softmax_host(xh, yh, xd, yd, rows, n, 1, chunks, NUL)
+
+    assert call(xh=NUL) == 1
+    assert call(yd=NUL) == 1
+    assert call(rows=0) == 1
+    assert call(n=0) == 1
+    assert call(chunks=-1) == 1
+    assert call(rows=2**31) == 2
+    assert call(xd=ctypes.c_void_p(0x10002)) == 3

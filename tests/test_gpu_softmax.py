@@ -81,3 +81,23 @@ def test_softmax_misaligned_rows_use_the_scalar_path(fa):
         fn(x, out=out)
         torch.cuda.synchronize()
         np.testing.assert_allclose(out.cpu().numpy(), y.cpu().numpy(), rtol=REL, atol=ABS)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("online", [True, False])
+def test_softmax_host_matches_device_call(fa, pinned, online):
+    """Rows from host memory through the pipelined call give the device
+    call's bits (n % 4 != 0 exercises the scalar path on every slice)."""
+    for rows, n, chunks in ((300, 1000, 0), (7, 4099, 3), (1, 64, 5)):
+        x = draw(rows, n, seed=rows + n, std=3.0)
+        xh = x.pin_memory() if pinned else x.clone()
+        yh = torch.full_like(x, float("nan"))
+        if pinned:
+            yh = yh.pin_memory()
+        xd, yd = torch.empty_like(x, device="cuda"), torch.empty_like(x, device="cuda")
+        fa.softmax_host(xh, yh, xd, yd, online=online, n_chunks=chunks)
+        torch.cuda.synchronize()
+        ref = (fa.softmax_online if online else fa.softmax_safe)(x.cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(yh, ref.cpu())
+        assert torch.equal(yd, ref)
