@@ -60,6 +60,7 @@ EXPORTED_SYMBOLS = (
     "fa_bwd_dkdv",
     "fa_bwd_dq",
     "fa_last_device_error",
+    "fa_selftest_wait_limit",
     "fa_status_string",
     "fa_version",
     "fa_bwd_noalloc",
@@ -134,6 +135,8 @@ def lib() -> ctypes.CDLL:
         L.fa_softmax_host.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
+        L.fa_selftest_wait_limit.argtypes = [vp]
+        L.fa_selftest_wait_limit.restype = i
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_version.argtypes = []
@@ -240,6 +243,14 @@ def bwd_dq(q, k, v, do, lse, Dvec, dq, causal=False, scale=None):
     _check(lib().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dq),
                            B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)),
            "fa_bwd_dq")
+
+
+def selftest_wait_limit(device=None) -> None:
+    """Enqueue the error-path self-test on the current stream: a wait that
+    nothing satisfies gives up after its limit, so the next
+    last_device_error() returns 5 (FA_ERR_TIMEOUT)."""
+    dev = torch.device("cuda") if device is None else device
+    _check(lib().fa_selftest_wait_limit(_stream(dev)), "fa_selftest_wait_limit")
 
 
 def last_device_error(device=None) -> int:

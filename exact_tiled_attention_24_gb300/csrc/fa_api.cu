@@ -243,6 +243,10 @@ int fa_attn_merge(const float* o_parts, const float* lse_parts, int n_parts, voi
                                         static_cast<cudaStream_t>(stream)));
 }
 
+int fa_selftest_wait_limit(void* stream) {
+  return map_cuda(fa::launch_wait_limit_selftest(static_cast<cudaStream_t>(stream)));
+}
+
 int fa_last_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t ef = 0, eb = 0, ed = 0;

@@ -338,6 +338,16 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
  */
 int fa_last_device_error(void* stream);
 
+/*
+ * Self-test of the device error path. Launches one warp on `stream` that
+ * waits on an mbarrier nothing arrives on, through the same bounded wait
+ * every kernel of this library uses; the wait gives up after its limit
+ * (2 s) and the kernel returns. The next fa_last_device_error then returns
+ * FA_ERR_TIMEOUT, and the context stays usable. Reads and writes no caller
+ * memory. Returns FA_OK when the launch was enqueued, else FA_ERR_CUDA.
+ */
+int fa_selftest_wait_limit(void* stream);
+
 /* Human-readable name of an fa_status value (static string). */
 const char* fa_status_string(int status);
 
