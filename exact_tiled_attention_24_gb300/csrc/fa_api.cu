@@ -249,13 +249,14 @@ int fa_selftest_wait_limit(void* stream) {
 
 int fa_last_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t ef = 0, eb = 0, ed = 0;
+  uint32_t ef = 0, eb = 0, ed = 0, et = 0;
   if (fa::read_and_clear_fwd_error(&ef, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_and_clear_bwd_error(&eb, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_and_clear_decode_error(&ed, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (ef == 1 || eb == 1 || ed == 1) return FA_ERR_TIMEOUT;
+  if (fa::read_and_clear_selftest_error(&et, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (ef == 1 || eb == 1 || ed == 1 || et == 1) return FA_ERR_TIMEOUT;
   if (ed == 2) return FA_ERR_BAD_INDEX;
-  if (ef || eb || ed) return FA_ERR_TIMEOUT;
+  if (ef || eb || ed || et) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
 

@@ -55,6 +55,7 @@ cudaError_t side_stream(cudaStream_t* out);
 
 // Device error words (one per translation unit): read, then clear.
 cudaError_t launch_wait_limit_selftest(cudaStream_t stream);
+cudaError_t read_and_clear_selftest_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_decode_error(uint32_t* out, cudaStream_t stream);

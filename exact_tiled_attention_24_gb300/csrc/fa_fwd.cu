@@ -457,25 +457,6 @@ cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, flo
                 : fwd::launch_t<128, false>(tq, tk, tv, to, lse, BH, G, N, scale, stream);
 }
 
-// One warp waits on an mbarrier that nothing ever arrives on, through the
-// bounded wait every pipeline role uses. The wait gives up after kWaitLimitNs
-// and records DEV_TIMEOUT in the forward error word; the kernel then returns,
-// so the context stays usable. It exists to exercise that error path.
-__global__ void __launch_bounds__(32) wait_limit_selftest_kernel() {
-  __shared__ __align__(8) uint64_t bar;
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  mbar_wait_warp(&bar, 0, &g_fwd_err);
-}
-
-cudaError_t launch_wait_limit_selftest(cudaStream_t stream) {
-  wait_limit_selftest_kernel<<<1, 32, 0, stream>>>();
-  return cudaGetLastError();
-}
-
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream) {
   cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fwd_err, sizeof(uint32_t), 0,
                                             cudaMemcpyDeviceToHost, stream);
