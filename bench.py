@@ -107,23 +107,42 @@ class ClockSampler:
         self.bus_id = bus_id
         self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []          # (arrival time, line)
         self.thread = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
+        """Start sampling and wait (at most 5 s) for the first sample, so that
+        the sampler is live when the timed region begins."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  f"-lms={self.period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            deadline = time.monotonic() + 5.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def region_start(self):
+        self.t0 = time.monotonic()
+
+    def region_end(self):
+        """Call after the timed region's final synchronize. Waits up to two
+        periods for a sample taken after the region (used only when the
+        region is shorter than the sampling period)."""
+        self.t1 = time.monotonic()
+        deadline = self.t1 + 2.5 * self.period_ms / 1000.0
+        while (self.proc is not None and time.monotonic() < deadline
+               and not any(t > self.t1 for t, _ in self.lines)):
+            time.sleep(0.005)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -135,8 +154,17 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self):
+        lines = list(self.lines)
+        where = "all"
+        if self.t0 is not None and self.t1 is not None:
+            inside = [(t, l) for t, l in lines if self.t0 <= t <= self.t1]
+            if inside:
+                lines, where = inside, "timed region"
+            else:
+                after = [(t, l) for t, l in lines if t > self.t1][:1]
+                lines, where = after, "first sample after the timed region (shorter than the period)"
         rows = []
-        for line in self.lines:
+        for _, line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
                 continue
@@ -157,7 +185,7 @@ class ClockSampler:
         under_load = [s for s in sm if smax and s >= 0.3 * max(smax)] or sm
         return {"sm_mhz": statistics.median(under_load) if under_load else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows),
+                "reasons": reasons, "samples": len(rows), "sampled": where,
                 "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
 
 
@@ -313,11 +341,13 @@ def run_ours(args, w, rank, world, dist):
     barrier(dist)
     torch.cuda.synchronize(dev)
     with ClockSampler(bus_id=bus) as clk:
+        clk.region_start()
         t_start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.region_end()
     barrier(dist)
     elapsed_ms = t_start.elapsed_time(t_end)
     if fa.last_device_error(dev) != 0:
@@ -470,6 +500,7 @@ def run_softmax(args, rw, rank, world, dist):
     barrier(dist)
     ms = {}
     with ClockSampler(bus_id=bus) as clk:
+        clk.region_start()
         for name, fn in fns.items():
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -478,6 +509,7 @@ def run_softmax(args, rw, rank, world, dist):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             ms[name] = e0.elapsed_time(e1) / args.steps
+        clk.region_end()
     barrier(dist)
     m_on, m_safe = max_over_ranks([ms["online"], ms["safe"]], dist, dev)
     ms = {"online": m_on, "safe": m_safe}
@@ -639,11 +671,13 @@ def run_decode(args, dw, rank, world, dist):
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(bus_id=bus) as clk:
+        clk.region_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
+        clk.region_end()
     ms = e0.elapsed_time(e1) / args.steps
     if fa.last_device_error(dev) != 0:
         raise RuntimeError("device error during the timed region")

@@ -1,7 +1,7 @@
 """Run the forward + backward a few times on one shape, for profiler captures.
 
     python -m exact_tiled_attention_24_gb300.profile_case --B 1 --H 32 --N 4096 --d 128 \
-        --causal --iters 2 [--Hkv 8]
+        --causal --iters 2 [--Hkv 8] [--fwd-only] [--q-std 4]
     python -m exact_tiled_attention_24_gb300.profile_case --softmax-rows 1216 --softmax-n 262144
     python -m exact_tiled_attention_24_gb300.profile_case --decode d1
 
@@ -21,6 +21,7 @@ def main():
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--q-std", type=float, default=1.0, help="standard deviation of q (c5 draws 4)")
     ap.add_argument("--Hkv", type=int, default=0, help="K/V heads (grouped-query); 0 = H")
     ap.add_argument("--softmax-rows", type=int, default=0, help="run the row softmax kernels instead")
     ap.add_argument("--softmax-n", type=int, default=262144)
@@ -55,7 +56,7 @@ def main():
         print("ok")
         return
     q, k, v, do = (t.to(dev) for t in make_inputs(args.B, args.H, args.N, args.d, seed=99,
-                                                   Hkv=args.Hkv or None))
+                                                   q_std=args.q_std, Hkv=args.Hkv or None))
     for _ in range(args.iters):
         o, lse = fa.fwd(q, k, v, causal=args.causal)
         if not args.fwd_only:
