@@ -131,7 +131,11 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!workspace || ws_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_WORKSPACE;
-  if (!aligned16(workspace) || !aligned16(o) || !aligned16(dq)) return FA_ERR_MISALIGNED;
+  // Every pointer is checked here, before the preprocess is launched, so
+  // that an error leaves nothing queued (the stages repeat these checks).
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return FA_ERR_MISALIGNED;
   float* Dvec = static_cast<float*>(workspace);
   st = fa_bwd_preprocess(o, dO, Dvec, B, H, N, d, stream);
   if (st != FA_OK) return st;

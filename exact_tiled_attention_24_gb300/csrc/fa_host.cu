@@ -110,7 +110,9 @@ cudaError_t run_pipeline(const fa_tensors& h, const fa_tensors& dv, float* Dvec,
   const int C = static_cast<int>(n_chunks < units ? n_chunks : units);
   const size_t row_b = static_cast<size_t>(N) * d * 2;  // one head of a bf16 tensor
   const size_t q_unit = row_b * G, kv_unit = row_b;     // bytes per pair
-  const size_t r_unit = static_cast<size_t>(N) * G * 4;  // lse, D per pair
+  // lse, D per pair. A slice of them may start only 4-byte aligned (N and G
+  // odd): every kernel reads and writes them one float at a time.
+  const size_t r_unit = static_cast<size_t>(N) * G * 4;
   auto bounds = [&](int c, long long* u0, long long* u1) {
     *u0 = units * c / C;
     *u1 = units * (c + 1) / C;

@@ -86,6 +86,12 @@ def test_bwd_argument_errors(L):
     assert call(workspace=NUL) == 6
     assert call(ws_bytes=ws - 1) == 6
     assert call(workspace=MIS) == 3
+    # a misaligned operand of a later stage is rejected before the first
+    # stage is queued (nothing reaches the device: no CUDA call is made)
+    for pos in range(9):
+        args = [FAKE] * 9
+        args[pos] = MIS
+        assert L.fa_bwd(*args, FAKE, ws, 1, 1, 16, 64, 0.125, 1, NUL) == 3, pos
     # stage entry points
     assert L.fa_bwd_preprocess(FAKE, FAKE, NUL, 1, 1, 16, 64, NUL) == 1
     assert L.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MIS, 1, 1, 1, 16, 64,
