@@ -153,6 +153,35 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+# Device type of every tensor the kernels touch. The library launches on the
+# current CUDA device, so the tensors must live there as well.
+_DEVICE_TYPE = "cuda"
+
+
+def _on_device(t, name):
+    """Raise unless t is a tensor on a device the library can launch on."""
+    if not isinstance(t, torch.Tensor) or t.device.type != _DEVICE_TYPE:
+        raise ValueError(f"{name} must be a {_DEVICE_TYPE.upper()} tensor")
+    if _DEVICE_TYPE == "cuda" and t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device} but the current device is cuda:"
+                         f"{torch.cuda.current_device()}: call under torch.cuda.device({t.device})")
+
+
+def _expect(t, name, shape, dtype, device):
+    """Raise unless t is a contiguous `dtype` tensor of exactly `shape` on
+    `device`: a buffer the kernels read or write in full, so a smaller one
+    would be overrun."""
+    if (not isinstance(t, torch.Tensor) or tuple(t.shape) != tuple(shape) or t.dtype != dtype
+            or not t.is_contiguous() or t.device != device):
+        raise ValueError(f"{name}: expected a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+
+
+def _expect_workspace(ws, device):
+    """The workspace's size is checked by the library; here its place."""
+    if not isinstance(ws, torch.Tensor) or ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+
+
 def _check(status, where):
     if status != 0:
         raise FAError(status, where)
@@ -165,8 +194,9 @@ def _check_inputs(q, k, v, *rest):
         raise ValueError("expected [B, H, N, d] tensors")
     B, H, N, d = q.shape
     Hkv = k.shape[1]
+    _on_device(q, "q")
     for t in (q, k, v) + rest:
-        if not t.is_cuda:
+        if t.device.type != _DEVICE_TYPE:
             raise ValueError("tensors must be on a CUDA device")
         if t.dtype != torch.bfloat16:
             raise ValueError("tensors must be bfloat16")
@@ -193,6 +223,10 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None):
     h then uses K/V head h // (H // Hkv)."""
     Hkv = _check_inputs(q, k, v)
     B, H, N, d = q.shape
+    if out is not None:
+        _expect(out, "out", q.shape, torch.bfloat16, q.device)
+    if lse is not None:
+        _expect(lse, "lse", (B, H, N), torch.float32, q.device)
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _check(lib().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, Hkv, N, d,
@@ -209,9 +243,11 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None):
     (dk, dv shaped like k, v; with grouped-query heads they sum over the group)."""
     Hkv = _check_inputs(q, k, v, o, do)
     B, H, N, d = q.shape
+    _expect(lse, "lse", (B, H, N), torch.float32, q.device)
     ws_bytes = bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _expect_workspace(workspace, q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     _check(lib().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                             _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -222,15 +258,21 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None):
 
 def bwd_preprocess(o, do, Dvec):
     """Dvec = rowsum(do * o) (fp32 [B, H, N])."""
+    _check_inputs(o, o, o, do)
     B, H, N, d = o.shape
+    _expect(Dvec, "Dvec", (B, H, N), torch.float32, o.device)
     _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(Dvec), B, H, N, d, _stream(o.device)),
            "fa_bwd_preprocess")
 
 
 def bwd_dkdv(q, k, v, do, lse, Dvec, dk, dv, causal=False, scale=None):
     """dk, dv (bf16, written in place) from the recomputed P and dS."""
+    Hkv = _check_inputs(q, k, v, do)
     B, H, N, d = q.shape
-    Hkv = k.shape[1]
+    _expect(lse, "lse", (B, H, N), torch.float32, q.device)
+    _expect(Dvec, "Dvec", (B, H, N), torch.float32, q.device)
+    _expect(dk, "dk", k.shape, torch.bfloat16, q.device)
+    _expect(dv, "dv", k.shape, torch.bfloat16, q.device)
     _check(lib().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dk),
                              _ptr(dv), B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)),
                              _stream(q.device)), "fa_bwd_dkdv")
@@ -238,8 +280,11 @@ def bwd_dkdv(q, k, v, do, lse, Dvec, dk, dv, causal=False, scale=None):
 
 def bwd_dq(q, k, v, do, lse, Dvec, dq, causal=False, scale=None):
     """dq (bf16, written in place) from the recomputed dS."""
+    Hkv = _check_inputs(q, k, v, do)
     B, H, N, d = q.shape
-    Hkv = k.shape[1]
+    _expect(lse, "lse", (B, H, N), torch.float32, q.device)
+    _expect(Dvec, "Dvec", (B, H, N), torch.float32, q.device)
+    _expect(dq, "dq", q.shape, torch.bfloat16, q.device)
     _check(lib().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dq),
                            B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)),
            "fa_bwd_dq")
@@ -259,34 +304,44 @@ def last_device_error(device=None) -> int:
     return int(lib().fa_last_device_error(_stream(dev)))
 
 
-def _softmax(fn, name, x, out):
-    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous() or x.dim() < 1:
+def _softmax(name, x, out):
+    if x.device.type != _DEVICE_TYPE or x.dtype != torch.float32 or not x.is_contiguous() or x.dim() < 1:
         raise ValueError("x must be a contiguous float32 CUDA tensor")
+    _on_device(x, "x")
     n = x.shape[-1]
     rows = x.numel() // n if n else 0
+    if out is not None:
+        _expect(out, "out", x.shape, torch.float32, x.device)
     y = torch.empty_like(x) if out is None else out
-    _check(fn(_ptr(x), _ptr(y), rows, n, _stream(x.device)), name)
+    _check(getattr(lib(), name)(_ptr(x), _ptr(y), rows, n, _stream(x.device)), name)
     return y
 
 
 def softmax_safe(x, out=None):
     """Softmax over the last dimension of fp32 x, three passes per row."""
-    return _softmax(lib().fa_softmax_safe, "fa_softmax_safe", x, out)
+    return _softmax("fa_softmax_safe", x, out)
 
 
 def softmax_online(x, out=None):
     """Softmax over the last dimension of fp32 x, two passes per row (online)."""
-    return _softmax(lib().fa_softmax_online, "fa_softmax_online", x, out)
+    return _softmax("fa_softmax_online", x, out)
 
 
 def attn_merge(o_parts, lse_parts, out=None, lse=None):
     """Combine partial attention results: o_parts [S, rows, d] fp32, lse_parts
     [S, rows] fp32 -> (o [rows, d] bf16, lse [rows] fp32)."""
+    _on_device(o_parts, "o_parts")
     S, rows, d = o_parts.shape
     if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
         raise ValueError("o_parts and lse_parts must be float32")
     if lse_parts.shape != (S, rows) or not (o_parts.is_contiguous() and lse_parts.is_contiguous()):
         raise ValueError("lse_parts must be a contiguous [S, rows] tensor beside contiguous o_parts")
+    if lse_parts.device != o_parts.device:
+        raise ValueError("o_parts and lse_parts must be on one device")
+    if out is not None:
+        _expect(out, "out", (rows, d), torch.bfloat16, o_parts.device)
+    if lse is not None:
+        _expect(lse, "lse", (rows,), torch.float32, o_parts.device)
     o = torch.empty((rows, d), dtype=torch.bfloat16, device=o_parts.device) if out is None else out
     lse_t = torch.empty((rows,), dtype=torch.float32, device=o_parts.device) if lse is None else lse
     _check(lib().fa_attn_merge(_ptr(o_parts), _ptr(lse_parts), S, _ptr(o), _ptr(lse_t), rows, d,
@@ -306,17 +361,25 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, n_splits=1, scale=N
     lse [B, H] fp32)."""
     B, H, d = q.shape
     num_blocks, Hkv, bs, dk = k_cache.shape
+    _on_device(q, "q")
     for t in (q, k_cache, v_cache):
-        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError("q, k_cache, v_cache must be contiguous bfloat16 CUDA tensors")
+        if t.device != q.device or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k_cache, v_cache must be contiguous bfloat16 CUDA tensors on one device")
     if v_cache.shape != k_cache.shape or dk != d:
         raise ValueError("k_cache and v_cache must be [num_blocks, Hkv, block_size, d]")
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32 or block_table.dim() != 2 \
             or block_table.shape[0] != B or seq_lens.shape != (B,) or not block_table.is_contiguous():
         raise ValueError("block_table [B, max_blocks] and seq_lens [B] must be int32")
+    _expect(block_table, "block_table", block_table.shape, torch.int32, q.device)
+    _expect(seq_lens, "seq_lens", (B,), torch.int32, q.device)
     ws_bytes = decode_workspace_bytes(B, H, d, n_splits)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _expect_workspace(workspace, q.device)
+    if out is not None:
+        _expect(out, "out", q.shape, torch.bfloat16, q.device)
+    if lse is not None:
+        _expect(lse, "lse", (B, H), torch.float32, q.device)
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
     _check(lib().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
@@ -341,8 +404,10 @@ def _tensors(ts: dict, on_cuda: bool, shapes: dict, names):
         want_dtype = torch.float32 if n == "lse" else torch.bfloat16
         if tuple(t.shape) != shapes[n] or t.dtype != want_dtype or not t.is_contiguous():
             raise ValueError(f"{n}: expected a contiguous {want_dtype} tensor of shape {shapes[n]}")
-        if t.is_cuda != on_cuda:
+        if (t.device.type == _DEVICE_TYPE) != on_cuda or (not on_cuda and t.device.type != "cpu"):
             raise ValueError(f"{n}: expected a {'CUDA' if on_cuda else 'host'} tensor")
+        if on_cuda and t.device != ts[names[0]].device:
+            raise ValueError(f"{n}: the device tensors must be on one device")
         setattr(st, n, t.data_ptr())
     return st
 
@@ -368,6 +433,7 @@ def fwd_host(host: dict, dev: dict, causal=False, scale=None, n_chunks=0):
     shapes = _host_shapes(q, k)
     h = _tensors(host, False, shapes, names)
     dv = _tensors(dev, True, shapes, names)
+    _on_device(dev["q"], 'dev["q"]')
     _check(lib().fa_fwd_host(ctypes.byref(h), ctypes.byref(dv), B, H, Hkv, N, d, _scale(d, scale),
                              int(bool(causal)), int(n_chunks), _stream(dev["q"].device)), "fa_fwd_host")
 
@@ -382,8 +448,8 @@ def fwd_bwd_host(host: dict, dev: dict, workspace, causal=False, scale=None, n_c
     shapes = _host_shapes(q, k)
     h = _tensors(host, False, shapes, _HOST_NAMES)
     dv = _tensors(dev, True, shapes, _HOST_NAMES)
-    if not workspace.is_cuda:
-        raise ValueError("workspace must be a CUDA tensor")
+    _on_device(dev["q"], 'dev["q"]')
+    _expect_workspace(workspace, dev["q"].device)
     _check(lib().fa_fwd_bwd_host(ctypes.byref(h), ctypes.byref(dv), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
                                  _scale(d, scale), int(bool(causal)), int(n_chunks),
@@ -395,10 +461,12 @@ def softmax_host(x_host, y_host, x_dev, y_dev, online=True, n_chunks=0):
     copied into x_dev, normalised into y_dev and copied back into y_host, in
     n_chunks pipelined slices of rows (0: the library's default).
     Asynchronous on the current stream: synchronise it before reading y_host."""
-    for t, cuda in ((x_host, False), (y_host, False), (x_dev, True), (y_dev, True)):
-        if t.is_cuda != cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.shape != x_host.shape:
+    for t, dev_side in ((x_host, False), (y_host, False), (x_dev, True), (y_dev, True)):
+        place_ok = t.device == x_dev.device if dev_side else t.device.type == "cpu"
+        if not place_ok or t.dtype != torch.float32 or not t.is_contiguous() or t.shape != x_host.shape:
             raise ValueError("x_host, y_host (CPU) and x_dev, y_dev (CUDA) must be contiguous float32 "
                              "tensors of one shape")
+    _on_device(x_dev, "x_dev")
     n = x_host.shape[-1]
     rows = x_host.numel() // n if n else 0
     _check(lib().fa_softmax_host(_ptr(x_host), _ptr(y_host), _ptr(x_dev), _ptr(y_dev), rows, n,
