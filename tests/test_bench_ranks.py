@@ -82,3 +82,27 @@ def test_reference_arm_prints_from_rank_zero_only(rank):
         assert res["e2e"]["h2d_bytes_per_step"] == 0
     else:
         assert lines == []
+
+
+@pytest.mark.parametrize("workload", ["c1", "s1", "d1"])
+def test_reference_arm_line_format(workload):
+    """One process, N = 1: the reference arm's single JSON line carries the
+    contract's keys for the attention, row-softmax and decode workloads."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        workload, "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    res = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in res, key
+    assert res["impl"] == "reference" and res["n_gpus"] == 1 and res["steps"] == 1 and res["warmup"] == 3
+    assert res["value"] > 0 and res["ms_per_step"] > 0 and res["higher_is_better"] is True
+    assert res["config"]["workload"].startswith(workload)
+    cb = res["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == res["value"]
+    assert res["e2e"] == {"value": res["value"], "unit": res["unit"], "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
