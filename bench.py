@@ -103,7 +103,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, bus_id=None, period_ms=100):
+    def __init__(self, bus_id=None, period_ms=20):
         self.bus_id = bus_id
         self.period_ms = period_ms
         self.proc = None
@@ -191,27 +191,69 @@ class ClockSampler:
 
 # -------------------------------------------------------------- oracle leg
 
-def oracle_sample(w, q, k, v, do, heads, n=None):
+def oracle_sample(w, q, k, v, do, heads, n=None, keep_first=False):
     """Time the fp64 oracle's forward + backward on the given heads, each
     restricted to its first n queries and keys (all N when n is None: a
     prefix of a head is itself a complete attention problem of length n).
-    Returns (seconds, algorithmic FLOPs of the sample)."""
+    Returns (seconds, algorithmic FLOPs of the sample), plus the first
+    head's oracle results {o, lse, dq, dk, dv} when keep_first is set."""
     from exact_tiled_attention_24_gb300.workloads import to_f64
     from oracle import attention_bwd_head, attention_fwd_head
     causal = True in w.causal
     n = w.N if n is None else n
+    first = None
     t0 = time.perf_counter()
     for (b, h) in heads:
         hk = h // (w.H // w.kv_heads)  # the K/V head query head h reads
         qq, dd = to_f64(q[b, h, :n]), (to_f64(do[b, h, :n]) if do is not None else None)
         kk, vv = to_f64(k[b, hk, :n]), to_f64(v[b, hk, :n])
-        attention_fwd_head(qq, kk, vv, w.scale, causal)
-        if do is not None:
-            attention_bwd_head(qq, kk, vv, dd, w.scale, causal)
+        fo = attention_fwd_head(qq, kk, vv, w.scale, causal)
+        bo = attention_bwd_head(qq, kk, vv, dd, w.scale, causal) if do is not None else None
+        if keep_first and first is None:
+            first = {"o": fo[0], "lse": fo[1]}
+            if bo is not None:
+                first.update({"dq": bo[0], "dk": bo[1], "dv": bo[2]})
     dt = time.perf_counter() - t0
     pairs = n * (n + 1) // 2 if causal else n * n
     per_head = (4 * w.d + (10 * w.d if do is not None else 0)) * pairs
+    if keep_first:
+        return dt, per_head * len(heads), first
     return dt, per_head * len(heads)
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def oracle_errors(first, gpu, b, h, G):
+    """Max-abs and mean-abs difference between the GPU's outputs for head
+    (b, h) and the oracle's. dk and dv are compared only with one K/V head
+    per query head (with grouped heads the GPU's dk, dv sum over the group)."""
+    import numpy as np
+    out = {}
+    for name, ref in first.items():
+        if name in ("dk", "dv") and G != 1:
+            continue
+        t = gpu[name][b, h] if name not in ("dk", "dv") else gpu[name][b, h // G]
+        got = t.detach().to("cpu", dtype=__import__("torch").float64).numpy()
+        diff = np.abs(got - ref)
+        out[name] = {"max_abs": float(diff.max()), "mean_abs": float(diff.mean())}
+    return out
 
 
 def run_reference(args, w, rank):
@@ -242,7 +284,7 @@ def run_reference(args, w, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(args, w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -278,6 +320,61 @@ def traffic_for(kernel_key, sources):
     if ent.get("source_sha256") != h.hexdigest():
         return None
     return ent.get("dram_bytes_per_launch")
+
+
+def pick_peak(peaks, region_s, clocks):
+    """The bf16 denominator for a kernel timed in this run: the burst figure
+    for a timed region under a second that kept its clocks (no power cap),
+    else the sustained figure (measured over seconds under the power cap)."""
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    name = "bf16_tflops" if region_s < 1.0 and not capped else "bf16_tflops_sustained"
+    return float(peaks.get(name, FALLBACK_PEAKS[name])), name
+
+
+def long_context_leg(args, dev, dist, peaks, peak_kind):
+    """The long-context forward (B=1 H=16 N=32768 d=128, causal, q ~ N(0, 4^2))
+    timed on its own with CUDA events, with its own clock samples."""
+    import torch
+
+    import exact_tiled_attention_24_gb300 as fa
+    from exact_tiled_attention_24_gb300.workloads import WORKLOADS, workload_inputs
+
+    w5 = WORKLOADS["c5"]
+    q, k, v = (t.to(dev) for t in workload_inputs("c5", with_do=False)[:3])
+    o = torch.empty_like(q)
+    lse = torch.empty((w5.B, w5.H, w5.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(5, min(args.steps, 20))
+    for _ in range(args.warmup):
+        fa.fwd(q, k, v, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(bus_id=bus) as clk:
+        clk.region_start()
+        e0.record(stream)
+        for _ in range(steps):
+            fa.fwd(q, k, v, causal=True, out=o, lse=lse)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk.region_end()
+    if fa.last_device_error(dev) != 0:
+        raise RuntimeError("device error during the long-context forward")
+    ms, = max_over_ranks([e0.elapsed_time(e1) / steps], dist, dev)
+    clocks = clk.summary()
+    peak, peak_name = pick_peak(peaks, ms * steps / 1e3, clocks)
+    tflops = flops(w5, "fwd") / (ms * 1e-3) / 1e12
+    fsrc = ["exact_tiled_attention_24_gb300/csrc/fa_fwd.cu", "exact_tiled_attention_24_gb300/csrc/fa_ptx.cuh"]
+    return {"workload": "c5: B=1 H=16 N=32768 d=128 causal=True bf16, q ~ N(0, 4^2)", "steps": steps,
+            "ms": ms, "tflops": tflops, "frac": tflops / peak, "peak": peak,
+            "peak_source": f"{peak_kind} {peak_name}", "nominal_2250": tflops / 2250.0,
+            "traffic": traffic_for("fwd_c5", fsrc), "clocks": clocks, "gpu_launches": steps}
 
 
 def run_ours(args, w, rank, world, dist):
@@ -385,11 +482,14 @@ def run_ours(args, w, rank, world, dist):
     if has_bwd:
         cands += [("bwd_dkdv", dkdv_ms, F_fwd * 2, bsrc), ("bwd_dq", dq_ms, F_fwd // 2, bsrc)]
     dom, dom_ms, dom_flops, srcs = max(cands, key=lambda c: c[1])
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    clocks = clk.summary()
+    region_s = elapsed_ms / 1e3
+    peak, peak_name = pick_peak(peaks, region_s, clocks)
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{peak_kind} bf16_tflops_sustained (kernel timed inside a long step)",
+                "peak_source": f"{peak_kind} {peak_name}",
+                "timed_region_s": region_s, "sm_mhz_median": clocks.get("sm_mhz"),
                 "traffic": traffic_for(f"{dom}_{args.workload}", srcs)}
 
     # End-to-end: host buffers in, results out, every step, through the
@@ -439,30 +539,38 @@ def run_ours(args, w, rank, world, dist):
         "fwd_tflops": F_fwd / (fwd_ms * 1e-3) / 1e12,
         "fwd_ms": fwd_ms,
         "frac_of_peak": {"fwd_bwd": value / world / peak, "fwd": F_fwd / (fwd_ms * 1e-3) / 1e12 / peak,
-                         "peak_tflops": peak, "peak_source": peak_kind,
+                         "peak_tflops": peak, "peak_source": f"{peak_kind} {peak_name}",
                          "nominal_2250": value / world / 2250.0},
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "host_chunks": args.host_chunks or "library default"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
     }
+    if args.workload == "c4" and not args.no_c5:
+        result["c5_fwd"] = long_context_leg(args, dev, dist, peaks, peak_kind)
     if has_bwd:
         result["bwd_ms"] = {"preprocess": pre_ms, "dkdv": dkdv_ms, "dq": dq_ms}
         result["bwd_tflops"] = F_bwd / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12
         result["mfu_style_tflops"] = 3 * F_fwd * world / (ms_per_step * 1e-3) / 1e12
     if rank == 0 and not args.no_cpu_baseline:
         heads = [(0, 0)]
-        dt, fl = oracle_sample(w, q, k, v, do, heads)
+        dt, fl, first = oracle_sample(w, q, k, v, do, heads, keep_first=True)
         reps = 1
         while dt * reps < 10.0 and reps < 8:
             dt2, _ = oracle_sample(w, q, k, v, do, [(0, reps % w.H)])
             dt += dt2
             reps += 1
+        gpu_out = {"o": o, "lse": lse}
+        if has_bwd:
+            gpu_out.update({"dq": dq, "dk": dk, "dv": dv})
         result["cpu_baseline"] = {
             "value": fl * reps / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{reps} head(s) of {args.workload} forward{'+backward' if has_bwd else ''}, "
-                      f"fp64 NumPy oracle, {dt:.1f} s"}
+                      f"fp64 NumPy oracle, {dt:.1f} s",
+            "error_vs_gpu": {"head": "b=0 h=0 (the GPU's outputs of the last timed step)",
+                             **oracle_errors(first, gpu_out, 0, 0, w.H // w.kv_heads)}}
     return result
 
 
@@ -745,6 +853,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-c5", action="store_true",
+                    help="skip the long-context forward leg of the default (c4) run")
     ap.add_argument("--host-chunks", type=int, default=0,
                     help="slices of the end-to-end host pipeline (0: the library's choice)")
     args = ap.parse_args()

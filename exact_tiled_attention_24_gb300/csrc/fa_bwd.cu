@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
 // ------------------------------------------------------- shared helpers
 
 constexpr int TILE = 128;       // rows of every K, V, Q, dO tile
-constexpr int HEAD_GROUP = 4;   // heads whose tiles are scheduled together
+constexpr int MAX_HEAD_GROUP = 4;   // most heads whose tiles are scheduled together
 constexpr int SWEEP_THREADS = 320;  // 10 warps: TMA, MMA, 8 compute
 
 template <int D>
@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tdk,
                     const __grid_constant__ CUtensorMap tdv, const float* __restrict__ lse,
-                    const float* __restrict__ Dvec, int BHkv, int G, int N, float scale, float scale_log2) {
+                    const float* __restrict__ Dvec, int BHkv, int G, int N, int head_group, float scale,
+                    float scale_log2) {
   using L = DkdvSmem<D>;
   using T = Tiles<D>;
   constexpr int QST = L::QST;
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int n_t = (N + TILE - 1) / TILE;
   int kt, bkv;  // causal: heaviest key tile (kt = 0) first within each head group
-  grouped_tile_order(static_cast<int>(blockIdx.x), BHkv, n_t, HEAD_GROUP, &kt, &bkv);
+  grouped_tile_order(static_cast<int>(blockIdx.x), BHkv, n_t, head_group, &kt, &bkv);
   const int k0 = kt * TILE;
   const int qt_begin = CAUSAL ? kt : 0;  // first query tile with a visible pair
   const int n_q = n_t - qt_begin;        // query tiles swept per query head
@@ -516,7 +517,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdq, const float* __restrict__ lse,
-                  const float* __restrict__ Dvec, int BH, int G, int N, float scale, float scale_log2) {
+                  const float* __restrict__ Dvec, int BH, int G, int N, int head_group, float scale,
+                  float scale_log2) {
   using L = DqSmem<D>;
   using T = Tiles<D>;
   constexpr int KST = L::KST;
@@ -547,7 +549,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int n_t = (N + TILE - 1) / TILE;
   int t, bh;  // causal: heaviest query tile (the last one) first within each head group
-  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_t, HEAD_GROUP, &t, &bh);
+  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_t, head_group, &t, &bh);
   const int qt = n_t - 1 - t;
   const int q0 = qt * TILE;
   const int bkv = bh / G;  // K/V head shared by G consecutive query heads
@@ -806,7 +808,9 @@ static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   if (e != cudaSuccess) return e;
   const int n_t = (N + TILE - 1) / TILE;
   dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BHkv));
-  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BHkv, G, N, scale,
+  // A K/V head's CTAs re-read Q and dO of its G query heads (4·N·D·G bytes).
+  const int group = head_group_for(4ll * N * D * G, MAX_HEAD_GROUP);
+  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, BHkv, G, N, group, scale,
                                                scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
@@ -821,7 +825,9 @@ static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, con
   if (e != cudaSuccess) return e;
   const int n_t = (N + TILE - 1) / TILE;
   dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BH));
-  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale,
+  // A query head's CTAs re-read K and V of its K/V head, shared by G heads.
+  const int group = head_group_for(4ll * N * D / G, MAX_HEAD_GROUP);
+  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, group, scale,
                                                scale * 1.4426950408889634f);
   return cudaGetLastError();
 }

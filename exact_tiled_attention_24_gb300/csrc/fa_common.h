@@ -9,6 +9,18 @@
 
 namespace fa {
 
+// Heads whose tiles are scheduled together: the CTAs resident at one time
+// then re-read one group's shared operand (K and V in the forward and the
+// dQ sweep, Q and dO in the dK/dV sweep), and the group is sized so that
+// operand stays in L2 (about 40 MB of the 129 MB). `bytes_per_head` is the
+// shared operand's size per scheduled head.
+constexpr long long kL2GroupBytes = 40ll << 20;
+inline int head_group_for(long long bytes_per_head, int max_group) {
+  long long g = bytes_per_head > 0 ? kL2GroupBytes / bytes_per_head : max_group;
+  if (g > max_group) g = max_group;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
 // Kernel launchers. Pointers are device pointers to contiguous [BH][N][d]
 // bf16 tensors (lse, Dvec: [BH][N] fp32); k, v, dk and dv hold BH / G heads,
 // query head h reading K/V head h / G (G = 1: one K/V head per query head).

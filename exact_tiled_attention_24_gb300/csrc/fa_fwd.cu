@@ -48,7 +48,7 @@ namespace fwd {
 constexpr int BM = 128;       // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;       // keys per tile
 constexpr int THREADS = 320;  // 10 warps
-constexpr int HEAD_GROUP = 8;
+constexpr int MAX_HEAD_GROUP = 8;
 constexpr float RESCALE_LOG2 = 8.f;
 
 template <int D>
@@ -75,7 +75,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                  float* __restrict__ lse, int BH, int G, int N, float scale_log2) {
+                  float* __restrict__ lse, int BH, int G, int N, int head_group, float scale_log2) {
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -102,11 +102,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Heads in groups of HEAD_GROUP (their K/V stay in L2 while the group
-  // runs); within a group the heaviest (causal) query blocks go first.
+  // Heads in groups of head_group (sized so that their K/V stay in L2 while
+  // the group runs); within a group the heaviest (causal) query blocks go
+  // first.
   const int n_qb = (N + 2 * BM - 1) / (2 * BM);  // blocks of two query tiles
   int t, bh;
-  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_qb, HEAD_GROUP, &t, &bh);
+  grouped_tile_order(static_cast<int>(blockIdx.x), BH, n_qb, head_group, &t, &bh);
   const int qb = n_qb - 1 - t;
   const int bkv = bh / G;  // K/V head shared by G consecutive query heads
   const int qrow0 = qb * 2 * BM;
@@ -437,7 +438,9 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
   const int n_qb = (N + 2 * BM - 1) / (2 * BM);
   dim3 grid(static_cast<unsigned>(n_qb) * static_cast<unsigned>(BH));
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, to, lse, BH, G, N, scale_log2);
+  // K and V of one K/V head (4·N·D bytes) serve G query heads.
+  const int group = head_group_for(4ll * N * D / G, MAX_HEAD_GROUP);
+  kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, to, lse, BH, G, N, group, scale_log2);
   return cudaGetLastError();
 }
 

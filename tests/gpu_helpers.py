@@ -11,6 +11,16 @@ TOL_O_MAX = 2e-2
 TOL_O_MEAN = 2e-3
 TOL_LSE = 1e-3
 TOL_GRAD = 5e-2
+# Gradients larger than unit scale (scores far from unit variance): the
+# bf16 path's error grows with the gradients themselves. Every product
+# operand is bf16 (8 significant bits, unit roundoff u = 2^-9), and each
+# gradient's chain carries at most three roundings (the stored O inside D,
+# P or dS, the operand), each of relative size u against the terms it
+# rounds; with fp32 sums on top, 8u = 2^-6 of the largest reference entry
+# bounds them. This equals the fixed bound at a largest entry of 3.2 and
+# widens it only above; the five benchmark configurations are held to the
+# fixed bound itself (their largest entries are 1.5 to 5.4).
+TOL_GRAD_REL = 2.0 ** -6
 
 
 def errs(got, ref):
@@ -33,3 +43,15 @@ def assert_lse(got, ref):
 def assert_grad(got, ref, what):
     mx, _ = errs(got, ref)
     assert mx <= TOL_GRAD, f"{what}: max-abs {mx}"
+
+
+def grad_bound(ref):
+    """The gradient bound for one tensor: the fixed bound, or 2^-6 of the
+    tensor's largest reference entry where that is larger."""
+    return max(TOL_GRAD, TOL_GRAD_REL * float(np.abs(ref).max()))
+
+
+def assert_grad_scaled(got, ref, what):
+    mx, _ = errs(got, ref)
+    bound = grad_bound(ref)
+    assert mx <= bound, f"{what}: max-abs {mx} > {bound} (max |ref| {float(np.abs(ref).max())})"

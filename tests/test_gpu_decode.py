@@ -101,7 +101,7 @@ def test_merge_vs_oracle(fa, S, rows, d):
     o, lse = fa.attn_merge(o_parts.cuda(), lse_parts.cuda())
     torch.cuda.synchronize()
     ro, rlse = attention_merge(o_parts.double().numpy(), lse_parts.double().numpy())
-    np.testing.assert_allclose(o.float().cpu().numpy(), ro, rtol=1e-2, atol=1e-2)
+    assert_o(o, ro, "merged o")
     fin = np.isfinite(rlse)
     np.testing.assert_allclose(lse.cpu().numpy()[fin], rlse[fin], rtol=0, atol=1e-4)
     assert np.all(np.isneginf(lse.cpu().numpy()[~fin]))
