@@ -24,6 +24,7 @@ __all__ = [
     "bwd_dq",
     "bwd_workspace_bytes",
     "last_device_error",
+    "debug_checks",
     "softmax_safe",
     "softmax_online",
     "attn_merge",
@@ -36,7 +37,10 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "_lib", "libfa.so")
+# FA_DEBUG_LIBRARY=1 selects the bounds-checked build (libfa_debug.so, made
+# by build.build(debug=True)); it computes the same results.
+_LIB_PATH = os.path.join(_HERE, "_lib",
+                         "libfa_debug.so" if os.environ.get("FA_DEBUG_LIBRARY") == "1" else "libfa.so")
 _lib = None
 
 FA_STATUS = {
@@ -48,6 +52,7 @@ FA_STATUS = {
     5: "FA_ERR_TIMEOUT",
     6: "FA_ERR_WORKSPACE",
     7: "FA_ERR_BAD_INDEX",
+    8: "FA_ERR_BOUNDS",
 }
 
 EXPORTED_SYMBOLS = (
@@ -72,6 +77,7 @@ EXPORTED_SYMBOLS = (
     "fa_fwd_host",
     "fa_fwd_bwd_host",
     "fa_softmax_host",
+    "fa_debug_checks",
 )
 
 
@@ -141,6 +147,8 @@ def lib() -> ctypes.CDLL:
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_version.argtypes = []
         L.fa_version.restype = ctypes.c_char_p
+        L.fa_debug_checks.argtypes = []
+        L.fa_debug_checks.restype = i
         _lib = L
     return _lib
 
@@ -296,6 +304,11 @@ def selftest_wait_limit(device=None) -> None:
     last_device_error() returns 5 (FA_ERR_TIMEOUT)."""
     dev = torch.device("cuda") if device is None else device
     _check(lib().fa_selftest_wait_limit(_stream(dev)), "fa_selftest_wait_limit")
+
+
+def debug_checks() -> bool:
+    """True when the loaded library is the bounds-checked FA_DEBUG build."""
+    return bool(lib().fa_debug_checks())
 
 
 def last_device_error(device=None) -> int:

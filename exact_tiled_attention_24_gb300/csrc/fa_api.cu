@@ -44,6 +44,14 @@ extern "C" {
 
 const char* fa_version(void) { return "0.1.0"; }
 
+int fa_debug_checks(void) {
+#ifdef FA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
@@ -54,6 +62,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
     case FA_ERR_BAD_INDEX: return "FA_ERR_BAD_INDEX";
+    case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS";
     default: return "FA_ERR_UNKNOWN";
   }
 }
@@ -253,14 +262,16 @@ int fa_selftest_wait_limit(void* stream) {
 
 int fa_last_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t ef = 0, eb = 0, ed = 0, et = 0;
+  uint32_t ef = 0, eb = 0, ed = 0, et = 0, es = 0;
   if (fa::read_and_clear_fwd_error(&ef, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_and_clear_bwd_error(&eb, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_and_clear_decode_error(&ed, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_and_clear_selftest_error(&et, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::read_and_clear_softmax_error(&es, s) != cudaSuccess) return FA_ERR_CUDA;
   if (ef == 1 || eb == 1 || ed == 1 || et == 1) return FA_ERR_TIMEOUT;
+  if (ef == 3 || eb == 3 || ed == 3 || es == 3) return FA_ERR_BOUNDS;
   if (ed == 2) return FA_ERR_BAD_INDEX;
-  if (ef || eb || ed || et) return FA_ERR_TIMEOUT;
+  if (ef || eb || ed || et || es) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
 

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   const long long row = static_cast<long long>(blockIdx.x) * RPB + threadIdx.x / TPR;
   const int part = threadIdx.x % TPR;
   float acc = 0.f;
-  if (row < rows) {
+  if (row < rows && in_range(static_cast<long long>(row) * D + part * 8, 8, rows * D, &g_bwd_err)) {
     const size_t off = static_cast<size_t>(row) * D + part * 8;
     const uint4 a = *reinterpret_cast<const uint4*>(o + off);
     const uint4 b = *reinterpret_cast<const uint4*>(dO + off);
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   }
 #pragma unroll
   for (int w = TPR / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-  if (row < rows && part == 0) Dvec[row] = acc;
+  if (row < rows && part == 0 && in_range(row, 1, rows, &g_bwd_err)) Dvec[row] = acc;
 }
 
 // ------------------------------------------------------- shared helpers
@@ -90,10 +90,10 @@ struct Tiles {
 
 // Stage columns [c_begin, c_begin + NCOLS) of a [128 rows] fp32 tile held in
 // TMEM (lane = row) as bf16, times `mul`, into a swizzled shared-memory tile
-// (panels of 64 columns) ready for a TMA store.
+// (panels of 64 columns, dst_bytes in all) ready for a TMA store.
 template <int NCOLS>
 __device__ __forceinline__ void stage_tmem_rows_bf16(uint32_t taddr, uint8_t* dst, int r, int c_begin,
-                                                     float mul) {
+                                                     float mul, int dst_bytes, uint32_t* err) {
 #pragma unroll
   for (int cc = 0; cc < NCOLS; cc += 32) {
     const int c = c_begin + cc;
@@ -110,7 +110,8 @@ __device__ __forceinline__ void stage_tmem_rows_bf16(uint32_t taddr, uint8_t* ds
       v.y = pack_bf16x2(__uint_as_float(a[ch * 8 + 2]) * mul, __uint_as_float(a[ch * 8 + 3]) * mul);
       v.z = pack_bf16x2(__uint_as_float(a[ch * 8 + 4]) * mul, __uint_as_float(a[ch * 8 + 5]) * mul);
       v.w = pack_bf16x2(__uint_as_float(a[ch * 8 + 6]) * mul, __uint_as_float(a[ch * 8 + 7]) * mul);
-      *reinterpret_cast<uint4*>(dst + panel * (TILE * 128) + r * 128 + ((chunk ^ (r & 7)) * 16)) = v;
+      const int off = panel * (TILE * 128) + r * 128 + ((chunk ^ (r & 7)) * 16);
+      if (in_range(off, 16, dst_bytes, err)) *reinterpret_cast<uint4*>(dst + off) = v;
     }
   }
 }
@@ -363,15 +364,17 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     // Stored negated (−lse·log2 e, −D) so that the packed pair arithmetic
     // below adds them; the products are the same as subtracting.
     const float stat_mul = ct < 128 ? -LOG2E : -1.f;
+    const long long n_rows = static_cast<long long>(BHkv) * G * N;  // lse and D entries
     auto load_stat = [&](int tile) -> float {
       if (tile >= n_it) return ct < 128 ? INFINITY : 0.f;
       const int gq = tile / n_q;
       const int q = (qt_begin + tile - gq * n_q) * TILE + (ct & 127);
       const size_t row = static_cast<size_t>(bkv * G + gq) * N + q;
-      if (ct < 128) return q < N ? lse[row] : INFINITY;
-      return q < N ? Dvec[row] : 0.f;
+      const bool live = q < N && in_range(static_cast<long long>(row), 1, n_rows, err);
+      if (ct < 128) return live ? lse[row] : INFINITY;
+      return live ? Dvec[row] : 0.f;
     };
-    sStat[ct] = load_stat(0) * stat_mul;  // buffer 0: lse[0..127], D[128..255]
+    if (in_range(ct, 1, 512, err)) sStat[ct] = load_stat(0) * stat_mul;  // buffer 0: lse[0..127], D[128..255]
     float stat_nx = load_stat(1);
     named_bar_sync(1, 256);
     bool ok = true;
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       if (lane == 0) mbar_arrive(ds_ready);
       // Next tile's (lse, D) into the other buffer; its previous readers
       // passed the barrier at the end of the previous iteration.
-      sStat[((i + 1) & 1) * 256 + ct] = stat_nx * stat_mul;
+      if (in_range(((i + 1) & 1) * 256 + ct, 1, 512, err)) sStat[((i + 1) & 1) * 256 + ct] = stat_nx * stat_mul;
       stat_nx = load_stat(i + 2);
       named_bar_sync(1, 256);
     }
@@ -466,8 +469,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     if (ok) ok = mbar_wait(final_bar, 0, err);
     if (ok) {
       tc_fence_after();
-      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + KV_COL_DK, sQ, r, half * (D / 2), scale);
-      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + KV_COL_DV, sdO, r, half * (D / 2), 1.f);
+      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + KV_COL_DK, sQ, r, half * (D / 2), scale, T::BYTES, err);
+      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + KV_COL_DV, sdO, r, half * (D / 2), 1.f, T::BYTES, err);
       fence_async_smem();
     }
     named_bar_sync(1, 256);
@@ -683,8 +686,9 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     const int q = q0 + r;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr float LOG2E = 1.4426950408889634f;
-    const float lse2 = (q < N) ? lse[static_cast<size_t>(bh) * N + q] * LOG2E : 0.f;
-    const float Dq = (q < N) ? Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
+    const bool q_live = q < N && in_range(static_cast<long long>(bh) * N + q, 1, static_cast<long long>(BH) * N, err);
+    const float lse2 = q_live ? lse[static_cast<size_t>(bh) * N + q] * LOG2E : 0.f;
+    const float Dq = q_live ? Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
     bool ok = mbar_wait(q_full, 0, err);
     if (ok) {
       // Copy this row of Q (half 0) or dO (half 1) into TMEM as bf16 pairs:
@@ -698,8 +702,9 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         for (int ch = 0; ch < 4; ++ch) {
           const int chunk = c16 / 4 + ch;  // 16-byte chunk = 8 elements = 4 columns
           const int panel = chunk / 8;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + panel * T::PANEL + r * 128 +
-                                                          (((chunk % 8) ^ (r & 7)) * 16));
+          const int off = panel * T::PANEL + r * 128 + (((chunk % 8) ^ (r & 7)) * 16);
+          const uint4 v = in_range(off, 16, T::BYTES, err) ? *reinterpret_cast<const uint4*>(src + off)
+                                                           : make_uint4(0u, 0u, 0u, 0u);
           w[ch * 4 + 0] = v.x;
           w[ch * 4 + 1] = v.y;
           w[ch * 4 + 2] = v.z;
@@ -779,7 +784,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     if (ok) ok = mbar_wait(final_bar, 0, err);
     if (ok) {
       tc_fence_after();
-      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + Q_COL_DQ, sQ, r, half * (D / 2), scale);
+      stage_tmem_rows_bf16<D / 2>(tmem + lane_addr + Q_COL_DQ, sQ, r, half * (D / 2), scale, T::BYTES, err);
       fence_async_smem();
     }
     named_bar_sync(1, 256);

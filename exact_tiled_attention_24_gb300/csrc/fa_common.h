@@ -71,5 +71,6 @@ cudaError_t read_and_clear_selftest_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_fwd_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream);
 cudaError_t read_and_clear_decode_error(uint32_t* out, cudaStream_t stream);
+cudaError_t read_and_clear_softmax_error(uint32_t* out, cudaStream_t stream);
 
 }  // namespace fa

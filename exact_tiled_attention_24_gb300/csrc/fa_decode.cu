@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
   uint32_t* err = &g_dec_err;
 
   // Context of request b, clamped to what its block-table row can address.
-  int Lb = seq_lens[b];
+  int Lb = in_range(b, 1, B, err) ? seq_lens[b] : 0;
   Lb = Lb < 0 ? 0 : (Lb > max_blocks * bs ? max_blocks * bs : Lb);
   const int n_tiles = (Lb + TK - 1) / TK;
   const int tps = (n_tiles + S - 1) / S;  // tiles per split
@@ -135,9 +135,11 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
   const int tile1 = min(n_tiles, tile0 + tps);
   const size_t head0 = static_cast<size_t>(b) * H + static_cast<size_t>(hk) * G_all + 16 * chunk;  // first query head
   const size_t prow = static_cast<size_t>(s) * B * H + head0;                     // its partial row
+  const long long part_rows = static_cast<long long>(S) * B * H;  // rows of o_part and lse_part
   if (tile0 >= tile1) {  // no key in this split: o_s = 0, lse_s = -inf (weight 0 in the merge)
-    for (int i = tid; i < G * D; i += THREADS) o_part[prow * D + i] = 0.f;
-    if (tid < G) lse_part[prow + tid] = -INFINITY;
+    for (int i = tid; i < G * D; i += THREADS)
+      if (in_range(static_cast<long long>(prow) * D + i, 1, part_rows * D, err)) o_part[prow * D + i] = 0.f;
+    if (tid < G && in_range(static_cast<long long>(prow) + tid, 1, part_rows, err)) lse_part[prow + tid] = -INFINITY;
     return;
   }
   const int t_begin = tile0 * TK, t_end = min(Lb, tile1 * TK);
@@ -154,9 +156,16 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
 
   for (int i = tid; i < GM * D; i += THREADS) {
     const int g = i / D;
-    sQ[i] = g < G ? __bfloat162float(q[(head0 + g) * D + (i % D)]) * scale_log2 : 0.f;
+    const long long qi = static_cast<long long>(head0 + g) * D + (i % D);
+    sQ[i] = g < G && in_range(qi, 1, static_cast<long long>(B) * H * D, err)
+                ? __bfloat162float(q[qi]) * scale_log2
+                : 0.f;
   }
-  for (int i = tid; i < nblk; i += THREADS) sTab[i] = block_table[static_cast<size_t>(b) * max_blocks + blk0 + i];
+  for (int i = tid; i < nblk; i += THREADS) {
+    const long long ti = static_cast<long long>(b) * max_blocks + blk0 + i;
+    if (in_range(i, 1, kDecodeMaxTable, err))
+      sTab[i] = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
+  }
   if (lane == 0) {
     for (int st = 0; st < NST; ++st) {
       fills[st * WARPS] = 0;
@@ -168,9 +177,18 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
 
   // One warp: copy its 8 keys of tile `tile` (K rows, then V rows) into its
   // slot of stage st. Lane r takes the r-th run of consecutive tokens inside
-  // one cache block. Entries outside [0, num_blocks) are skipped (their rows
-  // keep old bytes, masked later) and reported; only copied bytes are expected.
+  // one cache block. Entries outside [0, num_blocks) are never dereferenced:
+  // their copies are skipped and the error is reported, and their rows of the
+  // slot keep stale bytes, so the results of that request are undefined.
+  // Only copied bytes are expected on the barrier.
   const bool single_run = (bs & 7) == 0;  // a warp's 8 keys never cross a block boundary
+  const long long cache_elems = static_cast<long long>(num_blocks) * Hkv * bs * D;
+  // Table entry blk may be read for rows [row0, row0 + nrows) of head hk.
+  auto copy_ok = [&](int blk, int row0, int nrows) {
+    return blk >= 0 && blk < num_blocks &&
+           in_range((static_cast<long long>(blk) * Hkv + hk) * bs * D + static_cast<long long>(row0) * D,
+                    static_cast<long long>(nrows) * D, cache_elems, err);
+  };
   auto issue = [&](int tile, int st) {
     const int t0 = tile * TK + warp * 8, t1 = min(t_end, t0 + 8);
     if (single_run) {  // lane 0 alone: one table entry, two copies
@@ -181,8 +199,8 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
         if (t0 < t1) {
           const int bi = t0 / bs;  // the only division per tile
           off = t0 - bi * bs;
-          blk = sTab[bi - blk0];
-          if (blk >= 0 && blk < num_blocks) nbytes = static_cast<uint32_t>(t1 - t0) * L::ROW;
+          blk = in_range(bi - blk0, 1, nblk, err) ? sTab[bi - blk0] : -1;
+          if (copy_ok(blk, off, t1 - t0)) nbytes = static_cast<uint32_t>(t1 - t0) * L::ROW;
           else atomicExch(err, DEV_BAD_INDEX);
         }
         mbar_arrive_expect_tx(&full[st * WARPS], 2 * nbytes);
@@ -200,9 +218,9 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
     const int nrun = t0 < t1 ? (t1 - 1) / bs - b0 + 1 : 0;
     uint32_t bytes = 0;
     for (int r = lane; r < nrun; r += 32) {
-      const int blk = sTab[b0 + r - blk0];
+      const int blk = in_range(b0 + r - blk0, 1, nblk, err) ? sTab[b0 + r - blk0] : -1;
       const int rs = max(t0, (b0 + r) * bs), re = min(t1, (b0 + r + 1) * bs);
-      if (blk >= 0 && blk < num_blocks) bytes += static_cast<uint32_t>(re - rs) * L::ROW;
+      if (copy_ok(blk, rs - (b0 + r) * bs, re - rs)) bytes += static_cast<uint32_t>(re - rs) * L::ROW;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
@@ -213,9 +231,9 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
     __syncwarp();
     uint8_t* slot = sSlot + st * WARPS * L::WSLOT;
     for (int r = lane; r < nrun; r += 32) {
-      const int blk = sTab[b0 + r - blk0];
+      const int blk = in_range(b0 + r - blk0, 1, nblk, err) ? sTab[b0 + r - blk0] : -1;
       const int rs = max(t0, (b0 + r) * bs), re = min(t1, (b0 + r + 1) * bs);
-      if (blk >= 0 && blk < num_blocks) {
+      if (copy_ok(blk, rs - (b0 + r) * bs, re - rs)) {
         const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + (rs - (b0 + r) * bs)) * D;
         const uint32_t dst = static_cast<uint32_t>(rs - t0) * L::ROW;
         const uint32_t nbytes = static_cast<uint32_t>(re - rs) * L::ROW;
@@ -419,8 +437,9 @@ __global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial
       Ls += sML[(w * 2 + 1) * GM + g] * f;
       u += sAcc[(w * GM + g) * D + c] * f;
     }
-    o_part[(prow + g) * D + c] = u / Ls;
-    if (c == 0) lse_part[prow + g] = (M + __log2f(Ls)) * LN2;
+    if (in_range(static_cast<long long>(prow + g) * D + c, 1, part_rows * D, err)) o_part[(prow + g) * D + c] = u / Ls;
+    if (c == 0 && in_range(static_cast<long long>(prow) + g, 1, part_rows, err))
+      lse_part[prow + g] = (M + __log2f(Ls)) * LN2;
   }
 }
 
@@ -434,8 +453,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  uint32_t* err = &g_dec_err;
+  const long long prt = static_cast<long long>(S) * rows;  // rows of the partial results
   float m = -INFINITY;
-  for (int s = lane; s < S; s += 32) m = fmaxf(m, lse_parts[s * rows + row]);
+  for (int s = lane; s < S; s += 32)
+    if (in_range(s * rows + row, 1, prt, err)) m = fmaxf(m, lse_parts[s * rows + row]);
   m = warp_max(m);
   float l = 0.f;
   float acc[CPL];
@@ -443,6 +465,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
   for (int j = 0; j < CPL; ++j) acc[j] = 0.f;
   if (m != -INFINITY) {
     for (int s = 0; s < S; ++s) {
+      if (!in_range((s * rows + row) * D + lane * CPL, CPL, prt * D, err)) continue;
       const float w = ex2((lse_parts[s * rows + row] - m) * LOG2E);
       l += w;
       const float* src = o_parts + (s * rows + row) * D + lane * CPL;
@@ -453,9 +476,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int j = 0; j < CPL; j += 2)
-    *reinterpret_cast<__nv_bfloat162*>(o + row * D + lane * CPL + j) =
-        __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
-  if (lane == 0) lse[row] = l > 0.f ? m + __logf(l) : -INFINITY;
+    if (in_range(row * D + lane * CPL + j, 2, rows * D, err))
+      *reinterpret_cast<__nv_bfloat162*>(o + row * D + lane * CPL + j) =
+          __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+  if (lane == 0 && in_range(row, 1, rows, err)) lse[row] = l > 0.f ? m + __logf(l) : -INFINITY;
 }
 
 template <int D, int GM>

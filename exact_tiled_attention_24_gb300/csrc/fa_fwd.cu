@@ -403,12 +403,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           val.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * inv_l, __uint_as_float(o[ch * 8 + 3]) * inv_l);
           val.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * inv_l, __uint_as_float(o[ch * 8 + 5]) * inv_l);
           val.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * inv_l, __uint_as_float(o[ch * 8 + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(stage + panel * L::PANEL + r * 128 + ((chunk ^ (r & 7)) * 16)) = val;
+          const int off = g * L::TILE_BYTES + panel * L::PANEL + r * 128 + ((chunk ^ (r & 7)) * 16);
+          if (in_range(off, 16, 2 * L::TILE_BYTES, err))  // the Q0, Q1 region
+            *reinterpret_cast<uint4*>(sQ + off) = val;
         }
       }
-      if (qrow < N) {
+      const long long lrow = static_cast<long long>(bh) * N + qrow;
+      if (qrow < N && in_range(lrow, 1, static_cast<long long>(BH) * N, err)) {
         // lse in natural-log units: (m + log2 l) * ln 2
-        lse[static_cast<size_t>(bh) * N + qrow] = (m + __log2f(l)) * 0.69314718055994531f;
+        lse[lrow] = (m + __log2f(l)) * 0.69314718055994531f;
       }
       fence_async_smem();
     }

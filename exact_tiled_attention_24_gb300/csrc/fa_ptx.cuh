@@ -14,7 +14,26 @@
 namespace fa {
 
 // Error word values written by device code (host maps them to fa_status).
-enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
+enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2, DEV_BOUNDS = 3 };
+
+// Bounds checks of the FA_DEBUG build. Every address a kernel computes
+// itself (TMA tensor copies are bounded by their tensor maps) is checked
+// against the extent of the buffer it falls in: [off, off + len) must lie in
+// [0, count). A failed check records DEV_BOUNDS in the kernel's error word
+// and the caller skips the access; nothing traps. Release builds compile
+// the checks away (in_range is constant true).
+#ifdef FA_DEBUG
+constexpr bool kBoundsChecks = true;
+#else
+constexpr bool kBoundsChecks = false;
+#endif
+
+__device__ __forceinline__ bool in_range(long long off, long long len, long long count, uint32_t* err) {
+  if (!kBoundsChecks) return true;
+  if (off >= 0 && len >= 0 && off + len <= count) return true;
+  atomicExch(err, DEV_BOUNDS);
+  return false;
+}
 
 // Upper bound on any single mbarrier wait, in nanoseconds of %globaltimer.
 // No wait in these kernels legitimately takes more than microseconds.

@@ -25,6 +25,9 @@
 #include "fa_ptx.cuh"
 
 namespace fa {
+
+static __device__ uint32_t g_smx_err;
+
 namespace sm {
 
 constexpr int THREADS = 512;
@@ -136,13 +139,22 @@ struct Row<1> {
   }
 };
 
+// Element i (in units of U floats) of row `row` lies inside the [rows][n]
+// array (rows = the grid). Constant true outside the FA_DEBUG build.
+template <int U>
+__device__ __forceinline__ bool in_rows(long long row, int n, long long i) {
+  return in_range(row * n + i * U, U, static_cast<long long>(gridDim.x) * n, &g_smx_err);
+}
+
 // Final pass, shared by both forms: y = e^(x − m) / l.
 template <int U>
-__device__ __forceinline__ void write_pass(const float* xr, float* yr, long long nv, float m, float l) {
+__device__ __forceinline__ void write_pass(const float* xr, float* yr, long long row, int n, long long nv,
+                                           float m, float l) {
   using R = Row<U>;
   const float inv = 1.f / l;
 #pragma unroll 4
-  for (long long i = threadIdx.x; i < nv; i += THREADS) R::store(yr, i, R::vnorm(R::load(xr, i), m, inv));
+  for (long long i = threadIdx.x; i < nv; i += THREADS)
+    if (in_rows<U>(row, n, i)) R::store(yr, i, R::vnorm(R::load(xr, i), m, inv));
 }
 
 // Three passes: maximum, denominator, output.
@@ -156,13 +168,15 @@ __global__ void __launch_bounds__(THREADS) softmax_safe_kernel(const float* x, f
   const long long nv = n / U;
   float m = -INFINITY;
 #pragma unroll 4
-  for (long long i = threadIdx.x; i < nv; i += THREADS) m = fmaxf(m, R::vmax(R::load(xr, i)));
+  for (long long i = threadIdx.x; i < nv; i += THREADS)
+    if (in_rows<U>(row, n, i)) m = fmaxf(m, R::vmax(R::load(xr, i)));
   m = block_max(m, red);
   float l = 0.f;
 #pragma unroll 4
-  for (long long i = threadIdx.x; i < nv; i += THREADS) l += R::vexpsum(R::load(xr, i), m);
+  for (long long i = threadIdx.x; i < nv; i += THREADS)
+    if (in_rows<U>(row, n, i)) l += R::vexpsum(R::load(xr, i), m);
   l = block_sum(l, red);
-  write_pass<U>(xr, yr, nv, m, l);
+  write_pass<U>(xr, yr, row, n, nv, m, l);
 }
 
 // Two passes: maximum and denominator together (rescaling l when the
@@ -178,6 +192,7 @@ __global__ void __launch_bounds__(THREADS) softmax_online_kernel(const float* x,
   float m = -INFINITY, l = 0.f;
 #pragma unroll 4
   for (long long i = threadIdx.x; i < nv; i += THREADS) {
+    if (!in_rows<U>(row, n, i)) continue;
     const typename R::T v = R::load(xr, i);
     const float mn = fmaxf(m, R::vmax(v));
     if (mn == -INFINITY) continue;  // nothing but -inf so far
@@ -185,10 +200,22 @@ __global__ void __launch_bounds__(THREADS) softmax_online_kernel(const float* x,
     m = mn;
   }
   block_merge_ml(m, l, red);
-  write_pass<U>(xr, yr, nv, m, l);
+  write_pass<U>(xr, yr, row, n, nv, m, l);
 }
 
 }  // namespace sm
+
+cudaError_t read_and_clear_softmax_error(uint32_t* out, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_smx_err, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost,
+                                            stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  const uint32_t zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_smx_err, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
 
 cudaError_t launch_softmax(const float* x, float* y, long long rows, int n, bool online,
                            cudaStream_t stream) {

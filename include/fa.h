@@ -40,6 +40,10 @@
  *             limit) are reported by fa_last_device_error.
  *   Threads   entry points may be called from several host threads; each
  *             call works on its own descriptors.
+ *   Devices   per-device state the library keeps (its side streams, the
+ *             scratch address of fa_bwd_noalloc) lives as long as the
+ *             process; after cudaDeviceReset on a device, do not call into
+ *             the library on that device again in the same process.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -58,7 +62,8 @@ typedef enum {
   FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch error) */
   FA_ERR_TIMEOUT = 5,     /* device pipeline wait exceeded its limit */
   FA_ERR_WORKSPACE = 6,   /* workspace pointer null or smaller than required */
-  FA_ERR_BAD_INDEX = 7    /* (device) a block-table entry outside [0, num_blocks) */
+  FA_ERR_BAD_INDEX = 7,   /* (device) a block-table entry outside [0, num_blocks) */
+  FA_ERR_BOUNDS = 8       /* (device, FA_DEBUG build) a computed address left its buffer */
 } fa_status;
 
 /*
@@ -222,7 +227,11 @@ int fa_fwd_bwd_host(const fa_tensors* host, const fa_tensors* dev, void* workspa
  *     (B*H*N*4 bytes: up to 8,388,608 query rows over all heads).
  *   - The first call on a device looks up the array's device address with
  *     that device current (a one-time set-up per device); make that first
- *     call before any stream capture.
+ *     call before any stream capture. The address is kept for the life of
+ *     the process: after cudaDeviceReset (or any teardown of the device's
+ *     primary context) the library's per-device state, this address
+ *     included, is stale, so do not call into the library on that device
+ *     again in the same process.
  *   - Every call on a device shares the one array. Calls whose kernels
  *     overlap on the GPU (different streams or host threads without
  *     ordering between them) race on it and give undefined results; order
@@ -333,7 +342,9 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
  * Synchronises `stream`, then reads and clears the device error word set by
  * any kernel of this library on the current device. Returns FA_OK,
  * FA_ERR_TIMEOUT (a pipeline wait gave up; outputs of the calls since the
- * last check are undefined), FA_ERR_BAD_INDEX (a decode block table pointed
+ * last check are undefined), FA_ERR_BOUNDS (FA_DEBUG build only: an address
+ * a kernel computed fell outside its buffer; that access was skipped and the
+ * outputs are undefined), FA_ERR_BAD_INDEX (a decode block table pointed
  * outside the cache) or FA_ERR_CUDA.
  */
 int fa_last_device_error(void* stream);
@@ -353,6 +364,18 @@ const char* fa_status_string(int status);
 
 /* Library version, e.g. "0.1.0". */
 const char* fa_version(void);
+
+/*
+ * 1 when this library is the FA_DEBUG build (libfa_debug.so), else 0. That
+ * build checks every address the kernels compute themselves (all global
+ * loads and stores other than TMA tensor copies, the decode kernel's bulk
+ * copies, and the shared-memory staging of outputs) against the extent of
+ * its buffer; a failed check skips the access and records FA_ERR_BOUNDS for
+ * fa_last_device_error. No check traps. It stands in for a memory checker:
+ * results on valid inputs equal the release build's bit for bit.
+ * Pure host function; needs no GPU.
+ */
+int fa_debug_checks(void);
 
 #ifdef __cplusplus
 }
