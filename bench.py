@@ -822,9 +822,9 @@ def run_decode(args, dw, rank, world, dist):
                                f"block={dw.block_size} context {dw.min_len}-{dw.max_len} "
                                f"(total {tokens} tokens) splits={dw.n_splits}",
                    "l2": "K/V %d MB read per step vs 129 MB L2; no flush" % (kv_bytes // 2**20)},
-        "roofline": {"kernel": "decode_partial", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+        "roofline": {"kernel": "decode_mma", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                      "frac": gbs / hbm, "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": traffic_for(f"decode_partial_{dw.name}", src)},
+                     "traffic": traffic_for(f"decode_mma_{dw.name}", src)},
         "clocks": clk.summary(),
         "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

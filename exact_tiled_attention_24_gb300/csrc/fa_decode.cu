@@ -37,6 +37,7 @@
 
 #include "fa_common.h"
 #include "fa_ptx.cuh"
+#include "fa_tmap.h"
 
 namespace fa {
 
@@ -519,6 +520,419 @@ static cudaError_t launch_partial_d(const void* q, const void* kc, const void* v
 
 }  // namespace dec
 
+// ----------------------------------------------------------------------------
+// The same decode step on the tensor cores (d = 128; cache blocks of 8, 16,
+// 32, 64 or 128 tokens).
+//
+// The FMA-pipe kernel above issues about 140 warp instructions per KB of K/V
+// (converting bf16 rows, 8-lane dot products, shuffles), and that instruction
+// stream, not HBM, sets its rate. Here both products of a 128-key tile run on
+// the tensor core with the tile's keys as M, so the work per key is a few
+// instructions of softmax:
+//   Sᵀ = K Qᵀ    M = 128 keys, N = 16 query heads (padded), K = d; into TMEM
+//   Oᵀ += Vᵀ Pᵀ  M = 128 dims, N = 16 heads, K = 128 keys; accumulated in TMEM
+// One thread per TMEM lane: lane r is key r of the tile in Sᵀ and dimension r
+// in Oᵀ. Each cache block of the tile arrives as its own TMA box (the cache
+// viewed as (d, block_size, num_blocks·Hkv)), written at row offset
+// block·block_size of the 128-row tile; a block past the context or with a
+// table entry outside [0, num_blocks) is requested at an out-of-range
+// coordinate, so the box reads zeros and the entry is never dereferenced.
+// The softmax keeps one exponent reference per head, raised (and Oᵀ's column
+// rescaled) when a key outgrows it by more than 2^8, as in the forward.
+// Roles (224 threads): warp 0 loads K tiles (2 stages), warp 1 V tiles
+// (1 stage), warp 2 owns TMEM and issues the products, warps 3..6 run the
+// softmax and the epilogue. Two CTAs fit an SM.
+namespace decmma {
+
+constexpr int D = 128;
+constexpr int TK = 128;       // keys per tile (M of the score product)
+constexpr int NH = 16;        // query heads per CTA (N of both products)
+constexpr int THREADS = 224;  // 7 warps
+constexpr float RESCALE_LOG2 = 8.f;
+
+// Per-CTA configuration by the number of query heads GM the softmax keeps
+// state for (4, 8 or 16). With up to 8 heads the state fits 80 registers,
+// and three CTAs share an SM with one K stage, one V stage and one Pᵀ
+// buffer each (more CTAs hide each one's start and finish better than
+// deeper rings: measured 5930 against 5400 GB/s). With 16 heads, two CTAs
+// with two K stages and two Pᵀ buffers.
+template <int GM>
+struct Cfg {
+  static constexpr int CTAS = GM <= 8 ? 3 : 2;
+  static constexpr int KST = CTAS == 3 ? 1 : 2, VST = 1, PB = CTAS == 3 ? 1 : 2;
+};
+
+template <int KST, int VST, int PB>
+struct Smem {
+  static constexpr int PANEL = TK * 128;   // 128 rows x 64 bf16 columns
+  static constexpr int TILE = 2 * PANEL;   // 128 keys x 128 dims
+  static constexpr int QPANEL = NH * 128;  // 16 rows x 64 bf16 columns
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + KST * TILE;
+  static constexpr int Q_OFF = V_OFF + VST * TILE;
+  static constexpr int P_OFF = Q_OFF + 2 * QPANEL;         // Pᵀ: PB buffers x 2 panels (16 heads x 128 keys)
+  static constexpr int RED_OFF = P_OFF + PB * 2 * QPANEL;  // [4 warps][NH] fp32
+  static constexpr int BAR_OFF = RED_OFF + 4 * NH * 4;
+  // q_full, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2],
+  // p_full[PB], p_empty[PB], o_done, final
+  static constexpr int NBARS = 1 + 2 * KST + 2 * VST + 2 + 2 * PB + 2;
+  static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int BYTES = TMEM_SLOT_OFF + 16;
+  static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+};
+
+template <int GM>
+__global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    const __grid_constant__ CUtensorMap tv, const int* __restrict__ block_table,
+    const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B, int H,
+    int Hkv, int num_blocks, int bs, int max_blocks, float scale_log2) {
+  constexpr int KST = Cfg<GM>::KST, VST = Cfg<GM>::VST, PB = Cfg<GM>::PB;
+  using L = Smem<KST, VST, PB>;
+  static_assert(Cfg<GM>::CTAS * (L::ALLOC + 1024) <= 233472, "the CTAs must fit an SM");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = gridDim.x;
+  const int G_all = H / Hkv;
+  const int n_chunk = (G_all + NH - 1) / NH;
+  const int s = blockIdx.x, hk = blockIdx.y / n_chunk, chunk = blockIdx.y % n_chunk, b = blockIdx.z;
+  const int G = min(GM, G_all - NH * chunk);  // query heads served by this CTA (GM covers them)
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t* err = &g_dec_err;
+
+  int Lb = in_range(b, 1, B, err) ? seq_lens[b] : 0;
+  Lb = Lb < 0 ? 0 : (Lb > max_blocks * bs ? max_blocks * bs : Lb);
+  const int n_tiles = (Lb + TK - 1) / TK;
+  const int tps = (n_tiles + S - 1) / S;
+  const int tile0 = s * tps;
+  const int tile1 = min(n_tiles, tile0 + tps);
+  const int head0 = b * H + hk * G_all + NH * chunk;        // first query head (row of q)
+  const long long prow = static_cast<long long>(s) * B * H + head0;  // its partial row
+  const long long part_rows = static_cast<long long>(S) * B * H;
+  if (tile0 >= tile1) {  // no key in this split: o_s = 0, lse_s = -inf (weight 0 in the merge)
+    for (int i = threadIdx.x; i < G * D; i += THREADS)
+      if (in_range(prow * D + i, 1, part_rows * D, err)) o_part[prow * D + i] = 0.f;
+    if (threadIdx.x < G && in_range(prow + threadIdx.x, 1, part_rows, err)) lse_part[prow + threadIdx.x] = -INFINITY;
+    return;
+  }
+  const int n_t = tile1 - tile0;
+  const int t_end = min(Lb, tile1 * TK);  // keys at or past t_end are masked
+
+  uint8_t* sK = smem + L::K_OFF;
+  uint8_t* sV = smem + L::V_OFF;
+  uint8_t* sQ = smem + L::Q_OFF;
+  uint8_t* sP = smem + L::P_OFF;
+  float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;            // [KST]
+  uint64_t* k_empty = k_full + KST;       // [KST]
+  uint64_t* v_full = k_empty + KST;       // [VST]
+  uint64_t* v_empty = v_full + VST;       // [VST]
+  uint64_t* s_full = v_empty + VST;       // [2]
+  uint64_t* p_full = s_full + 2;          // [PB]
+  uint64_t* p_empty = p_full + PB;        // [PB]
+  uint64_t* o_done = p_empty + PB;
+  uint64_t* final_bar = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < KST; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < VST; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
+    for (int i = 0; i < PB; ++i) {
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_empty[i], 1);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(final_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 64);  // Sᵀ buffers at columns 0 and 16, Oᵀ at 32
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Loads of one 128-key tile of the cache: one box per cache block.
+  const int bpt = TK / bs;  // blocks per tile
+  auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile) {
+    const int blk_first = tile * bpt;
+    for (int i = 0; i < bpt; ++i) {
+      const int bi = blk_first + i;
+      int z = num_blocks * Hkv;  // out of range: the box reads zeros
+      if (bi * bs < Lb) {
+        const long long ti = static_cast<long long>(b) * max_blocks + bi;
+        const int blk = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
+        if (blk >= 0 && blk < num_blocks) z = blk * Hkv + hk;
+        else atomicExch(err, DEV_BAD_INDEX);
+      }
+      for (int p = 0; p < 2; ++p) tma_load_3d(dst + p * L::PANEL + i * bs * 128, map, bar, p * 64, 0, z);
+    }
+  };
+
+  if (warp == 0) {
+    // --------------------------------------------------------- K producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      mbar_arrive_expect_tx(q_full, 2 * L::QPANEL);
+      for (int p = 0; p < 2; ++p) tma_load_3d(sQ + p * L::QPANEL, &tq, q_full, p * 64, head0, 0);
+      int issued = 0;
+      for (int j = 0; j < n_t; ++j) {
+        const int st = j % KST;
+        if (!mbar_wait(&k_empty[st], ((j / KST) & 1) ^ 1, err)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::TILE);
+        load_tile(&tk, sK + st * L::TILE, &k_full[st], tile0 + j);
+        issued = j + 1;
+      }
+      mbar_wait(q_full, 0, err);
+      for (int j = max(0, issued - KST); j < issued; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, err);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- V producer
+    if (lane == 0) {
+      prefetch_tmap(&tv);
+      int issued = 0;
+      for (int j = 0; j < n_t; ++j) {
+        const int st = j % VST;
+        if (!mbar_wait(&v_empty[st], ((j / VST) & 1) ^ 1, err)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::TILE);
+        load_tile(&tv, sV + st * L::TILE, &v_full[st], tile0 + j);
+        issued = j + 1;
+      }
+      for (int j = max(0, issued - VST); j < issued; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, err);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16(TK, NH, false, false);  // A = K (K-major), B = Q (K-major)
+    constexpr uint32_t idesc_o = idesc_bf16(D, NH, true, false);    // A = Vᵀ (MN-major), B = Pᵀ (K-major)
+    const uint64_t dq = sdesc_kmajor(smem_u32(sQ), 0);
+    // Sᵀ_j = K_j Qᵀ into TMEM buffer j % 2. Issued one tile ahead of O: its
+    // buffer's previous reader (the softmax of tile j - 2) released it before
+    // P_{j-2}, which O_{j-2}, issued earlier, waited for.
+    auto issue_s = [&](int j) -> bool {
+      const int st = j % KST;
+      if (!mbar_wait_warp(&k_full[st], (j / KST) & 1, err)) return false;
+      tc_fence_after();
+      const uint64_t dk = sdesc_kmajor(smem_u32(sK + st * L::TILE), 0);
+      if (elect_one()) {
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16)
+          mma_ss(tmem + (j & 1) * NH, desc_add(dk, kmajor_step(k16, L::PANEL)),
+                 desc_add(dq, kmajor_step(k16, L::QPANEL)), idesc_s, k16 > 0);
+        tc_commit(&s_full[j & 1]);
+        tc_commit(&k_empty[st]);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = mbar_wait_warp(q_full, 0, err) && issue_s(0);
+    for (int j = 0; j < n_t && ok; ++j) {
+      const int vs = j % VST, pb = j % PB;
+      // The next tile's scores first, so its softmax can run while V_j lands.
+      if (j + 1 < n_t && !issue_s(j + 1)) {
+        ok = false;
+        break;
+      }
+      ok = mbar_wait_warp(&v_full[vs], (j / VST) & 1, err) && mbar_wait_warp(&p_full[pb], (j / PB) & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dv = sdesc_mnmajor(smem_u32(sV + vs * L::TILE), 0, L::PANEL);
+      const uint64_t dp = sdesc_kmajor(smem_u32(sP + pb * 2 * L::QPANEL), 0);
+      if (elect_one()) {
+#pragma unroll
+        for (int k16 = 0; k16 < TK / 16; ++k16)
+          mma_ss(tmem + 32, desc_add(dv, mnmajor_step(k16)), desc_add(dp, kmajor_step(k16, L::QPANEL)), idesc_o,
+                 (j > 0 || k16 > 0) ? 1u : 0u);
+        tc_commit(&v_empty[vs]);
+        tc_commit(&p_empty[pb]);
+        tc_commit(o_done);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) tc_commit(final_bar);
+    __syncwarp();
+    mbar_wait_warp(final_bar, 0, err);
+  } else {
+    // ------------------------------------------------------ softmax (3..6)
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;     // key of the tile in Sᵀ, dimension in Oᵀ
+    const int wi = warp - 3;               // 0..3, index into the reduction scratch
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    // Pᵀ rows of padded heads (h >= G) are zero in both buffers for good.
+    for (int i = r; i < PB * 2 * NH * 64; i += 128) {
+      const int h = (i / 64) % NH;
+      if (h >= G) reinterpret_cast<uint16_t*>(sP)[i] = 0;
+    }
+    float m[GM], l[GM];
+#pragma unroll
+    for (int h = 0; h < GM; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+    bool ok = true;
+    for (int j = 0; j < n_t; ++j) {
+      const int sb = j & 1, pb = j % PB;
+      if (ok) ok = mbar_wait(&s_full[sb], (j >> 1) & 1, err);
+      if (named_bar_any(1, 128, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t raw[16];
+      tmem_ld16(tmem + lane_addr + sb * NH, raw);
+      tmem_ld_wait();
+      const bool live = (tile0 + j) * TK + r < t_end;
+      float x[GM];
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        x[h] = live && h < G ? __uint_as_float(raw[h]) * scale_log2 : -INFINITY;
+        need |= x[h] > m[h] + RESCALE_LOG2;
+      }
+      if (named_bar_any(1, 128, need)) {
+        // Raise every head's reference to its exact maximum so far.
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          float v = x[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          if (lane == 0) red[wi * NH + h] = v;
+        }
+        named_bar_sync(1, 128);
+        float alpha[GM];
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          const float tmax = fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h]));
+          const float m_new = fmaxf(m[h], tmax);
+          alpha[h] = m_new == -INFINITY ? 1.f : ex2(m[h] - m_new);  // 0 on a head's first key
+          m[h] = m_new;
+          l[h] *= alpha[h];
+        }
+        named_bar_sync(1, 128);  // the scratch is read before anyone rewrites it
+        if (j > 0) {
+          // Oᵀ columns *= alpha once O_{j-1} has landed (O_j accumulates into
+          // it). When S_j completed, O_{j-2} had (it was issued before S_j), so
+          // o_done is at most one phase behind and the parity wait is exact.
+          ok = mbar_wait(o_done, (j - 1) & 1, err);
+          tc_fence_after();
+          if (ok) {
+            uint32_t o[16];
+            tmem_ld16(tmem + lane_addr + 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < GM; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+            tmem_st16(tmem + lane_addr + 32, o);
+          }
+        }
+      }
+      // P_j (bf16) into Pᵀ buffer j % PB once O_{j-PB} has read it.
+      if (ok) ok = mbar_wait(&p_empty[pb], ((j / PB) & 1) ^ 1, err);
+      uint8_t* pbuf = sP + pb * 2 * L::QPANEL + (r / 64) * L::QPANEL;
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        if (h >= G) break;
+        const float pv = ex2(x[h] - m[h]);  // x = -inf (masked) gives 0
+        l[h] += pv;
+        const int off = h * 128 + ((((r % 64) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2;
+        if (in_range((r / 64) * L::QPANEL + off, 2, 2 * L::QPANEL, err))
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = __float2bfloat16_rn(pv);
+      }
+      fence_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[pb]);
+    }
+    // ------------------------------------------------------------ epilogue
+    // Wait for the issuer's final commit, not for o_done: with the scores
+    // issued a tile ahead the softmax can finish its last tile while o_done
+    // is two phases behind, and a parity wait would then match an earlier
+    // completed phase. The final barrier has one phase only.
+    if (ok) ok = mbar_wait(final_bar, 0, err);
+    if (!named_bar_any(1, 128, !ok)) {
+      tc_fence_after();
+      // Every thread's partial denominators, summed per head.
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        float v = l[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[wi * NH + h] = v;
+      }
+      named_bar_sync(1, 128);
+      uint32_t o[16];
+      tmem_ld16(tmem + lane_addr + 32, o);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        if (h >= G) break;
+        const float lh = (red[h] + red[NH + h]) + (red[2 * NH + h] + red[3 * NH + h]);
+        const long long orow = prow + h;
+        if (in_range(orow * D + r, 1, part_rows * D, err)) o_part[orow * D + r] = __uint_as_float(o[h]) / lh;
+        if (r == 0 && in_range(orow, 1, part_rows, err)) lse_part[orow] = (m[h] + __log2f(lh)) * dec::LN2;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+template <int GM>
+static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const int* table,
+                            const int* seq_lens, float* o_part, float* lse_part, int B, int H, int Hkv,
+                            int num_blocks, int bs, int max_blocks, float scale, int S, cudaStream_t stream) {
+  using C = Cfg<GM>;
+  const int smem = Smem<C::KST, C::VST, C::PB>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_chunk = (H / Hkv + NH - 1) / NH;
+  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(Hkv * n_chunk), static_cast<unsigned>(B));
+  decode_mma_kernel<GM><<<grid, THREADS, smem, stream>>>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv,
+                                                         num_blocks, bs, max_blocks, scale * dec::LOG2E);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch(const void* q, const void* kc, const void* vc, const int* table, const int* seq_lens,
+                          float* o_part, float* lse_part, int B, int H, int Hkv, int num_blocks, int bs,
+                          int max_blocks, float scale, int S, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16(&tq, q, 1, B * H, D, NH) || !make_tmap_bf16(&tk, kc, num_blocks * Hkv, bs, D, bs) ||
+      !make_tmap_bf16(&tv, vc, num_blocks * Hkv, bs, D, bs))
+    return cudaErrorInvalidValue;
+  const int G = H / Hkv;  // query heads per K/V head; CTAs take them 16 at a time
+  if (G <= 4)
+    return launch_t<4>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks, scale,
+                       S, stream);
+  if (G <= 8)
+    return launch_t<8>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks, scale,
+                       S, stream);
+  return launch_t<16>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks, scale,
+                      S, stream);
+}
+
+// Shapes this kernel serves; the others take the FMA-pipe kernel.
+inline bool serves(int d, int bs) { return d == D && bs % 8 == 0 && TK % bs == 0; }
+
+}  // namespace decmma
+
 cudaError_t launch_attn_merge(const float* o_parts, const float* lse_parts, int S, void* o, float* lse,
                               long long rows, int d, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
@@ -536,6 +950,12 @@ cudaError_t launch_decode_paged(const void* q, const void* k_cache, const void* 
                                 float* o_part, float* lse_part, int B, int H, int Hkv, int d,
                                 int num_blocks, int block_size, int max_blocks, float scale, int S,
                                 cudaStream_t stream) {
+  if (decmma::serves(d, block_size)) {
+    cudaError_t e = decmma::launch(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H, Hkv,
+                                   num_blocks, block_size, max_blocks, scale, S, stream);
+    if (e != cudaSuccess) return e;
+    return launch_attn_merge(o_part, lse_part, S, o, lse, static_cast<long long>(B) * H, d, stream);
+  }
   cudaError_t e =
       d == 64 ? dec::launch_partial_d<64>(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H,
                                           Hkv, num_blocks, block_size, max_blocks, scale, S, stream)
