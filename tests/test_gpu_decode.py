@@ -56,6 +56,10 @@ def run_case(fa, q, kc, vc, table, lens, n_splits, scale):
     (1, 2, 1, 64, 48, [2000], 7),            # block size not a power of two
     (2, 32, 1, 128, 16, [300, 1500], 3),     # 32 query heads on one K/V head: two CTAs of 16
     (1, 24, 1, 64, 32, [777], 2),            # 24 = 16 + 8
+    # d = 128 with blocks of 8 to 128 tokens runs on the tensor cores
+    (2, 8, 2, 128, 8, [100, 37], 2),         # eight-token blocks: 16 boxes per tile
+    (2, 12, 3, 128, 64, [700, 129], 3),      # 64-token blocks
+    (1, 40, 5, 128, 16, [1025], 4),          # 8 query heads per K/V head
 ])
 def test_decode_paged_vs_oracle(fa, B, H, Hkv, d, bs, seq_lens, n_splits):
     q, kc, vc, table, lens = paged_case(B, H, Hkv, d, bs, seq_lens, seed=B * 100 + H + bs + sum(seq_lens))
@@ -78,15 +82,18 @@ def test_decode_split_count_does_not_change_the_result(fa):
         assert (lse - outs[0][1]).abs().max() <= 1e-4
 
 
-def test_decode_bad_block_index_is_reported_not_read(fa):
-    q, kc, vc, table, lens = paged_case(2, 4, 2, 64, 16, [40, 40], seed=9)
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_bad_block_index_is_reported_not_read(fa, d):
+    # d = 64 runs the FMA-pipe kernel, d = 128 the tensor-core one
+    q, kc, vc, table, lens = paged_case(2, 4, 2, d, 16, [40, 40], seed=9)
     table[1, 1] = kc.shape[0] + 5  # outside the cache
     fa.decode_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), lens.cuda(), n_splits=2)
     assert fa.last_device_error() == 7  # FA_ERR_BAD_INDEX
     assert fa.last_device_error() == 0  # read and cleared
     # request 0 does not use the bad entry and is still right
-    o, lse = run_case(fa, q[:1].contiguous(), kc, vc, table[:1].contiguous(), lens[:1].contiguous(), 2, 0.125)
-    ro, rlse = decode_paged(to_f64(q[:1]), to_f64(kc), to_f64(vc), table[:1].numpy(), lens[:1].numpy(), 0.125)
+    scale = d ** -0.5
+    o, lse = run_case(fa, q[:1].contiguous(), kc, vc, table[:1].contiguous(), lens[:1].contiguous(), 2, scale)
+    ro, rlse = decode_paged(to_f64(q[:1]), to_f64(kc), to_f64(vc), table[:1].numpy(), lens[:1].numpy(), scale)
     assert_o(o, ro)
 
 
