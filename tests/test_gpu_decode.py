@@ -112,3 +112,26 @@ def test_merge_vs_oracle(fa, S, rows, d):
     fin = np.isfinite(rlse)
     np.testing.assert_allclose(lse.cpu().numpy()[fin], rlse[fin], rtol=0, atol=1e-4)
     assert np.all(np.isneginf(lse.cpu().numpy()[~fin]))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_peaked_scores_raise_the_reference(fa, d):
+    # q ~ N(0, 8²): scaled scores have a standard deviation of 8 (11.5 in log2
+    # units), so a head's maximum keeps outgrowing its exponent reference by
+    # more than 2^8 after the first tile, and the output columns are rescaled.
+    q, kc, vc, table, lens = paged_case(2, 8, 2, d, 16, [1500, 700], seed=31 + d)
+    q = (q.float() * 8).to(torch.bfloat16)
+    scale = d ** -0.5
+    qd, kd = to_f64(q), to_f64(kc)
+    # the scenario holds: for some head, a key past the first 128 outscores the
+    # first 128 keys' maximum by more than 8 in log2 units
+    t = table[0].long()
+    keys = np.swapaxes(kd[t], 0, 1).reshape(kd.shape[1], -1, d)[:, :int(lens[0])]  # [Hkv, L, d]
+    G = q.shape[1] // kc.shape[1]
+    s = np.einsum("hd,hkd->hk", qd[0], np.repeat(keys, G, axis=0)) * scale * np.log2(np.e)
+    assert np.any(s[:, 128:].max(1) - s[:, :128].max(1) > 8)
+    for n_splits in (1, 3):
+        o, lse = run_case(fa, q, kc, vc, table, lens, n_splits, scale)
+        ro, rlse = decode_paged(qd, kd, to_f64(vc), table.numpy(), lens.numpy(), scale)
+        assert_o(o, ro)
+        assert_lse(lse, rlse)
