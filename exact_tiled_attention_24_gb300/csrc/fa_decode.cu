@@ -521,8 +521,8 @@ static cudaError_t launch_partial_d(const void* q, const void* kc, const void* v
 }  // namespace dec
 
 // ----------------------------------------------------------------------------
-// The same decode step on the tensor cores (d = 128; cache blocks of 8, 16,
-// 32, 64 or 128 tokens).
+// The same decode step on the tensor cores (d = 64 or 128; cache blocks of
+// 8, 16, 32, 64 or 128 tokens).
 //
 // The FMA-pipe kernel above issues about 140 warp instructions per KB of K/V
 // (converting bf16 rows, 8-lane dot products, shuffles), and that instruction
@@ -530,7 +530,8 @@ static cudaError_t launch_partial_d(const void* q, const void* kc, const void* v
 // the tensor core with the tile's keys as M, so the work per key is a few
 // instructions of softmax:
 //   Sᵀ = K Qᵀ    M = 128 keys, N = 16 query heads (padded), K = d; into TMEM
-//   Oᵀ += Vᵀ Pᵀ  M = 128 dims, N = 16 heads, K = 128 keys; accumulated in TMEM
+//   Oᵀ += Vᵀ Pᵀ  M = 128 dims (d = 64: padded by a zero panel), N = 16 heads,
+//                K = 128 keys; accumulated in TMEM
 // One thread per TMEM lane: lane r is key r of the tile in Sᵀ and dimension r
 // in Oᵀ. Each cache block of the tile arrives as its own TMA box (the cache
 // viewed as (d, block_size, num_blocks·Hkv)), written at row offset
@@ -544,7 +545,6 @@ static cudaError_t launch_partial_d(const void* q, const void* kc, const void* v
 // softmax and the epilogue. Two CTAs fit an SM.
 namespace decmma {
 
-constexpr int D = 128;
 constexpr int TK = 128;       // keys per tile (M of the score product)
 constexpr int NH = 16;        // query heads per CTA (N of both products)
 constexpr int THREADS = 224;  // 7 warps
@@ -562,15 +562,20 @@ struct Cfg {
   static constexpr int KST = CTAS == 3 ? 1 : 2, VST = 1, PB = CTAS == 3 ? 1 : 2;
 };
 
-template <int KST, int VST, int PB>
+// K tiles hold D / 64 panels of 64 columns; a V tile always holds two, so
+// that Oᵀ = Vᵀ Pᵀ is an M = 128 product: at d = 64 its second panel stays
+// zero, and rows 64..127 of Oᵀ are zero and never written out.
+template <int D, int KST, int VST, int PB>
 struct Smem {
   static constexpr int PANEL = TK * 128;   // 128 rows x 64 bf16 columns
-  static constexpr int TILE = 2 * PANEL;   // 128 keys x 128 dims
+  static constexpr int KPANELS = D / 64;
+  static constexpr int K_TILE = KPANELS * PANEL;
+  static constexpr int V_TILE = 2 * PANEL;
   static constexpr int QPANEL = NH * 128;  // 16 rows x 64 bf16 columns
   static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = K_OFF + KST * TILE;
-  static constexpr int Q_OFF = V_OFF + VST * TILE;
-  static constexpr int P_OFF = Q_OFF + 2 * QPANEL;         // Pᵀ: PB buffers x 2 panels (16 heads x 128 keys)
+  static constexpr int V_OFF = K_OFF + KST * K_TILE;
+  static constexpr int Q_OFF = V_OFF + VST * V_TILE;
+  static constexpr int P_OFF = Q_OFF + KPANELS * QPANEL;   // Pᵀ: PB buffers x 2 panels (16 heads x 128 keys)
   static constexpr int RED_OFF = P_OFF + PB * 2 * QPANEL;  // [4 warps][NH] fp32
   static constexpr int BAR_OFF = RED_OFF + 4 * NH * 4;
   // q_full, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2],
@@ -581,14 +586,14 @@ struct Smem {
   static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
 };
 
-template <int GM>
+template <int D, int GM>
 __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const int* __restrict__ block_table,
     const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B, int H,
     int Hkv, int num_blocks, int bs, int max_blocks, float scale_log2) {
   constexpr int KST = Cfg<GM>::KST, VST = Cfg<GM>::VST, PB = Cfg<GM>::PB;
-  using L = Smem<KST, VST, PB>;
+  using L = Smem<D, KST, VST, PB>;
   static_assert(Cfg<GM>::CTAS * (L::ALLOC + 1024) <= 233472, "the CTAs must fit an SM");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -668,7 +673,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
 
   // Loads of one 128-key tile of the cache: one box per cache block.
   const int bpt = TK / bs;  // blocks per tile
-  auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile) {
+  auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile) {  // D / 64 panels
     const int blk_first = tile * bpt;
     for (int i = 0; i < bpt; ++i) {
       const int bi = blk_first + i;
@@ -679,7 +684,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
         if (blk >= 0 && blk < num_blocks) z = blk * Hkv + hk;
         else atomicExch(err, DEV_BAD_INDEX);
       }
-      for (int p = 0; p < 2; ++p) tma_load_3d(dst + p * L::PANEL + i * bs * 128, map, bar, p * 64, 0, z);
+      for (int p = 0; p < L::KPANELS; ++p) tma_load_3d(dst + p * L::PANEL + i * bs * 128, map, bar, p * 64, 0, z);
     }
   };
 
@@ -688,14 +693,14 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
-      mbar_arrive_expect_tx(q_full, 2 * L::QPANEL);
-      for (int p = 0; p < 2; ++p) tma_load_3d(sQ + p * L::QPANEL, &tq, q_full, p * 64, head0, 0);
+      mbar_arrive_expect_tx(q_full, L::KPANELS * L::QPANEL);
+      for (int p = 0; p < L::KPANELS; ++p) tma_load_3d(sQ + p * L::QPANEL, &tq, q_full, p * 64, head0, 0);
       int issued = 0;
       for (int j = 0; j < n_t; ++j) {
         const int st = j % KST;
         if (!mbar_wait(&k_empty[st], ((j / KST) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::TILE);
-        load_tile(&tk, sK + st * L::TILE, &k_full[st], tile0 + j);
+        mbar_arrive_expect_tx(&k_full[st], L::K_TILE);
+        load_tile(&tk, sK + st * L::K_TILE, &k_full[st], tile0 + j);
         issued = j + 1;
       }
       mbar_wait(q_full, 0, err);
@@ -709,8 +714,8 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
       for (int j = 0; j < n_t; ++j) {
         const int st = j % VST;
         if (!mbar_wait(&v_empty[st], ((j / VST) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::TILE);
-        load_tile(&tv, sV + st * L::TILE, &v_full[st], tile0 + j);
+        mbar_arrive_expect_tx(&v_full[st], L::K_TILE);  // the real panels of the V tile
+        load_tile(&tv, sV + st * L::V_TILE, &v_full[st], tile0 + j);
         issued = j + 1;
       }
       for (int j = max(0, issued - VST); j < issued; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, err);
@@ -718,7 +723,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   } else if (warp == 2) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16(TK, NH, false, false);  // A = K (K-major), B = Q (K-major)
-    constexpr uint32_t idesc_o = idesc_bf16(D, NH, true, false);    // A = Vᵀ (MN-major), B = Pᵀ (K-major)
+    constexpr uint32_t idesc_o = idesc_bf16(128, NH, true, false);  // A = Vᵀ (MN-major, M = 128), B = Pᵀ (K-major)
     const uint64_t dq = sdesc_kmajor(smem_u32(sQ), 0);
     // Sᵀ_j = K_j Qᵀ into TMEM buffer j % 2. Issued one tile ahead of O: its
     // buffer's previous reader (the softmax of tile j - 2) released it before
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
       const int st = j % KST;
       if (!mbar_wait_warp(&k_full[st], (j / KST) & 1, err)) return false;
       tc_fence_after();
-      const uint64_t dk = sdesc_kmajor(smem_u32(sK + st * L::TILE), 0);
+      const uint64_t dk = sdesc_kmajor(smem_u32(sK + st * L::K_TILE), 0);
       if (elect_one()) {
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
@@ -750,7 +755,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
       ok = mbar_wait_warp(&v_full[vs], (j / VST) & 1, err) && mbar_wait_warp(&p_full[pb], (j / PB) & 1, err);
       if (!ok) break;
       tc_fence_after();
-      const uint64_t dv = sdesc_mnmajor(smem_u32(sV + vs * L::TILE), 0, L::PANEL);
+      const uint64_t dv = sdesc_mnmajor(smem_u32(sV + vs * L::V_TILE), 0, L::PANEL);
       const uint64_t dp = sdesc_kmajor(smem_u32(sP + pb * 2 * L::QPANEL), 0);
       if (elect_one()) {
 #pragma unroll
@@ -772,11 +777,16 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     const int r = quarter * 32 + lane;     // key of the tile in Sᵀ, dimension in Oᵀ
     const int wi = warp - 3;               // 0..3, index into the reduction scratch
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    // Pᵀ rows of padded heads (h >= G) are zero in both buffers for good.
+    // Pᵀ rows of padded heads (h >= G) are zero in both buffers for good;
+    // at d = 64 so is the second panel of every V stage.
     for (int i = r; i < PB * 2 * NH * 64; i += 128) {
       const int h = (i / 64) % NH;
       if (h >= G) reinterpret_cast<uint16_t*>(sP)[i] = 0;
     }
+    if (D == 64)
+      for (int st = 0; st < VST; ++st)
+        for (int i = r; i < L::PANEL / 16; i += 128)
+          reinterpret_cast<uint4*>(sV + st * L::V_TILE + L::PANEL)[i] = make_uint4(0u, 0u, 0u, 0u);
     float m[GM], l[GM];
 #pragma unroll
     for (int h = 0; h < GM; ++h) {
@@ -882,7 +892,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
         if (h >= G) break;
         const float lh = (red[h] + red[NH + h]) + (red[2 * NH + h] + red[3 * NH + h]);
         const long long orow = prow + h;
-        if (in_range(orow * D + r, 1, part_rows * D, err)) o_part[orow * D + r] = __uint_as_float(o[h]) / lh;
+        if (r < D && in_range(orow * D + r, 1, part_rows * D, err)) o_part[orow * D + r] = __uint_as_float(o[h]) / lh;
         if (r == 0 && in_range(orow, 1, part_rows, err)) lse_part[orow] = (m[h] + __log2f(lh)) * dec::LN2;
       }
     }
@@ -895,41 +905,51 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   }
 }
 
-template <int GM>
+template <int D, int GM>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const int* table,
                             const int* seq_lens, float* o_part, float* lse_part, int B, int H, int Hkv,
                             int num_blocks, int bs, int max_blocks, float scale, int S, cudaStream_t stream) {
   using C = Cfg<GM>;
-  const int smem = Smem<C::KST, C::VST, C::PB>::ALLOC;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = Smem<D, C::KST, C::VST, C::PB>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_chunk = (H / Hkv + NH - 1) / NH;
   const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(Hkv * n_chunk), static_cast<unsigned>(B));
-  decode_mma_kernel<GM><<<grid, THREADS, smem, stream>>>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv,
+  decode_mma_kernel<D, GM><<<grid, THREADS, smem, stream>>>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv,
                                                          num_blocks, bs, max_blocks, scale * dec::LOG2E);
   return cudaGetLastError();
 }
 
-static cudaError_t launch(const void* q, const void* kc, const void* vc, const int* table, const int* seq_lens,
-                          float* o_part, float* lse_part, int B, int H, int Hkv, int num_blocks, int bs,
-                          int max_blocks, float scale, int S, cudaStream_t stream) {
+template <int D>
+static cudaError_t launch_d(const void* q, const void* kc, const void* vc, const int* table, const int* seq_lens,
+                            float* o_part, float* lse_part, int B, int H, int Hkv, int num_blocks, int bs,
+                            int max_blocks, float scale, int S, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16(&tq, q, 1, B * H, D, NH) || !make_tmap_bf16(&tk, kc, num_blocks * Hkv, bs, D, bs) ||
       !make_tmap_bf16(&tv, vc, num_blocks * Hkv, bs, D, bs))
     return cudaErrorInvalidValue;
   const int G = H / Hkv;  // query heads per K/V head; CTAs take them 16 at a time
   if (G <= 4)
-    return launch_t<4>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks, scale,
-                       S, stream);
+    return launch_t<D, 4>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks,
+                          scale, S, stream);
   if (G <= 8)
-    return launch_t<8>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks, scale,
-                       S, stream);
-  return launch_t<16>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks, scale,
-                      S, stream);
+    return launch_t<D, 8>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks,
+                          scale, S, stream);
+  return launch_t<D, 16>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks,
+                         scale, S, stream);
+}
+
+static cudaError_t launch(const void* q, const void* kc, const void* vc, const int* table, const int* seq_lens,
+                          float* o_part, float* lse_part, int B, int H, int Hkv, int d, int num_blocks, int bs,
+                          int max_blocks, float scale, int S, cudaStream_t stream) {
+  return d == 64 ? launch_d<64>(q, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                                max_blocks, scale, S, stream)
+                 : launch_d<128>(q, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                                 max_blocks, scale, S, stream);
 }
 
 // Shapes this kernel serves; the others take the FMA-pipe kernel.
-inline bool serves(int d, int bs) { return d == D && bs % 8 == 0 && TK % bs == 0; }
+inline bool serves(int d, int bs) { return (d == 64 || d == 128) && bs % 8 == 0 && TK % bs == 0; }
 
 }  // namespace decmma
 
@@ -951,7 +971,7 @@ cudaError_t launch_decode_paged(const void* q, const void* k_cache, const void* 
                                 int num_blocks, int block_size, int max_blocks, float scale, int S,
                                 cudaStream_t stream) {
   if (decmma::serves(d, block_size)) {
-    cudaError_t e = decmma::launch(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H, Hkv,
+    cudaError_t e = decmma::launch(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H, Hkv, d,
                                    num_blocks, block_size, max_blocks, scale, S, stream);
     if (e != cudaSuccess) return e;
     return launch_attn_merge(o_part, lse_part, S, o, lse, static_cast<long long>(B) * H, d, stream);

@@ -56,7 +56,7 @@ def run_case(fa, q, kc, vc, table, lens, n_splits, scale):
     (1, 2, 1, 64, 48, [2000], 7),            # block size not a power of two
     (2, 32, 1, 128, 16, [300, 1500], 3),     # 32 query heads on one K/V head: two CTAs of 16
     (1, 24, 1, 64, 32, [777], 2),            # 24 = 16 + 8
-    # d = 128 with blocks of 8 to 128 tokens runs on the tensor cores
+    # blocks of 8 to 128 tokens run on the tensor cores (1 and 48 above on the FMA pipe)
     (2, 8, 2, 128, 8, [100, 37], 2),         # eight-token blocks: 16 boxes per tile
     (2, 12, 3, 128, 64, [700, 129], 3),      # 64-token blocks
     (1, 40, 5, 128, 16, [1025], 4),          # 8 query heads per K/V head
@@ -84,7 +84,7 @@ def test_decode_split_count_does_not_change_the_result(fa):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_decode_bad_block_index_is_reported_not_read(fa, d):
-    # d = 64 runs the FMA-pipe kernel, d = 128 the tensor-core one
+    # both head sizes run the tensor-core kernel with 16-token blocks
     q, kc, vc, table, lens = paged_case(2, 4, 2, d, 16, [40, 40], seed=9)
     table[1, 1] = kc.shape[0] + 5  # outside the cache
     fa.decode_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), lens.cuda(), n_splits=2)
