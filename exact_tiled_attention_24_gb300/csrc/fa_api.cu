@@ -224,11 +224,6 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
   const long long ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
   if (ctx > INT_MAX / 2 || static_cast<long long>(num_blocks) * Hkv * block_size * d > (1ll << 40))
     return FA_ERR_UNSUPPORTED;
-  // Block-table entries one split can touch.
-  const long long T = fa::kDecodeTileKeys;
-  const long long tiles = (ctx + T - 1) / T;
-  const long long per_split = (tiles + n_splits - 1) / n_splits * T;
-  if ((per_split + block_size - 1) / block_size + 1 > fa::kDecodeMaxTable) return FA_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < fa_decode_workspace_bytes(B, H, d, n_splits)) return FA_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
       !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||

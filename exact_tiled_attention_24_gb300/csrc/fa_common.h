@@ -42,11 +42,6 @@ cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const voi
 cudaError_t launch_softmax(const float* x, float* y, long long rows, int n, bool online,
                            cudaStream_t stream);
 
-// Block-table entries one decode split may use (its slice is staged in
-// shared memory); the host rejects splits that could need more.
-constexpr int kDecodeMaxTable = 1024;
-constexpr int kDecodeTileKeys = 64;
-
 // Decode of one new query row per request against a paged KV cache
 // (k_cache, v_cache [num_blocks][Hkv][block_size][d] bf16), split over the
 // context into S parts, partial results in o_part [S][B*H][d] fp32 and

@@ -17,23 +17,15 @@
 //     lse = ln Σ_s e^(lse_s),   o = Σ_s e^(lse_s − lse) · o_s.
 //
 // Kernels:
-//   decode_partial  one CTA per (context split, K/V head, request). It serves
-//                   the G query heads that share the K/V head, so each K/V
-//                   byte is read once per step (G > 16: one CTA per 16 of
-//                   them, each reading the K/V head). 64-key tiles of K and V are
-//                   copied into shared memory by bulk copies (one per run of
-//                   consecutive tokens inside a cache block), three tiles in
-//                   flight. Each warp owns 8 keys of every tile and keeps
-//                   its own running (m, l) and fp32 output rows; the warps'
-//                   states are merged once at the end. Writes o_s (fp32)
-//                   and lse_s per head.
-//   merge           one warp per output row: the combination above.
-// The work per byte is a few FMAs (G·d per key and head pair), far below the
-// tensor-core ridge, so the products run on the FMA pipe.
+//   decode_mma  one CTA per (context split, K/V head, request, 16 query
+//               heads): both products of each 128-key tile on the tensor
+//               cores; writes o_s (fp32) and lse_s per head.
+//   merge       one warp per output row: the combination above.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "fa_common.h"
 #include "fa_ptx.cuh"
@@ -45,403 +37,13 @@ static __device__ uint32_t g_dec_err;
 
 namespace dec {
 
-constexpr int THREADS = 256;
-constexpr int TK = 64;  // keys per tile
-// Stages of the K/V ring. Two CTAs per SM with three 32 KB stages each keep
-// ~128 KB of loads in flight per SM, what HBM latency under load needs.
-constexpr int NST = 3;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.69314718055994531f;
-
-template <int D, int GM>
-struct Smem {
-  static constexpr int WARPS = THREADS / 32;
-  static constexpr int ROW = D * 2;             // bytes of one key (or value) row
-  static constexpr int TILE = TK * ROW;         // one K or V tile
-  // Each warp streams its own 8 keys of every tile: stage st of warp w holds
-  // their K rows then their V rows (after the loop, the stages hold the
-  // warps' partial output rows).
-  static constexpr int WSLOT = 2 * 8 * ROW;
-  static constexpr int SLOT_OFF = 0;
-  static constexpr int Q_OFF = NST * WARPS * WSLOT;  // q rows fp32 [GM][D], times scale·log2 e
-  // Per-warp scratch: the scores, then the (p, p) pairs, of its 8 keys x 4
-  // heads (64 floats), then the 4 heads' rescale factors.
-  static constexpr int W_OFF = Q_OFF + GM * D * 4;
-  static constexpr int W_BYTES = (8 * 4 * 2 + 4) * 4;
-  static constexpr int ML_OFF = W_OFF + WARPS * W_BYTES;  // per-warp (m, l) per head: [WARPS][2][GM]
-  static constexpr int TAB_OFF = ML_OFF + WARPS * 2 * GM * 4;  // block-table slice, int32
-  static constexpr int BAR_OFF = TAB_OFF + kDecodeMaxTable * 4;
-  // full[NST][WARPS] mbarriers, then fills so far per (stage, warp)
-  static constexpr int CNT_OFF = BAR_OFF + NST * WARPS * 8;
-  static constexpr int BYTES = CNT_OFF + NST * WARPS * 4 + 16;
-  static_assert(WARPS * GM * D * 4 <= NST * WARPS * WSLOT, "the warps' partial rows must fit the idle stages");
-};
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
-}
-
-// Two fp32 multiply-adds in one instruction: d = a * b + c, element-wise.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(*reinterpret_cast<unsigned long long*>(&d))
-      : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
-        "l"(*reinterpret_cast<const unsigned long long*>(&b)),
-        "l"(*reinterpret_cast<const unsigned long long*>(&c)));
-  return d;
-}
-
-// bf16 pair (low half = first element) -> two floats, exactly.
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-// Each warp owns keys 8w .. 8w + 7 of every tile: it streams their K and V
-// rows through its own NST-slot ring (own mbarriers, refilled by itself as
-// soon as it has read a slot) and keeps its own running (m, l) and output
-// rows for the G heads. The warps never wait for one another inside the
-// tile loop; their states are merged at the end with the same rescaling as
-// the split merge. Two CTAs share an SM (the ring depth above assumes it),
-// so the kernel is held to 128 registers a thread, except with 16 heads of
-// 128 columns, whose accumulators would then spill.
-template <int D, int GM>
-__global__ void __launch_bounds__(THREADS, D * GM > 1024 ? 1 : 2) decode_partial_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cache,
-    const __nv_bfloat16* __restrict__ v_cache, const int* __restrict__ block_table,
-    const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B,
-    int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale_log2) {
-  using L = Smem<D, GM>;
-  constexpr int WARPS = L::WARPS;
-  constexpr int CPL = D / 32;  // output columns per lane
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int S = gridDim.x;
-  // blockIdx.y = (K/V head, chunk of at most 16 of its query heads)
-  const int G_all = H / Hkv;
-  const int n_chunk = (G_all + 15) / 16;
-  const int s = blockIdx.x, hk = blockIdx.y / n_chunk, chunk = blockIdx.y % n_chunk, b = blockIdx.z;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  const int G = min(16, G_all - 16 * chunk);  // query heads served by this CTA
-  uint32_t* err = &g_dec_err;
-
-  // Context of request b, clamped to what its block-table row can address.
-  int Lb = in_range(b, 1, B, err) ? seq_lens[b] : 0;
-  Lb = Lb < 0 ? 0 : (Lb > max_blocks * bs ? max_blocks * bs : Lb);
-  const int n_tiles = (Lb + TK - 1) / TK;
-  const int tps = (n_tiles + S - 1) / S;  // tiles per split
-  const int tile0 = s * tps;
-  const int tile1 = min(n_tiles, tile0 + tps);
-  const size_t head0 = static_cast<size_t>(b) * H + static_cast<size_t>(hk) * G_all + 16 * chunk;  // first query head
-  const size_t prow = static_cast<size_t>(s) * B * H + head0;                     // its partial row
-  const long long part_rows = static_cast<long long>(S) * B * H;  // rows of o_part and lse_part
-  if (tile0 >= tile1) {  // no key in this split: o_s = 0, lse_s = -inf (weight 0 in the merge)
-    for (int i = tid; i < G * D; i += THREADS)
-      if (in_range(static_cast<long long>(prow) * D + i, 1, part_rows * D, err)) o_part[prow * D + i] = 0.f;
-    if (tid < G && in_range(static_cast<long long>(prow) + tid, 1, part_rows, err)) lse_part[prow + tid] = -INFINITY;
-    return;
-  }
-  const int t_begin = tile0 * TK, t_end = min(Lb, tile1 * TK);
-  const int blk0 = t_begin / bs;
-  const int nblk = (t_end - 1) / bs + 1 - blk0;  // <= kDecodeMaxTable (checked on the host)
-
-  uint8_t* sSlot = smem + L::SLOT_OFF + warp * L::WSLOT;  // this warp's slot of stage 0
-  float* sQ = reinterpret_cast<float*>(smem + L::Q_OFF);
-  float* sW = reinterpret_cast<float*>(smem + L::W_OFF + warp * L::W_BYTES);
-  float* sML = reinterpret_cast<float*>(smem + L::ML_OFF);
-  int* sTab = reinterpret_cast<int*>(smem + L::TAB_OFF);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp;  // [st * WARPS]
-  int* fills = reinterpret_cast<int*>(smem + L::CNT_OFF) + warp;           // [st * WARPS]
-
-  for (int i = tid; i < GM * D; i += THREADS) {
-    const int g = i / D;
-    const long long qi = static_cast<long long>(head0 + g) * D + (i % D);
-    sQ[i] = g < G && in_range(qi, 1, static_cast<long long>(B) * H * D, err)
-                ? __bfloat162float(q[qi]) * scale_log2
-                : 0.f;
-  }
-  for (int i = tid; i < nblk; i += THREADS) {
-    const long long ti = static_cast<long long>(b) * max_blocks + blk0 + i;
-    if (in_range(i, 1, kDecodeMaxTable, err))
-      sTab[i] = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
-  }
-  if (lane == 0) {
-    for (int st = 0; st < NST; ++st) {
-      fills[st * WARPS] = 0;
-      mbar_init(&full[st * WARPS], 1);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // One warp: copy its 8 keys of tile `tile` (K rows, then V rows) into its
-  // slot of stage st. Lane r takes the r-th run of consecutive tokens inside
-  // one cache block. Entries outside [0, num_blocks) are never dereferenced:
-  // their copies are skipped and the error is reported, and their rows of the
-  // slot keep stale bytes, so the results of that request are undefined.
-  // Only copied bytes are expected on the barrier.
-  const bool single_run = (bs & 7) == 0;  // a warp's 8 keys never cross a block boundary
-  const long long cache_elems = static_cast<long long>(num_blocks) * Hkv * bs * D;
-  // Table entry blk may be read for rows [row0, row0 + nrows) of head hk.
-  auto copy_ok = [&](int blk, int row0, int nrows) {
-    return blk >= 0 && blk < num_blocks &&
-           in_range((static_cast<long long>(blk) * Hkv + hk) * bs * D + static_cast<long long>(row0) * D,
-                    static_cast<long long>(nrows) * D, cache_elems, err);
-  };
-  auto issue = [&](int tile, int st) {
-    const int t0 = tile * TK + warp * 8, t1 = min(t_end, t0 + 8);
-    if (single_run) {  // lane 0 alone: one table entry, two copies
-      if (lane == 0) {
-        ++fills[st * WARPS];
-        uint32_t nbytes = 0;
-        int blk = -1, off = 0;
-        if (t0 < t1) {
-          const int bi = t0 / bs;  // the only division per tile
-          off = t0 - bi * bs;
-          blk = in_range(bi - blk0, 1, nblk, err) ? sTab[bi - blk0] : -1;
-          if (copy_ok(blk, off, t1 - t0)) nbytes = static_cast<uint32_t>(t1 - t0) * L::ROW;
-          else atomicExch(err, DEV_BAD_INDEX);
-        }
-        mbar_arrive_expect_tx(&full[st * WARPS], 2 * nbytes);
-        if (nbytes) {
-          uint8_t* slot = sSlot + st * WARPS * L::WSLOT;
-          const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + off) * D;
-          bulk_load(slot, k_cache + src, nbytes, &full[st * WARPS]);
-          bulk_load(slot + 8 * L::ROW, v_cache + src, nbytes, &full[st * WARPS]);
-        }
-      }
-      __syncwarp();
-      return;
-    }
-    const int b0 = t0 / bs;  // the only division per tile
-    const int nrun = t0 < t1 ? (t1 - 1) / bs - b0 + 1 : 0;
-    uint32_t bytes = 0;
-    for (int r = lane; r < nrun; r += 32) {
-      const int blk = in_range(b0 + r - blk0, 1, nblk, err) ? sTab[b0 + r - blk0] : -1;
-      const int rs = max(t0, (b0 + r) * bs), re = min(t1, (b0 + r + 1) * bs);
-      if (copy_ok(blk, rs - (b0 + r) * bs, re - rs)) bytes += static_cast<uint32_t>(re - rs) * L::ROW;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-    if (lane == 0) {
-      ++fills[st * WARPS];
-      mbar_arrive_expect_tx(&full[st * WARPS], 2 * bytes);
-    }
-    __syncwarp();
-    uint8_t* slot = sSlot + st * WARPS * L::WSLOT;
-    for (int r = lane; r < nrun; r += 32) {
-      const int blk = in_range(b0 + r - blk0, 1, nblk, err) ? sTab[b0 + r - blk0] : -1;
-      const int rs = max(t0, (b0 + r) * bs), re = min(t1, (b0 + r + 1) * bs);
-      if (copy_ok(blk, rs - (b0 + r) * bs, re - rs)) {
-        const size_t src = ((static_cast<size_t>(blk) * Hkv + hk) * bs + (rs - (b0 + r) * bs)) * D;
-        const uint32_t dst = static_cast<uint32_t>(rs - t0) * L::ROW;
-        const uint32_t nbytes = static_cast<uint32_t>(re - rs) * L::ROW;
-        bulk_load(slot + dst, k_cache + src, nbytes, &full[st * WARPS]);
-        bulk_load(slot + 8 * L::ROW + dst, v_cache + src, nbytes, &full[st * WARPS]);
-      } else {
-        atomicExch(err, DEV_BAD_INDEX);
-      }
-    }
-  };
-
-  // Scores: 8 lanes per key (lane = 8·kw + dq); lane dq covers the 16-byte
-  // chunks dq (and dq + 8 when d = 128) of the row, so the 8 lanes of a load
-  // phase hit distinct banks. Four heads at a time; their q slices stay in
-  // registers for the whole sweep when G <= 4.
-  constexpr int CH = D / 64;
-  const int dq = lane & 7, kw = lane >> 3;
-  float2 qr[4][CH * 4];
-  auto load_q = [&](int hg) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int ch = 0; ch < CH; ++ch) {
-        const float* src = sQ + (hg * 4 + j) * D + (dq + 8 * ch) * 8;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qr[j][ch * 4 + i] = make_float2(src[2 * i], src[2 * i + 1]);
-      }
-  };
-  if (GM == 4) load_q(0);
-
-  // Per-warp state: lanes 8j .. 8j + 7 hold (m, l) of head 4·hg + j; every
-  // lane holds output columns CPL·lane .. + CPL - 1 of every head.
-  float m_run[GM / 4], l_run[GM / 4];
-#pragma unroll
-  for (int hg = 0; hg < GM / 4; ++hg) {
-    m_run[hg] = -INFINITY;
-    l_run[hg] = 0.f;
-  }
-  float2 acc[GM][CPL / 2];
-#pragma unroll
-  for (int g = 0; g < GM; ++g)
-#pragma unroll
-    for (int c = 0; c < CPL / 2; ++c) acc[g][c] = make_float2(0.f, 0.f);
-
-  // The first NST tiles fill every slot of this warp.
-  __syncthreads();  // barrier inits and the table slice are visible
-  for (int j = 0; j < NST && tile0 + j < tile1; ++j) issue(tile0 + j, j);
-  bool ok = true;
-  int it = 0;
-  for (int tile = tile0; tile < tile1; ++tile, ++it) {
-    const int st = it % NST;
-    ok = mbar_wait_warp(&full[st * WARPS], (it / NST) & 1, err);
-    if (!ok) break;
-    const int nk = min(t_end, (tile + 1) * TK) - tile * TK;
-    const uint8_t* kt = sSlot + st * WARPS * L::WSLOT;  // this warp's 8 K rows, then its 8 V rows
-    const uint32_t* vt = reinterpret_cast<const uint32_t*>(kt + 8 * L::ROW);
-#pragma unroll
-    for (int hg = 0; hg < GM / 4; ++hg) {
-      if (hg * 4 >= G) continue;  // warp-uniform
-      if (GM > 4) load_q(hg);
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int kk = p * 4 + kw;  // key within the warp's eight
-        const int k = warp * 8 + kk;
-        float2 a[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a[j] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int ch = 0; ch < CH; ++ch) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(kt + kk * L::ROW + (dq + 8 * ch) * 16);
-          const float2 k0 = bf2_to_f2(kv.x), k1 = bf2_to_f2(kv.y), k2 = bf2_to_f2(kv.z), k3 = bf2_to_f2(kv.w);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            a[j] = fma2(k0, qr[j][ch * 4 + 0], a[j]);
-            a[j] = fma2(k1, qr[j][ch * 4 + 1], a[j]);
-            a[j] = fma2(k2, qr[j][ch * 4 + 2], a[j]);
-            a[j] = fma2(k3, qr[j][ch * 4 + 3], a[j]);
-          }
-        }
-        const float s0 = a[0].x + a[0].y, s1 = a[1].x + a[1].y;
-        const float s2 = a[2].x + a[2].y, s3 = a[3].x + a[3].y;
-        // Reduce-scatter over the key's 8 lanes: 4 shuffles leave lane pair
-        // (dq, dq ^ 1) with the full score of head j = 2·bit2 + bit1.
-        const bool hi = dq & 4, mid = dq & 2;
-        const float t0 = __shfl_xor_sync(0xffffffffu, hi ? s0 : s2, 4);
-        const float t1 = __shfl_xor_sync(0xffffffffu, hi ? s1 : s3, 4);
-        const float a0 = (hi ? s2 : s0) + t0, a1 = (hi ? s3 : s1) + t1;
-        float r = (mid ? a1 : a0) + __shfl_xor_sync(0xffffffffu, mid ? a0 : a1, 2);
-        r += __shfl_xor_sync(0xffffffffu, r, 1);
-        const int j = (hi ? 2 : 0) + (mid ? 1 : 0);
-        // Rows past the context end hold stale bytes: their score is -inf
-        // whatever r is.
-        if ((dq & 1) == 0) sW[j * 8 + kk] = (k < nk && hg * 4 + j < G) ? r : -INFINITY;
-      }
-      __syncwarp();
-      // Online softmax of the warp's 8 keys: lane = 8j + kk holds head j, key kk.
-      float pr, al;
-      {
-        const int j = lane >> 3;
-        const float sc = sW[lane];
-        float mx = sc;
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        const float m_new = fmaxf(m_run[hg], mx);
-        if (m_new == -INFINITY) {  // no key of this head seen by the warp yet
-          pr = 0.f;
-          al = 1.f;
-        } else {
-          pr = ex2(sc - m_new);
-          al = ex2(m_run[hg] - m_new);
-        }
-        float sum = pr;
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        l_run[hg] = l_run[hg] * al + sum;
-        m_run[hg] = m_new;
-        (void)j;
-      }
-      __syncwarp();
-      // (p, p) pairs, key-major: [kk][head j][2]; alphas of the 4 heads after.
-      sW[((lane & 7) * 4 + (lane >> 3)) * 2] = pr;
-      sW[((lane & 7) * 4 + (lane >> 3)) * 2 + 1] = pr;
-      if ((lane & 7) == 0) sW[64 + (lane >> 3)] = al;
-      __syncwarp();
-      // Output columns: acc_j = α_j·acc_j + Σ_kk P_j,kk · V_kk[cols].
-      {
-        const float4 al4 = *reinterpret_cast<const float4*>(sW + 64);
-        const float alj[4] = {al4.x, al4.y, al4.z, al4.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int c = 0; c < CPL / 2; ++c)
-            acc[hg * 4 + j][c] = make_float2(acc[hg * 4 + j][c].x * alj[j], acc[hg * 4 + j][c].y * alj[j]);
-        auto pv_key = [&](int kk) {
-          const uint32_t* vr = vt + kk * (D / 2) + lane * (CPL / 2);
-          float2 v[CPL / 2];
-#pragma unroll
-          for (int c = 0; c < CPL / 2; ++c) v[c] = bf2_to_f2(vr[c]);
-          const float4 p01 = *reinterpret_cast<const float4*>(sW + kk * 8);
-          const float4 p23 = *reinterpret_cast<const float4*>(sW + kk * 8 + 4);
-          const float2 pp[4] = {make_float2(p01.x, p01.y), make_float2(p01.z, p01.w),
-                                make_float2(p23.x, p23.y), make_float2(p23.z, p23.w)};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int c = 0; c < CPL / 2; ++c) acc[hg * 4 + j][c] = fma2(v[c], pp[j], acc[hg * 4 + j][c]);
-        };
-        if (warp * 8 + 8 <= nk) {
-          // All 8 rows hold copied keys (every tile but a context's last):
-          // a branch-free loop whose shared-memory loads can be hoisted.
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) pv_key(kk);
-        } else {
-          // Rows past the context end were never copied (P is 0 there, and
-          // their bytes may be anything): skip them, warp-uniformly.
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            if (warp * 8 + kk >= nk) break;
-            pv_key(kk);
-          }
-        }
-      }
-      __syncwarp();  // the scratch is rewritten by the next head group
-    }
-    // This warp has read its slot of stage st: refill it.
-    if (tile + NST < tile1) issue(tile + NST, st);
-  }
-  if (__syncthreads_or(!ok)) {
-    // Let copies already issued land before the CTA exits (bounded).
-    if (lane == 0)
-      for (int st = 0; st < NST; ++st)
-        if (fills[st * WARPS] > 0) mbar_wait(&full[st * WARPS], (fills[st * WARPS] - 1) & 1, err);
-    return;
-  }
-  // Merge the warps' states per head: M = max_w m_w, L = Σ_w l_w 2^(m_w − M),
-  // o = Σ_w acc_w 2^(m_w − M) / L, lse = (M + log2 L)·ln 2.
-  float* sAcc = reinterpret_cast<float*>(smem + L::SLOT_OFF);  // [WARPS][GM][D]; the stages are idle
-#pragma unroll
-  for (int g = 0; g < GM; ++g)
-#pragma unroll
-    for (int c = 0; c < CPL / 2; ++c)
-      *reinterpret_cast<float2*>(sAcc + (warp * GM + g) * D + lane * CPL + 2 * c) = acc[g][c];
-#pragma unroll
-  for (int hg = 0; hg < GM / 4; ++hg)
-    if ((lane & 7) == 0) {
-      sML[(warp * 2 + 0) * GM + hg * 4 + (lane >> 3)] = m_run[hg];
-      sML[(warp * 2 + 1) * GM + hg * 4 + (lane >> 3)] = l_run[hg];
-    }
-  __syncthreads();
-  for (int i = tid; i < G * D; i += THREADS) {
-    const int g = i / D, c = i % D;
-    float M = -INFINITY;
-    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sML[(w * 2) * GM + g]);
-    float Ls = 0.f, u = 0.f;
-    for (int w = 0; w < WARPS; ++w) {
-      const float mw = sML[(w * 2) * GM + g];
-      if (mw == -INFINITY) continue;
-      const float f = ex2(mw - M);
-      Ls += sML[(w * 2 + 1) * GM + g] * f;
-      u += sAcc[(w * GM + g) * D + c] * f;
-    }
-    if (in_range(static_cast<long long>(prow + g) * D + c, 1, part_rows * D, err)) o_part[(prow + g) * D + c] = u / Ls;
-    if (c == 0 && in_range(static_cast<long long>(prow) + g, 1, part_rows, err))
-      lse_part[prow + g] = (M + __log2f(Ls)) * LN2;
-  }
 }
 
 // One warp per output row: o = Σ_s e^(lse_s − lse) o_s, lse = ln Σ_s e^(lse_s).
@@ -483,66 +85,38 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
   if (lane == 0 && in_range(row, 1, rows, err)) lse[row] = l > 0.f ? m + __logf(l) : -INFINITY;
 }
 
-template <int D, int GM>
-static cudaError_t launch_partial_t(const void* q, const void* kc, const void* vc, const int* table,
-                                    const int* seq_lens, float* o_part, float* lse_part, int B, int H,
-                                    int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
-                                    cudaStream_t stream) {
-  auto kern = decode_partial_kernel<D, GM>;
-  const int smem = Smem<D, GM>::BYTES;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const int n_chunk = (H / Hkv + 15) / 16;  // CTAs per K/V head (16 query heads each at most)
-  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(Hkv * n_chunk), static_cast<unsigned>(B));
-  kern<<<grid, THREADS, smem, stream>>>(static_cast<const __nv_bfloat16*>(q),
-                                         static_cast<const __nv_bfloat16*>(kc),
-                                         static_cast<const __nv_bfloat16*>(vc), table, seq_lens, o_part,
-                                         lse_part, B, H, Hkv, num_blocks, bs, max_blocks,
-                                         scale * LOG2E);
-  return cudaGetLastError();
-}
-
-template <int D>
-static cudaError_t launch_partial_d(const void* q, const void* kc, const void* vc, const int* table,
-                                    const int* seq_lens, float* o_part, float* lse_part, int B, int H,
-                                    int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
-                                    cudaStream_t stream) {
-  const int G = H / Hkv;
-  if (G <= 4)
-    return launch_partial_t<D, 4>(q, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                                  max_blocks, scale, S, stream);
-  if (G <= 8)
-    return launch_partial_t<D, 8>(q, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                                  max_blocks, scale, S, stream);
-  return launch_partial_t<D, 16>(q, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                                 max_blocks, scale, S, stream);
-}
-
 }  // namespace dec
 
 // ----------------------------------------------------------------------------
-// The same decode step on the tensor cores (d = 64 or 128; cache blocks of
-// 8, 16, 32, 64 or 128 tokens).
+// The decode step on the tensor cores (d = 64 or 128, any cache block size).
 //
-// The FMA-pipe kernel above issues about 140 warp instructions per KB of K/V
-// (converting bf16 rows, 8-lane dot products, shuffles), and that instruction
-// stream, not HBM, sets its rate. Here both products of a 128-key tile run on
-// the tensor core with the tile's keys as M, so the work per key is a few
+// The work per K/V byte is small (G·d multiply-adds per key and head pair),
+// but done on the FMA pipe its instruction stream, not HBM, sets the rate:
+// converting bf16 rows, dot products and shuffles came to about 140 warp
+// instructions per KB. Here both products of a 128-key tile run on the
+// tensor core with the tile's keys as M, so the work per key is a few
 // instructions of softmax:
 //   Sᵀ = K Qᵀ    M = 128 keys, N = 16 query heads (padded), K = d; into TMEM
 //   Oᵀ += Vᵀ Pᵀ  M = 128 dims (d = 64: padded by a zero panel), N = 16 heads,
 //                K = 128 keys; accumulated in TMEM
 // One thread per TMEM lane: lane r is key r of the tile in Sᵀ and dimension r
-// in Oᵀ. Each cache block of the tile arrives as its own TMA box (the cache
-// viewed as (d, block_size, num_blocks·Hkv)), written at row offset
-// block·block_size of the 128-row tile; a block past the context or with a
-// table entry outside [0, num_blocks) is requested at an out-of-range
-// coordinate, so the box reads zeros and the entry is never dereferenced.
+// in Oᵀ. K and V tiles reach shared memory in the 128-byte-swizzled K-major
+// layout the products read, one of two ways:
+//   boxes   block size a multiple of 8 dividing 128: each cache block of the
+//           tile is its own TMA box (the cache viewed as (d, block_size,
+//           num_blocks·Hkv)) at row offset block·block_size of the tile; a
+//           block past the context or with a table entry outside
+//           [0, num_blocks) is requested at an out-of-range coordinate, so
+//           the box reads zeros and the entry is never dereferenced.
+//   gather  any other block size: the producer warp's lanes look up each
+//           token's block and copy its row in 16-byte pieces to the
+//           swizzled position (zero fill for the same two cases).
 // The softmax keeps one exponent reference per head, raised (and Oᵀ's column
 // rescaled) when a key outgrows it by more than 2^8, as in the forward.
-// Roles (224 threads): warp 0 loads K tiles (2 stages), warp 1 V tiles
-// (1 stage), warp 2 owns TMEM and issues the products, warps 3..6 run the
-// softmax and the epilogue. Two CTAs fit an SM.
+// Roles (224 threads): warp 0 loads K tiles, warp 1 V tiles (lane 0 for
+// boxes, the whole warp to gather), warp 2 owns TMEM and issues the
+// products, warps 3..6 run the softmax and the epilogue. Two or three CTAs
+// share an SM.
 namespace decmma {
 
 constexpr int TK = 128;       // keys per tile (M of the score product)
@@ -586,10 +160,15 @@ struct Smem {
   static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
 };
 
-template <int D, int GM>
+// GATHER: the cache's block size does not tile a 128-key tile into whole
+// 8-row swizzle groups (a multiple of 8 dividing 128), so K and V arrive by
+// per-token 16-byte copies instead of one TMA box per cache block; tk and tv
+// are then unused and kc, vc are read directly.
+template <int D, int GM, bool GATHER>
 __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-    const __grid_constant__ CUtensorMap tv, const int* __restrict__ block_table,
+    const __grid_constant__ CUtensorMap tv, const __nv_bfloat16* __restrict__ kc,
+    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table,
     const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B, int H,
     int Hkv, int num_blocks, int bs, int max_blocks, float scale_log2) {
   constexpr int KST = Cfg<GM>::KST, VST = Cfg<GM>::VST, PB = Cfg<GM>::PB;
@@ -645,12 +224,13 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    // Gathered tiles: one arrival per producer lane once its copies landed.
     for (int i = 0; i < KST; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], GATHER ? 32 : 1);
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < VST; ++i) {
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], GATHER ? 32 : 1);
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
@@ -688,7 +268,92 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     }
   };
 
-  if (warp == 0) {
+  // The same tile by per-token copies, run by a whole warp. resolve() looks
+  // up where rows lane, lane + 32, lane + 64 and lane + 96 of a tile live
+  // (element offset, or -1: past the context or a bad block index, zero
+  // fill); copy_tile() then moves chunk c (16 bytes) of row r into the
+  // 128-byte-swizzled K-major layout the products read: panel c / 8, at
+  // 128 r + 16 ((c mod 8) xor (r mod 8)).
+  const long long cache_elems = static_cast<long long>(num_blocks) * Hkv * bs * D;
+  auto resolve = [&](int tile, long long (&row_off)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = tile * TK + lane + 32 * u;
+      long long off = -1;
+      if (t < Lb) {
+        const int bi = t / bs;
+        const long long ti = static_cast<long long>(b) * max_blocks + bi;
+        const int blk = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
+        if (blk >= 0 && blk < num_blocks)
+          off = ((static_cast<long long>(blk) * Hkv + hk) * bs + (t - bi * bs)) * D;
+        else
+          atomicExch(err, DEV_BAD_INDEX);
+      }
+      row_off[u] = off;
+    }
+  };
+  auto copy_tile = [&](const __nv_bfloat16* cache, uint8_t* dst, const long long (&row_off)[4]) {
+    constexpr int CH = D / 8;     // 16-byte chunks per row
+    constexpr int RPI = 32 / CH;  // rows per warp instruction
+    const int c = lane % CH, rsub = lane / CH;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll 4
+      for (int r1 = 0; r1 < 32; r1 += RPI) {
+        const int r = 32 * u + r1 + rsub;
+        const long long off = __shfl_sync(0xffffffffu, row_off[u], r1 + rsub);
+        const bool live = off >= 0 && in_range(off + c * 8, 8, cache_elems, err);
+        cp_async_16(dst + (c >> 3) * L::PANEL + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                    live ? cache + off + c * 8 : cache, live ? 16u : 0u);
+      }
+    }
+  };
+  // Producer loop of the gathered path (NST stages; the whole warp). The
+  // next tile's rows are looked up while this tile's copies are in flight.
+  // A tile's full barrier gets each lane's arrival once that lane's copies
+  // completed and were fenced for the tensor core; with two stages the
+  // wait trails the issue by one tile, so two tiles' copies overlap.
+  auto gather_loop = [&](const __nv_bfloat16* cache, uint8_t* base, int stage_bytes, uint64_t* full,
+                         uint64_t* empty, auto nst_c) {
+    constexpr int NST = decltype(nst_c)::value;
+    long long cur[4], nxt[4] = {-1, -1, -1, -1};
+    resolve(tile0, cur);
+    int j = 0;
+    for (; j < n_t; ++j) {
+      const int st = j % NST;
+      if (!mbar_wait_warp(&empty[st], ((j / NST) & 1) ^ 1, err)) break;
+      copy_tile(cache, base + st * stage_bytes, cur);
+      cp_async_commit();
+      if (j + 1 < n_t) resolve(tile0 + j + 1, nxt);
+      if (NST == 1 || j >= 1) {
+        cp_async_wait<NST - 1>();
+        fence_async_smem();
+        mbar_arrive(&full[(j - (NST - 1)) % NST]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+    }
+    cp_async_wait<0>();  // nothing may land after the CTA exits
+    if (NST > 1 && j == n_t && n_t >= 1) {
+      fence_async_smem();
+      mbar_arrive(&full[(n_t - 1) % NST]);
+    }
+  };
+
+  if (GATHER && warp <= 1) {
+    // ------------------------------------ K (warp 0) and V (warp 1) producers
+    if (warp == 0 && lane == 0) {
+      prefetch_tmap(&tq);
+      mbar_arrive_expect_tx(q_full, L::KPANELS * L::QPANEL);
+      for (int p = 0; p < L::KPANELS; ++p) tma_load_3d(sQ + p * L::QPANEL, &tq, q_full, p * 64, head0, 0);
+    }
+    __syncwarp();
+    if (warp == 0)
+      gather_loop(kc, sK, L::K_TILE, k_full, k_empty, std::integral_constant<int, KST>{});
+    else
+      gather_loop(vc, sV, L::V_TILE, v_full, v_empty, std::integral_constant<int, VST>{});
+    if (warp == 0 && lane == 0) mbar_wait(q_full, 0, err);
+  } else if (warp == 0) {
     // --------------------------------------------------------- K producer
     if (lane == 0) {
       prefetch_tmap(&tq);
@@ -905,19 +570,38 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   }
 }
 
-template <int D, int GM>
-static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const int* table,
-                            const int* seq_lens, float* o_part, float* lse_part, int B, int H, int Hkv,
-                            int num_blocks, int bs, int max_blocks, float scale, int S, cudaStream_t stream) {
+// TMA boxes serve a block size that is a multiple of 8 dividing 128 (each box
+// lands on whole 1024-byte swizzle groups); other sizes gather per token.
+inline bool boxes(int bs) { return bs % 8 == 0 && TK % bs == 0; }
+
+template <int D, int GM, bool GATHER>
+static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const void* kc,
+                            const void* vc, const int* table, const int* seq_lens, float* o_part, float* lse_part,
+                            int B, int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
+                            cudaStream_t stream) {
   using C = Cfg<GM>;
   const int smem = Smem<D, C::KST, C::VST, C::PB>::ALLOC;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = decode_mma_kernel<D, GM, GATHER>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_chunk = (H / Hkv + NH - 1) / NH;
   const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(Hkv * n_chunk), static_cast<unsigned>(B));
-  decode_mma_kernel<D, GM><<<grid, THREADS, smem, stream>>>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv,
-                                                         num_blocks, bs, max_blocks, scale * dec::LOG2E);
+  kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, static_cast<const __nv_bfloat16*>(kc),
+                                        static_cast<const __nv_bfloat16*>(vc), table, seq_lens, o_part, lse_part, B, H,
+                                        Hkv, num_blocks, bs, max_blocks, scale * dec::LOG2E);
   return cudaGetLastError();
+}
+
+template <int D, int GM>
+static cudaError_t launch_g(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const void* kc,
+                            const void* vc, const int* table, const int* seq_lens, float* o_part, float* lse_part,
+                            int B, int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
+                            cudaStream_t stream) {
+  if (boxes(bs))
+    return launch_t<D, GM, false>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                                  max_blocks, scale, S, stream);
+  return launch_t<D, GM, true>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                               max_blocks, scale, S, stream);
 }
 
 template <int D>
@@ -925,18 +609,23 @@ static cudaError_t launch_d(const void* q, const void* kc, const void* vc, const
                             float* o_part, float* lse_part, int B, int H, int Hkv, int num_blocks, int bs,
                             int max_blocks, float scale, int S, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16(&tq, q, 1, B * H, D, NH) || !make_tmap_bf16(&tk, kc, num_blocks * Hkv, bs, D, bs) ||
-      !make_tmap_bf16(&tv, vc, num_blocks * Hkv, bs, D, bs))
-    return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tq, q, 1, B * H, D, NH)) return cudaErrorInvalidValue;
+  if (boxes(bs)) {
+    if (!make_tmap_bf16(&tk, kc, num_blocks * Hkv, bs, D, bs) || !make_tmap_bf16(&tv, vc, num_blocks * Hkv, bs, D, bs))
+      return cudaErrorInvalidValue;
+  } else {
+    tk = tq;  // unused: the gathered path reads the caches directly
+    tv = tq;
+  }
   const int G = H / Hkv;  // query heads per K/V head; CTAs take them 16 at a time
   if (G <= 4)
-    return launch_t<D, 4>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks,
-                          scale, S, stream);
+    return launch_g<D, 4>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                          max_blocks, scale, S, stream);
   if (G <= 8)
-    return launch_t<D, 8>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks,
-                          scale, S, stream);
-  return launch_t<D, 16>(tq, tk, tv, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs, max_blocks,
-                         scale, S, stream);
+    return launch_g<D, 8>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                          max_blocks, scale, S, stream);
+  return launch_g<D, 16>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                         max_blocks, scale, S, stream);
 }
 
 static cudaError_t launch(const void* q, const void* kc, const void* vc, const int* table, const int* seq_lens,
@@ -948,8 +637,8 @@ static cudaError_t launch(const void* q, const void* kc, const void* vc, const i
                                  max_blocks, scale, S, stream);
 }
 
-// Shapes this kernel serves; the others take the FMA-pipe kernel.
-inline bool serves(int d, int bs) { return (d == 64 || d == 128) && bs % 8 == 0 && TK % bs == 0; }
+// Shapes this kernel serves (any block size).
+inline bool serves(int d, int bs) { return (d == 64 || d == 128) && bs >= 1; }
 
 }  // namespace decmma
 
@@ -970,17 +659,9 @@ cudaError_t launch_decode_paged(const void* q, const void* k_cache, const void* 
                                 float* o_part, float* lse_part, int B, int H, int Hkv, int d,
                                 int num_blocks, int block_size, int max_blocks, float scale, int S,
                                 cudaStream_t stream) {
-  if (decmma::serves(d, block_size)) {
-    cudaError_t e = decmma::launch(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H, Hkv, d,
-                                   num_blocks, block_size, max_blocks, scale, S, stream);
-    if (e != cudaSuccess) return e;
-    return launch_attn_merge(o_part, lse_part, S, o, lse, static_cast<long long>(B) * H, d, stream);
-  }
-  cudaError_t e =
-      d == 64 ? dec::launch_partial_d<64>(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H,
-                                          Hkv, num_blocks, block_size, max_blocks, scale, S, stream)
-              : dec::launch_partial_d<128>(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B,
-                                           H, Hkv, num_blocks, block_size, max_blocks, scale, S, stream);
+  if (!decmma::serves(d, block_size)) return cudaErrorInvalidValue;
+  cudaError_t e = decmma::launch(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H, Hkv, d,
+                                 num_blocks, block_size, max_blocks, scale, S, stream);
   if (e != cudaSuccess) return e;
   return launch_attn_merge(o_part, lse_part, S, o, lse, static_cast<long long>(B) * H, d, stream);
 }

@@ -321,12 +321,14 @@ int fa_attn_merge(const float* o_parts, const float* lse_parts, int n_parts, voi
  *                context length); query head h reads K/V head h / (H/Hkv).
  *   workspace    device buffer of fa_decode_workspace_bytes(B, H, d,
  *                n_splits) bytes (16-byte aligned), for the partial results.
+ *   block_size   any size >= 1. Sizes that are a multiple of 8 dividing 128
+ *                load each cache block as one TMA box; others are gathered
+ *                token by token (fewer bytes per second).
  *   n_splits     the context of every request is cut into n_splits parts of
- *                whole 64-token tiles, processed in parallel and combined
+ *                whole 128-token tiles, processed in parallel and combined
  *                as in fa_attn_merge (two kernels on `stream`).
  * Errors: null pointer, sizes < 1, Hkv not dividing H, bad scale ->
- * FA_ERR_INVALID_ARG; d not 64/128, B > 65535, Hkv·ceil(H/Hkv / 16) > 65535,
- * a split that could span more than 1024 cache blocks (use more splits) ->
+ * FA_ERR_INVALID_ARG; d not 64/128, B > 65535, Hkv·ceil(H/Hkv / 16) > 65535 ->
  * FA_ERR_UNSUPPORTED; short workspace -> FA_ERR_WORKSPACE; misaligned ->
  * FA_ERR_MISALIGNED. A block-table entry outside [0, num_blocks) is never
  * dereferenced: the tokens it maps are skipped (the results are then

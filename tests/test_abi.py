@@ -158,7 +158,7 @@ def test_decode_and_merge_argument_errors(L):
     assert dec(scale=-1.0) == 1
     assert dec(d=96) == 2
     assert dec(B=70000) == 2                  # more requests than one grid dimension holds
-    assert dec(max_blocks=100000, S=1) == 2   # a split could span > 1024 blocks
+    assert dec(max_blocks=1 << 27, bs=16) == 2   # a context of 2^31 tokens: past the int range
     assert dec(ws_ptr=NUL) == 6
     assert dec(ws_bytes=ws - 1) == 6
     assert dec(q=MIS) == 3

@@ -56,10 +56,15 @@ def run_case(fa, q, kc, vc, table, lens, n_splits, scale):
     (1, 2, 1, 64, 48, [2000], 7),            # block size not a power of two
     (2, 32, 1, 128, 16, [300, 1500], 3),     # 32 query heads on one K/V head: two CTAs of 16
     (1, 24, 1, 64, 32, [777], 2),            # 24 = 16 + 8
-    # blocks of 8 to 128 tokens run on the tensor cores (1 and 48 above on the FMA pipe)
+    # blocks that are a multiple of 8 dividing 128 arrive as TMA boxes; 1, 48
+    # above and the sizes below are gathered token by token
     (2, 8, 2, 128, 8, [100, 37], 2),         # eight-token blocks: 16 boxes per tile
     (2, 12, 3, 128, 64, [700, 129], 3),      # 64-token blocks
     (1, 40, 5, 128, 16, [1025], 4),          # 8 query heads per K/V head
+    (2, 16, 2, 128, 3, [700, 131], 2),       # gathered, 8 query heads per K/V head
+    (2, 32, 2, 64, 5, [900, 1], 3),          # gathered, 16 heads per K/V head (two K stages)
+    (1, 16, 1, 128, 1, [3000], 1),           # one split over 3000 one-token blocks
+    (1, 4, 1, 128, 200, [1000], 2),          # blocks larger than a tile
 ])
 def test_decode_paged_vs_oracle(fa, B, H, Hkv, d, bs, seq_lens, n_splits):
     q, kc, vc, table, lens = paged_case(B, H, Hkv, d, bs, seq_lens, seed=B * 100 + H + bs + sum(seq_lens))
@@ -82,10 +87,10 @@ def test_decode_split_count_does_not_change_the_result(fa):
         assert (lse - outs[0][1]).abs().max() <= 1e-4
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_decode_bad_block_index_is_reported_not_read(fa, d):
-    # both head sizes run the tensor-core kernel with 16-token blocks
-    q, kc, vc, table, lens = paged_case(2, 4, 2, d, 16, [40, 40], seed=9)
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 16), (128, 3)])
+def test_decode_bad_block_index_is_reported_not_read(fa, d, bs):
+    # TMA boxes (16-token blocks) and per-token gathering (3-token blocks)
+    q, kc, vc, table, lens = paged_case(2, 4, 2, d, bs, [40, 40], seed=9)
     table[1, 1] = kc.shape[0] + 5  # outside the cache
     fa.decode_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), lens.cuda(), n_splits=2)
     assert fa.last_device_error() == 7  # FA_ERR_BAD_INDEX
