@@ -6,7 +6,7 @@ its grouped-query form with 8 K/V heads), bf16 inputs
 drawn from the seeded generator. Prints one JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c4|c2|c5|c3|c1|g4|s1|s2|d1]
+                    [--workload c4|c2|c5|c3|c1|g4|s1|s2|d1|d2]
 
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (the path shards by independent heads; there is no data exchange), timing
@@ -17,7 +17,8 @@ cores, one bounded sample (one head's forward + backward) per step.
 
 ``--workload s1|s2`` instead times the standalone row softmax kernels (the
 two-pass online form against the three-pass safe form) and reports GB/s;
-``--workload d1`` times one paged-KV decode step and reports K/V GB/s.
+``--workload d1`` times one paged-KV decode step and reports K/V GB/s (``d2``:
+the same step with one-token cache blocks).
 """
 from __future__ import annotations
 

@@ -119,8 +119,8 @@ ROW_WORKLOADS = {
 @dataclass(frozen=True)
 class DecodeWorkload:
     """One decode step of B requests against a paged KV cache: context
-    lengths drawn uniformly from [min_len, max_len], 16-token blocks placed
-    in a random order, q, K, V ~ N(0, 1) in bf16."""
+    lengths drawn uniformly from [min_len, max_len], cache blocks of
+    block_size tokens placed in a random order, q, K, V ~ N(0, 1) in bf16."""
     name: str
     B: int
     H: int
@@ -137,6 +137,9 @@ DECODE_WORKLOADS = {
     # 32 requests with 2k-8k cached tokens, Llama-3-8B heads (32 over 8):
     # about 670 MB of K and V read per step, more than L2
     "d1": DecodeWorkload("d1", 32, 32, 8, 128, 16, 2048, 8192, 8, 3001),
+    # the same step with one token per cache block (page size 1): the
+    # blocks do not tile into TMA boxes and are gathered token by token
+    "d2": DecodeWorkload("d2", 32, 32, 8, 128, 1, 2048, 8192, 8, 3001),
 }
 
 

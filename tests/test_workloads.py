@@ -1,6 +1,8 @@
 """The seeded input generators that feed both the CUDA path and the oracle:
 the documented recipe (generator, draw order, scaling, bf16 rounding), the
 workload table, and the invariants of the paged decode inputs. CPU only."""
+import dataclasses
+
 import torch
 
 from exact_tiled_attention_24_gb300.workloads import (DECODE_WORKLOADS, ROW_WORKLOADS, WORKLOADS, DecodeWorkload,
@@ -58,6 +60,9 @@ def test_rows_generator():
 def test_decode_generator_invariants():
     d1 = DECODE_WORKLOADS["d1"]
     assert (d1.B, d1.H, d1.Hkv, d1.d, d1.block_size, d1.min_len, d1.max_len) == (32, 32, 8, 128, 16, 2048, 8192)
+    # d2: the same step and draws with one-token blocks
+    d2 = DECODE_WORKLOADS["d2"]
+    assert dataclasses.replace(d2, name="d1", block_size=16) == d1
     # the same generator on a small workload of the same kind
     dw = DecodeWorkload("small", 6, 8, 2, 64, 16, 20, 300, 4, 3101)
     q, kc, vc, table, lens = make_decode(dw, torch.device("cpu"))
