@@ -403,6 +403,10 @@ def run_ours(args, w, rank, world, dist):
         dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
         Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # The backward in the order fa_bwd takes for this shape: the dQ sweep
+    # forming D, then the dK/dV sweep; or the D pass, dK/dV, then dQ (one
+    # stream here, so each kernel is timed on its own).
+    fuse_d = has_bwd and fa.bwd_fuses_d(B, H, kg.shape[1], N, d)
 
     def step(ev=None):
         if ev is not None:
@@ -410,7 +414,16 @@ def run_ours(args, w, rank, world, dist):
         fa.fwd(qg, kg, vg, causal=causal, out=o, lse=lse)
         if ev is not None:
             ev[1].record(stream)
-        if has_bwd:
+        if has_bwd and fuse_d:
+            if ev is not None:
+                ev[2].record(stream)  # no D pass
+            fa.bwd_dq_d(qg, kg, vg, o, dog, lse, Dvec, dq, causal=causal)
+            if ev is not None:
+                ev[3].record(stream)
+            fa.bwd_dkdv(qg, kg, vg, dog, lse, Dvec, dk, dv, causal=causal)
+            if ev is not None:
+                ev[4].record(stream)
+        elif has_bwd:
             fa.bwd_preprocess(o, dog, Dvec)
             if ev is not None:
                 ev[2].record(stream)
@@ -421,7 +434,7 @@ def run_ours(args, w, rank, world, dist):
             if ev is not None:
                 ev[4].record(stream)
 
-    launches_per_step = 4 if has_bwd else 1
+    launches_per_step = (3 if fuse_d else 4) if has_bwd else 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -464,8 +477,9 @@ def run_ours(args, w, rank, world, dist):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     if has_bwd:
         pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-        dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-        dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+        k_a = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+        k_b = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+        dq_ms, dkdv_ms = (k_a, k_b) if fuse_d else (k_b, k_a)
     F_fwd = flops(w, "fwd")
     F_bwd = flops(w, "bwd") if has_bwd else 0
     F_step = F_fwd + F_bwd
@@ -552,6 +566,8 @@ def run_ours(args, w, rank, world, dist):
         result["c5_fwd"] = long_context_leg(args, dev, dist, peaks, peak_kind)
     if has_bwd:
         result["bwd_ms"] = {"preprocess": pre_ms, "dkdv": dkdv_ms, "dq": dq_ms}
+        result["bwd_order"] = ("dq sweep forming D, then dkdv (no D pass)" if fuse_d
+                               else "D pass, dkdv, dq")
         result["bwd_tflops"] = F_bwd / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12
         result["mfu_style_tflops"] = 3 * F_fwd * world / (ms_per_step * 1e-3) / 1e12
     if rank == 0 and not args.no_cpu_baseline:

@@ -22,6 +22,8 @@ __all__ = [
     "bwd_preprocess",
     "bwd_dkdv",
     "bwd_dq",
+    "bwd_dq_d",
+    "bwd_fuses_d",
     "bwd_workspace_bytes",
     "last_device_error",
     "debug_checks",
@@ -64,6 +66,8 @@ EXPORTED_SYMBOLS = (
     "fa_bwd_preprocess",
     "fa_bwd_dkdv",
     "fa_bwd_dq",
+    "fa_bwd_dq_d",
+    "fa_bwd_fuses_d",
     "fa_last_device_error",
     "fa_selftest_wait_limit",
     "fa_status_string",
@@ -119,6 +123,10 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_bwd_dkdv.restype = i
         L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_bwd_dq_d.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_bwd_dq_d.restype = i
+        L.fa_bwd_fuses_d.argtypes = [i, i, i, i, i]
+        L.fa_bwd_fuses_d.restype = i
         L.fa_bwd_dq.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
@@ -284,6 +292,25 @@ def bwd_dkdv(q, k, v, do, lse, Dvec, dk, dv, causal=False, scale=None):
     _check(lib().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dk),
                              _ptr(dv), B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)),
                              _stream(q.device)), "fa_bwd_dkdv")
+
+
+def bwd_dq_d(q, k, v, o, do, lse, Dvec, dq, causal=False, scale=None):
+    """dq (bf16) and Dvec = rowsum(do * o) (fp32), both written in place, by
+    the dQ sweep alone (no preprocess); bwd_dkdv can then read Dvec."""
+    Hkv = _check_inputs(q, k, v, o, do)
+    B, H, N, d = q.shape
+    _expect(lse, "lse", (B, H, N), torch.float32, q.device)
+    _expect(Dvec, "Dvec", (B, H, N), torch.float32, q.device)
+    _expect(dq, "dq", q.shape, torch.bfloat16, q.device)
+    _check(lib().fa_bwd_dq_d(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(Dvec), _ptr(dq),
+                             B, H, Hkv, N, d, _scale(d, scale), int(bool(causal)), _stream(q.device)),
+           "fa_bwd_dq_d")
+
+
+def bwd_fuses_d(B, H, Hkv, N, d):
+    """True when bwd() runs the dQ sweep with D first and the dK/dV sweep
+    after it for these sizes on the current device (see fa_bwd_fuses_d)."""
+    return bool(lib().fa_bwd_fuses_d(int(B), int(H), int(Hkv), int(N), int(d)))
 
 
 def bwd_dq(q, k, v, do, lse, Dvec, dq, causal=False, scale=None):

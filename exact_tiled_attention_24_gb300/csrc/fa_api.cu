@@ -131,6 +131,26 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const
                                     causal != 0, static_cast<cudaStream_t>(stream)));
 }
 
+int fa_bwd_dq_d(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                float* Dvec, void* dq, int B, int H, int Hkv, int N, int d, float scale, int causal,
+                void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !Dvec || !dq) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(Dvec) || !aligned16(dq))
+    return FA_ERR_MISALIGNED;
+  return map_cuda(fa::launch_bwd_dq_d(q, k, v, o, dO, dq, lse, Dvec, B * H, H / Hkv, N, d, scale, causal != 0,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_fuses_d(int B, int H, int Hkv, int N, int d) {
+  if (check_sizes(B, H, N, d) != FA_OK || check_heads(H, Hkv) != FA_OK) return 0;
+  return fa::bwd_fuse_d(B * H, H / Hkv, N) ? 1 : 0;
+}
+
 int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
                const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream) {
@@ -146,6 +166,11 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
   for (const void* p : ptrs)
     if (!aligned16(p)) return FA_ERR_MISALIGNED;
   float* Dvec = static_cast<float*>(workspace);
+  if (fa::bwd_fuse_d(B * H, H / Hkv, N)) {  // D inside the dQ sweep, then dK/dV
+    st = fa_bwd_dq_d(q, k, v, o, dO, lse, Dvec, dq, B, H, Hkv, N, d, scale, causal, stream);
+    if (st != FA_OK) return st;
+    return fa_bwd_dkdv(q, k, v, dO, lse, Dvec, dk, dv, B, H, Hkv, N, d, scale, causal, stream);
+  }
   st = fa_bwd_preprocess(o, dO, Dvec, B, H, N, d, stream);
   if (st != FA_OK) return st;
   // The dQ sweep needs only D: it runs on the library's side stream, forked

@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
 
 constexpr uint32_t Q_COL_S = 0, Q_COL_DP = 128, Q_COL_DQ = 256, Q_COL_Q = 384, Q_COL_DO = 448;
 
-template <int D>
+template <int D, bool FUSE_D>
 struct DqSmem {
   using T = Tiles<D>;
   // Three K/V stages: 0 and 1 are dedicated; stage 2 is the Q/dO region,
@@ -505,7 +505,10 @@ struct DqSmem {
   static constexpr int DO_OFF = Q_OFF + T::BYTES;  // dO tile, then V of stage 2
   static constexpr int K_OFF = DO_OFF + T::BYTES;  // K of stages 0, 1
   static constexpr int V_OFF = K_OFF + 2 * T::BYTES;  // V of stages 0, 1
-  static constexpr int BAR_OFF = V_OFF + 2 * T::BYTES;
+  // FUSE_D: the O tile, and the two halves of each row's D (fp32 [2][128]).
+  static constexpr int O_OFF = V_OFF + 2 * T::BYTES;
+  static constexpr int RED_OFF = O_OFF + (FUSE_D ? T::BYTES : 0);
+  static constexpr int BAR_OFF = RED_OFF + (FUSE_D ? 2 * TILE * 4 : 0);
   // q_full, s_go[KST], kv_empty[KST], a_ready, s_full, dp_full, ds_ready,
   // final
   static constexpr int NBARS = 1 + 2 * KST + 5;
@@ -515,14 +518,17 @@ struct DqSmem {
   static_assert(BYTES <= kMaxDynSmem, "shared memory layout exceeds the per-block limit");
 };
 
-template <int D, bool CAUSAL>
+// FUSE_D: the sweep also forms D = rowsum(dO ∘ O) for its query tile (O
+// loaded beside Q and dO through `to`) and writes it to Dvec, instead of
+// reading it there; the dK/dV sweep then runs after this one.
+template <int D, bool CAUSAL, bool FUSE_D>
 __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                  const __grid_constant__ CUtensorMap tdq, const float* __restrict__ lse,
-                  const float* __restrict__ Dvec, int BH, int G, int N, int head_group, float scale,
-                  float scale_log2) {
-  using L = DqSmem<D>;
+                  const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap to,
+                  const float* __restrict__ lse, float* __restrict__ Dvec, int BH, int G, int N,
+                  int head_group, float scale, float scale_log2) {
+  using L = DqSmem<D, FUSE_D>;
   using T = Tiles<D>;
   constexpr int KST = L::KST;
   extern __shared__ uint8_t smem_raw[];
@@ -588,10 +594,11 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
-      mbar_arrive_expect_tx(q_full, 2 * T::BYTES);
+      mbar_arrive_expect_tx(q_full, (FUSE_D ? 3 : 2) * T::BYTES);
       for (int p = 0; p < T::PANELS; ++p) {
         tma_load_3d(sQ + p * T::PANEL, &tq, q_full, p * 64, q0, bh);
         tma_load_3d(sdO + p * T::PANEL, &tdo, q_full, p * 64, q0, bh);
+        if (FUSE_D) tma_load_3d(smem + L::O_OFF + p * T::PANEL, &to, q_full, p * 64, q0, bh);
       }
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
@@ -688,7 +695,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     constexpr float LOG2E = 1.4426950408889634f;
     const bool q_live = q < N && in_range(static_cast<long long>(bh) * N + q, 1, static_cast<long long>(BH) * N, err);
     const float lse2 = q_live ? lse[static_cast<size_t>(bh) * N + q] * LOG2E : 0.f;
-    const float Dq = q_live ? Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
+    float Dq = (!FUSE_D && q_live) ? Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
+    float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
     bool ok = mbar_wait(q_full, 0, err);
     if (ok) {
       // Copy this row of Q (half 0) or dO (half 1) into TMEM as bf16 pairs:
@@ -712,6 +720,28 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
         }
         tmem_st16(dst + c16, w);
       }
+      if constexpr (FUSE_D) {
+        // This half's share of D for row r: columns 64h..64h+63 (32h.. at
+        // d = 64) of O and dO, read before the dO tile is overwritten by
+        // stage 2 of the K/V ring.
+        constexpr int CPH = D / 16;  // 16-byte chunks per half row
+        float acc = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < CPH; ++ch) {
+          const int chunk = half * CPH + ch;
+          const int off = (chunk / 8) * T::PANEL + r * 128 + (((chunk % 8) ^ (r & 7)) * 16);
+          if (!in_range(off, 16, T::BYTES, err)) continue;
+          const uint4 a = *reinterpret_cast<const uint4*>(smem + L::O_OFF + off);
+          const uint4 b = *reinterpret_cast<const uint4*>(sdO + off);
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int t2 = 0; t2 < 4; ++t2) {
+            acc = fmaf(__uint_as_float(aw[t2] << 16), __uint_as_float(bw[t2] << 16), acc);
+            acc = fmaf(__uint_as_float(aw[t2] & 0xffff0000u), __uint_as_float(bw[t2] & 0xffff0000u), acc);
+          }
+        }
+        if (in_range(half * TILE + r, 1, 2 * TILE, err)) red[half * TILE + r] = acc;
+      }
       tmem_st_wait();
       tc_fence_before();
     }
@@ -719,6 +749,11 @@ __global__ void __launch_bounds__(SWEEP_THREADS, 1)
     if (lane == 0) {
       mbar_arrive(a_ready);
       mbar_arrive(&s_go[0]);
+    }
+    if constexpr (FUSE_D) {
+      named_bar_sync(1, 256);  // both halves of every row written
+      Dq = red[r] + red[TILE + r];
+      if (ok && half == 0 && q_live) Dvec[static_cast<size_t>(bh) * N + q] = Dq;
     }
     for (int j = 0; j < n_kv && ok; ++j) {
       const int kb0 = j * TILE + half * 64;  // first key of this warp's half
@@ -820,21 +855,42 @@ static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FUSE_D>
 static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse,
-                               const float* Dvec, int BH, int G, int N, float scale, cudaStream_t stream) {
-  auto kern = bwd_dq_kernel<D, CAUSAL>;
-  const int smem = DqSmem<D>::ALLOC;
+                               const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to,
+                               const float* lse, float* Dvec, int BH, int G, int N, float scale,
+                               cudaStream_t stream) {
+  auto kern = bwd_dq_kernel<D, CAUSAL, FUSE_D>;
+  const int smem = DqSmem<D, FUSE_D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_t = (N + TILE - 1) / TILE;
   dim3 grid(static_cast<unsigned>(n_t) * static_cast<unsigned>(BH));
   // A query head's CTAs re-read K and V of its K/V head, shared by G heads.
   const int group = head_group_for(4ll * N * D / G, MAX_HEAD_GROUP);
-  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, group, scale,
+  kern<<<grid, SWEEP_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, to, lse, Dvec, BH, G, N, group, scale,
                                                scale * 1.4426950408889634f);
   return cudaGetLastError();
+}
+
+template <bool FUSE_D>
+static cudaError_t launch_dq(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             void* dq, const float* lse, float* Dvec, int BH, int G, int N, int d,
+                             float scale, bool causal, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tdo, tdq, to;
+  const int T = TILE;
+  const int BHkv = BH / G;
+  if (!make_tmap_bf16(&tq, q, BH, N, d, T) || !make_tmap_bf16(&tdo, dO, BH, N, d, T) ||
+      !make_tmap_bf16(&tk, k, BHkv, N, d, T) || !make_tmap_bf16(&tv, v, BHkv, N, d, T) ||
+      !make_tmap_bf16(&tdq, dq, BH, N, d, T))
+    return cudaErrorInvalidValue;
+  if (!FUSE_D) to = tq;  // unused
+  else if (!make_tmap_bf16(&to, o, BH, N, d, T)) return cudaErrorInvalidValue;
+  if (d == 64)
+    return causal ? launch_dq_t<64, true, FUSE_D>(tq, tk, tv, tdo, tdq, to, lse, Dvec, BH, G, N, scale, stream)
+                  : launch_dq_t<64, false, FUSE_D>(tq, tk, tv, tdo, tdq, to, lse, Dvec, BH, G, N, scale, stream);
+  return causal ? launch_dq_t<128, true, FUSE_D>(tq, tk, tv, tdo, tdq, to, lse, Dvec, BH, G, N, scale, stream)
+                : launch_dq_t<128, false, FUSE_D>(tq, tk, tv, tdo, tdq, to, lse, Dvec, BH, G, N, scale, stream);
 }
 
 }  // namespace bwd
@@ -872,18 +928,25 @@ cudaError_t launch_bwd_dkdv(const void* q, const void* k, const void* v, const v
 cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
                           const float* lse, const float* Dvec, int BH, int G, int N, int d, float scale,
                           bool causal, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv, tdo, tdq;
-  const int T = bwd::TILE;
-  const int BHkv = BH / G;
-  if (!make_tmap_bf16(&tq, q, BH, N, d, T) || !make_tmap_bf16(&tdo, dO, BH, N, d, T) ||
-      !make_tmap_bf16(&tk, k, BHkv, N, d, T) || !make_tmap_bf16(&tv, v, BHkv, N, d, T) ||
-      !make_tmap_bf16(&tdq, dq, BH, N, d, T))
-    return cudaErrorInvalidValue;
-  if (d == 64)
-    return causal ? bwd::launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream)
-                  : bwd::launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream);
-  return causal ? bwd::launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream)
-                : bwd::launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, lse, Dvec, BH, G, N, scale, stream);
+  // D is only read in this form.
+  return bwd::launch_dq<false>(q, k, v, nullptr, dO, dq, lse, const_cast<float*>(Dvec), BH, G, N, d, scale,
+                               causal, stream);
+}
+
+cudaError_t launch_bwd_dq_d(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                            void* dq, const float* lse, float* Dvec, int BH, int G, int N, int d, float scale,
+                            bool causal, cudaStream_t stream) {
+  return bwd::launch_dq<true>(q, k, v, o, dO, dq, lse, Dvec, BH, G, N, d, scale, causal, stream);
+}
+
+bool bwd_fuse_d(int BH, int G, int N) {
+  if (G != 1) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return false;
+  const long long ctas = static_cast<long long>(BH) * ((N + bwd::TILE - 1) / bwd::TILE);
+  return ctas >= 4LL * sms;
 }
 
 cudaError_t read_and_clear_bwd_error(uint32_t* out, cudaStream_t stream) {

@@ -72,6 +72,13 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   float* Dvec = static_cast<float*>(scratch);
   const int BH = B * H;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fa::bwd_fuse_d(BH, 1, N)) {  // the order fa_bwd takes for this shape, so the results match it
+    if (fa::launch_bwd_dq_d(q, k, v, o, dO, dq, lse, Dvec, BH, 1, N, d, scale, causal != 0, s) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (fa::launch_bwd_dkdv(q, k, v, dO, dk, dv, lse, Dvec, BH, 1, N, d, scale, causal != 0, s) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
   if (fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o),
                                 static_cast<const __nv_bfloat16*>(dO), Dvec, BH, N, d,
                                 s) != cudaSuccess)

@@ -105,14 +105,20 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   dq, dk, dv      [B][H][N][d] bf16 outputs.
  *   workspace       device buffer of at least fa_bwd_workspace_bytes(...)
  *                   bytes, 16-byte aligned; contents on entry are ignored.
- * Launches three kernels: preprocess (D) on `stream`, then the dK/dV sweep
- * over query tiles on `stream` and, beside it, the dQ sweep over key tiles
- * on a side stream the library forks from `stream` after the preprocess and
- * joins back to it (work queued on `stream` afterwards sees all three; the
- * call is capturable into a CUDA graph). The first call on a host thread
- * and device creates that side stream, kept until the thread exits. Calls
+ * Launches the kernels in one of two orders, chosen by fa_bwd_fuses_d:
+ *   fused      the dQ sweep, which also forms D (fa_bwd_dq_d), then the
+ *              dK/dV sweep, both on `stream`;
+ *   side by    preprocess (D) on `stream`, then the dK/dV sweep over query
+ *   side       tiles on `stream` and, beside it, the dQ sweep over key tiles
+ *              on a side stream the library forks from `stream` after the
+ *              preprocess and joins back to it.
+ * Work queued on `stream` afterwards sees every kernel; the call is
+ * capturable into a CUDA graph. The first call on a host thread and device
+ * that takes the side stream creates it, kept until the thread exits. Calls
  * from one host thread share it, so their dQ sweeps run in call order even
- * when the calls are on different streams.
+ * when the calls are on different streams. The two orders compute D in a
+ * different summation order, so their gradients can differ in the last bit
+ * of bf16 (both are within the same tolerance of the exact result).
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
@@ -132,13 +138,20 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream);
 
 /*
- * The three backward stages as separate calls, each on `stream` (fa_bwd_gqa
- * runs all three, the dQ sweep beside the dK/dV sweep). They share fa_bwd_gqa's argument rules
- * (Hkv = H for plain multi-head attention); `Dvec` is fp32 [B][H][N]
- * caller-owned device memory.
+ * The backward stages as separate calls, each on `stream` (fa_bwd_gqa runs
+ * preprocess, dK/dV and dQ, or dQ-with-D then dK/dV: see fa_bwd). They
+ * share fa_bwd_gqa's argument rules (Hkv = H for plain multi-head
+ * attention); `Dvec` is fp32 [B][H][N] caller-owned device memory.
  *   fa_bwd_preprocess : Dvec_i = Σ_c dO_ic·O_ic.
- *   fa_bwd_dkdv       : dk = scale·dSᵀ q and dv = Pᵀ dO (bf16, final).
- *   fa_bwd_dq         : dq = scale·dS k (bf16, final).
+ *   fa_bwd_dkdv       : dk = scale·dSᵀ q and dv = Pᵀ dO (bf16, final); reads Dvec.
+ *   fa_bwd_dq         : dq = scale·dS k (bf16, final); reads Dvec.
+ *   fa_bwd_dq_d       : fa_bwd_dq that forms Dvec_i itself from o (loaded
+ *                       beside q and dO, one query tile per CTA) and writes
+ *                       it, so no preprocess runs; fa_bwd_dkdv goes after it.
+ *                       Errors: as fa_bwd_dq, and o NULL or misaligned.
+ * fa_bwd_fuses_d returns 1 when fa_bwd_gqa takes the fused order for these
+ * sizes on the current device (one K/V head per query head, and a dK/dV grid
+ * of at least 4 CTAs per SM), else 0 (also for invalid sizes).
  */
 int fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, int H, int N, int d,
                       void* stream);
@@ -148,6 +161,10 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, con
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
               const float* Dvec, void* dq, int B, int H, int Hkv, int N, int d, float scale,
               int causal, void* stream);
+int fa_bwd_dq_d(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                float* Dvec, void* dq, int B, int H, int Hkv, int N, int d, float scale, int causal,
+                void* stream);
+int fa_bwd_fuses_d(int B, int H, int Hkv, int N, int d);
 
 /*
  * Addresses of one attention problem's tensors, in host or in device
@@ -221,7 +238,9 @@ int fa_fwd_bwd_host(const fa_tensors* host, const fa_tensors* dev, void* workspa
  * file-scope __device__ array of FA_BWD_NOALLOC_SCRATCH_BYTES inside
  * the library image, held on every GPU that loads the library until the
  * process exits. The call itself allocates nothing (no cudaMalloc,
- * cudaFree or allocating library routine).
+ * cudaFree or allocating library routine). Its kernels run one after another
+ * on `stream`, in the order fa_bwd takes for the same sizes
+ * (fa_bwd_fuses_d), so its results equal fa_bwd's bit for bit.
  *   - Problems whose scratch need exceeds FA_BWD_NOALLOC_SCRATCH_BYTES are
  *     rejected with FA_ERR_WORKSPACE before anything is launched
  *     (B*H*N*4 bytes: up to 8,388,608 query rows over all heads).

@@ -101,6 +101,19 @@ def test_bwd_argument_errors(L):
     assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 16, 64, 0.0, 1, NUL) == 1
     assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 16, 96, 0.1, 1, NUL) == 2
     assert L.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 0, 16, 64, 0.1, 1, NUL) == 1
+    # the dQ sweep that forms D itself: o is an input, Dvec an output
+    def dq_d(o=FAKE, Dvec=FAKE, H=1, Hkv=1, d=64, scale=0.1):
+        return L.fa_bwd_dq_d(FAKE, FAKE, FAKE, o, FAKE, FAKE, Dvec, FAKE, 1, H, Hkv, 16, d, scale, 1, NUL)
+
+    assert dq_d(o=NUL) == 1 and dq_d(Dvec=NUL) == 1
+    assert dq_d(o=MIS) == 3 and dq_d(Dvec=MIS) == 3
+    assert dq_d(d=96) == 2
+    assert dq_d(H=4, Hkv=3) == 1 and dq_d(scale=0.0) == 1
+    # the order fa_bwd takes: never fused with grouped-query heads or bad sizes
+    assert L.fa_bwd_fuses_d(2, 32, 8, 8192, 128) == 0
+    assert L.fa_bwd_fuses_d(1, 4, 3, 16, 64) == 0
+    assert L.fa_bwd_fuses_d(0, 4, 4, 16, 64) == 0
+    assert L.fa_bwd_fuses_d(1, 4, 4, 16, 96) == 0
 
 
 def test_gqa_argument_errors(L):

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from exact_tiled_attention_24_gb300.workloads import WORKLOADS, make_inputs, to_f64, workload_inputs
-from oracle import attention_bwd, attention_bwd_head, attention_dq_rows_head, attention_fwd
+from oracle import attention_bwd, attention_bwd_gqa, attention_bwd_head, attention_dq_rows_head, attention_fwd
 from gpu_helpers import assert_grad, assert_lse, assert_o
 
 pytestmark = pytest.mark.gpu
@@ -72,6 +72,56 @@ def test_bwd_stages_match_fused_call(fa):
     ref_D = (dog.double() * o.double()).sum(-1)
     assert torch.allclose(Dvec.double(), ref_D, atol=1e-3, rtol=1e-3)
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2) and torch.equal(dq, dq2)
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal", [
+    (1, 2, 2, 300, 128, True),
+    (2, 3, 3, 129, 64, False),
+    (1, 4, 2, 257, 128, True),   # grouped-query heads: D for every query head
+])
+def test_bwd_dq_d_then_dkdv_vs_oracle(fa, B, H, Hkv, N, d, causal):
+    """The dQ sweep that forms D itself (no preprocess), then the dK/dV
+    sweep reading that D: D against rowsum(dO ∘ O) of the GPU's own O, the
+    gradients against the oracle."""
+    q, k, v, do = make_inputs(B, H, N, d, seed=B * 31 + H + N + d, Hkv=Hkv)
+    scale = d ** -0.5
+    dev = torch.device("cuda")
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fwd(qg, kg, vg, causal=causal, scale=scale)
+    Dvec = torch.full((B, H, N), float("nan"), device=dev)
+    dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+    fa.bwd_dq_d(qg, kg, vg, o, dog, lse, Dvec, dq, causal=causal, scale=scale)
+    fa.bwd_dkdv(qg, kg, vg, dog, lse, Dvec, dk, dv, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    ref_D = (dog.double() * o.double()).sum(-1)
+    assert torch.allclose(Dvec.double(), ref_D, atol=1e-4, rtol=1e-5)
+    rdq, rdk, rdv, _ = attention_bwd_gqa(to_f64(q), to_f64(k), to_f64(v), to_f64(do), scale, causal)
+    assert_grad(dq, rdq, "dq")
+    assert_grad(dk, rdk, "dk")
+    assert_grad(dv, rdv, "dv")
+
+
+def test_bwd_fused_order_matches_its_stages(fa):
+    """Where fa_bwd forms D inside the dQ sweep (one K/V head per query head,
+    a dK/dV grid of at least 4 CTAs per SM), it equals bwd_dq_d then
+    bwd_dkdv bit for bit; below the threshold it takes the D pass."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, N, d = 1, 4 * sms // 8 + 8, 1024, 64  # 8 key tiles per head
+    assert fa.bwd_fuses_d(B, H, H, N, d) and not fa.bwd_fuses_d(1, 2, 2, N, d)
+    assert not fa.bwd_fuses_d(B, H, H // 2, N, d)  # grouped-query heads
+    q, k, v, do = make_inputs(B, H, N, d, seed=5)
+    dev = torch.device("cuda")
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fwd(qg, kg, vg, causal=True)
+    dq, dk, dv = fa.bwd(qg, kg, vg, o, lse, dog, causal=True)
+    Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq2, dk2, dv2 = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+    fa.bwd_dq_d(qg, kg, vg, o, dog, lse, Dvec, dq2, causal=True)
+    fa.bwd_dkdv(qg, kg, vg, dog, lse, Dvec, dk2, dv2, causal=True)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
 def test_bwd_deterministic(fa):
