@@ -140,23 +140,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       : "memory");
 }
 
-// Non-tensor bulk copy global -> shared of `bytes` (a multiple of 16; both
-// addresses 16-byte aligned), completing its bytes on the mbarrier.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-// Make generic-proxy shared-memory writes visible to the async (TMA/MMA) proxy.
+
 // 16-byte asynchronous copy global -> shared through L2 only. src_bytes < 16
 // zero-fills the rest of the 16 bytes; 0 reads nothing. The copy writes
 // shared memory through the generic proxy: wait for it (cp_async_wait) and
@@ -173,6 +163,7 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Make generic-proxy shared-memory writes visible to the async (TMA/MMA) proxy.
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
