@@ -37,6 +37,14 @@ def run_cases():
             check(tag)
             for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
                 out[f"{tag}_{n}"] = t.cpu()
+            # the dQ sweep that forms D itself, then dK/dV reading that D
+            Dv = torch.empty((B, H, N), device=dev)
+            dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            fa.bwd_dq_d(q, k, v, o, do, lse, Dv, dq2, causal=causal)
+            fa.bwd_dkdv(q, k, v, do, lse, Dv, dk2, dv2, causal=causal)
+            check(tag + "_dq_d")
+            for n, t in (("D", Dv), ("dq", dq2), ("dk", dk2), ("dv", dv2)):
+                out[f"{tag}_dq_d_{n}"] = t.cpu()
     # row softmax: vector (n % 4 == 0) and scalar paths
     g = torch.Generator().manual_seed(7)
     for rows, n in ((5, 1000), (3, 1001)):
@@ -50,22 +58,25 @@ def run_cases():
     mo, ml = fa.attn_merge(o_parts, lse_parts)
     check("merge")
     out["merge_o"], out["merge_lse"] = mo.cpu(), ml.cpu()
-    B, H, Hkv, d, bs = 3, 8, 2, 128, 16
-    lens = [37, 1, 160]
-    nb = [(L + bs - 1) // bs for L in lens]
-    total = sum(nb) + 2
-    qd = torch.randn((B, H, d), generator=g).to(torch.bfloat16).to(dev)
-    kc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16).to(dev)
-    vc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16).to(dev)
-    perm = torch.randperm(total, generator=g)
-    table = torch.zeros((B, max(nb)), dtype=torch.int32)
-    pos = 0
-    for b in range(B):
-        table[b, :nb[b]] = perm[pos:pos + nb[b]].to(torch.int32)
-        pos += nb[b]
-    od, ld = fa.decode_paged(qd, kc, vc, table.to(dev), torch.tensor(lens, dtype=torch.int32).to(dev), n_splits=3)
-    check("decode")
-    out["decode_o"], out["decode_lse"] = od.cpu(), ld.cpu()
+    # paged decode: TMA boxes (16-token blocks) and per-token gathering (3)
+    for bs in (16, 3):
+        B, H, Hkv, d = 3, 8, 2, 128
+        lens = [37, 1, 160]
+        nb = [(L + bs - 1) // bs for L in lens]
+        total = sum(nb) + 2
+        qd = torch.randn((B, H, d), generator=g).to(torch.bfloat16).to(dev)
+        kc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16).to(dev)
+        vc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16).to(dev)
+        perm = torch.randperm(total, generator=g)
+        table = torch.zeros((B, max(nb)), dtype=torch.int32)
+        pos = 0
+        for b in range(B):
+            table[b, :nb[b]] = perm[pos:pos + nb[b]].to(torch.int32)
+            pos += nb[b]
+        od, ld = fa.decode_paged(qd, kc, vc, table.to(dev), torch.tensor(lens, dtype=torch.int32).to(dev),
+                                 n_splits=3)
+        check(f"decode_bs{bs}")
+        out[f"decode_bs{bs}_o"], out[f"decode_bs{bs}_lse"] = od.cpu(), ld.cpu()
     return out
 
 
