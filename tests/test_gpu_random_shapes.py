@@ -1,8 +1,11 @@
-"""A seeded sweep of random problem shapes through the forward, the full
-backward (whichever kernel order fa_bwd takes) and the dQ-sweep-with-D
-stage order, each against the fp64 oracle: batch, grouped-query ratio,
-ragged length, head size, mask and scale drawn together, so that
-combinations no hand-picked case names are exercised too."""
+"""Seeded sweeps of random problem shapes against the fp64 oracle, so that
+combinations no hand-picked case names are exercised too:
+- attention: batch, grouped-query ratio, ragged length, head size, mask and
+  scale drawn together, through the forward, the full backward (whichever
+  kernel order fa_bwd takes) and the dQ-sweep-with-D stage order;
+- paged decode: batch, query heads per K/V head (up to 20, so beyond one
+  CTA's 16), block size (TMA boxes and per-token gathering), context
+  lengths (empty and single-token ones included), splits and head size."""
 import random
 
 import pytest
@@ -64,3 +67,51 @@ def test_random_shape_vs_oracle(fa, B, H, Hkv, N, d, causal, scale, seed):
     # D as the dQ sweep formed it, against rowsum(dO ∘ O) of the same bf16 O in fp64
     ref_D = (dog.double() * o.double()).sum(-1)
     assert torch.allclose(Dvec.double(), ref_D, atol=1e-4, rtol=1e-5)
+
+
+def draw_decode_cases(n, seed):
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        d = rng.choice((64, 128))
+        Hkv = rng.randint(1, 4)
+        G = rng.choice((1, 2, 4, 8, 16, 20))
+        B = rng.randint(1, 4)
+        bs = rng.choice((1, 2, 3, 8, 16, 24, 32, 64, 128, 200))  # TMA boxes and per-token gathering
+        lens = []
+        for _ in range(B):
+            r = rng.random()
+            lens.append(0 if r < 0.1 else (1 if r < 0.2 else rng.randint(2, 3000)))
+        splits = rng.randint(1, 6)
+        cases.append((B, Hkv * G, Hkv, d, bs, tuple(lens), splits, 7000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("B,H,Hkv,d,bs,lens,splits,seed", draw_decode_cases(24, seed=2027))
+def test_random_decode_vs_oracle(fa, B, H, Hkv, d, bs, lens, splits, seed):
+    from oracle import decode_paged
+    g = torch.Generator().manual_seed(seed)
+    nb = [(L + bs - 1) // bs for L in lens]
+    total = sum(nb) + 2
+    q = torch.randn((B, H, d), generator=g).to(torch.bfloat16)
+    kc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((total, Hkv, bs, d), generator=g).to(torch.bfloat16)
+    perm = torch.randperm(total, generator=g)
+    table = torch.zeros((B, max(max(nb), 1)), dtype=torch.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :nb[b]] = perm[pos:pos + nb[b]].to(torch.int32)
+        pos += nb[b]
+    seq = torch.tensor(lens, dtype=torch.int32)
+    scale = d ** -0.5
+    o, lse = fa.decode_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), seq.cuda(), n_splits=splits, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    ro, rlse = decode_paged(to_f64(q), to_f64(kc), to_f64(vc), table.numpy(), seq.numpy(), scale)
+    live = seq.numpy() > 0
+    if live.any():
+        assert_o(o[live], ro[live])
+        assert_lse(lse[live], rlse[live])
+    if not live.all():  # no cached token: o = 0, lse = -inf
+        dead = ~torch.from_numpy(live)
+        assert torch.all(o[dead].float() == 0) and torch.all(torch.isneginf(lse[dead]))
