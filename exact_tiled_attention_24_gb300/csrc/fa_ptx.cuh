@@ -302,7 +302,6 @@ __host__ __device__ constexpr uint32_t kmajor_step(int ks, uint32_t panel_bytes)
 // Offset of K step ks of an MN-major operand (two 8-row groups per step).
 __host__ __device__ constexpr uint32_t mnmajor_step(int ks) { return static_cast<uint32_t>(ks) * 2048u; }
 
-// TMEM load: 32 lanes x 32 bits, N consecutive columns per thread.
 // TMEM load: 32 lanes x 32 bits, 16 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -314,6 +313,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// TMEM load: 32 lanes x 32 bits, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
