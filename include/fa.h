@@ -200,7 +200,7 @@ typedef struct {
  * inputs go in on a copy-in stream, its kernels run on `stream`, its
  * outputs come out on a copy-out stream as soon as they are ready. Host
  * buffers should be page-locked (cudaHostAlloc / cudaHostRegister), else
- * the copies are staged by the driver and do not overlap.
+ * the CUDA driver stages the copies and they do not overlap.
  *
  *   Ordering   the call starts after the work already queued on `stream`,
  *              and work queued on `stream` after it starts after every
