@@ -13,7 +13,7 @@
 // key/value tiles once for both ("ping-pong"): while one softmax group
 // exponentiates its S tile, the tensor core runs the other group's products.
 // Roles (320 threads):
-//   warp 0      TMA producer: Q0, Q1 and K_0 once, then V_j with K_{j+1}
+//   warp 0      TMA producer: Q0, K_0 and Q1 once, then V_j with K_{j+1}
 //               into 2-stage rings (one full and one empty barrier per pair)
 //   warp 1      TMEM owner and MMA issuer (warp-uniform, one elected lane issues)
 //   warps 2..5  softmax group 0 (Q0), one thread per query row (TMEM lane)
@@ -61,9 +61,9 @@ struct Smem {
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-  // q_full, k0_full, kv_full[2], kv_empty[2], s_full[2], p_ready[2] (keys
-  // 0..63 of P), pv_done[2], final, p_hi[2] (keys 64..127)
-  static constexpr int NBARS = 2 + 2 * STAGES + 6 + 1 + 2;
+  // q_full (Q0), k0_full, kv_full[2], kv_empty[2], s_full[2], p_ready[2]
+  // (keys 0..63 of P), pv_done[2], final, p_hi[2] (keys 64..127), q1_full (Q1)
+  static constexpr int NBARS = 2 + 2 * STAGES + 6 + 1 + 2 + 1;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = TMEM_SLOT_OFF + 16;
   // Slack for 1024-byte alignment; at least 116 KB so that only one CTA
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* pv_done = p_ready + 2;          // [2]
   uint64_t* final_bar = pv_done + 2;
   uint64_t* p_hi = final_bar + 1;           // [2]
+  uint64_t* q1_full = p_hi + 2;  // Q1 (q_full: Q0): group 0's first S needs only Q0 and K_0
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q1_full, 1);
     mbar_init(k0_full, 1);
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -149,13 +151,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      mbar_arrive_expect_tx(q_full, 2 * L::TILE_BYTES);
-      for (int g = 0; g < 2; ++g)
-        for (int p = 0; p < L::PANELS; ++p)
-          tma_load_3d(sQ + g * L::TILE_BYTES + p * L::PANEL, &tq, q_full, p * 64, qrow0 + g * BM, bh);
+      // Q0 and K_0 first: group 0's first S needs only these two.
+      mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
+      for (int p = 0; p < L::PANELS; ++p)
+        tma_load_3d(sQ + p * L::PANEL, &tq, q_full, p * 64, qrow0, bh);
       mbar_arrive_expect_tx(k0_full, L::TILE_BYTES);
       for (int p = 0; p < L::PANELS; ++p)
         tma_load_3d(sK + p * L::PANEL, &tk, k0_full, p * 64, 0, bkv);
+      mbar_arrive_expect_tx(q1_full, L::TILE_BYTES);
+      for (int p = 0; p < L::PANELS; ++p)
+        tma_load_3d(sQ + L::TILE_BYTES + p * L::PANEL, &tq, q1_full, p * 64, qrow0 + BM, bh);
       // Slot j: V_j and K_{j+1}, issued once step j - 2 (the prologue for
       // j = 1, whose S_0 read K_0) has released their stages.
       int issued = 0;
@@ -173,6 +178,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // Drain: never leave the CTA with copies still landing in its smem.
       mbar_wait(q_full, 0, err);
+      mbar_wait(q1_full, 0, err);
       mbar_wait(k0_full, 0, err);
       for (int j = max(0, issued - L::STAGES); j < issued; ++j)
         mbar_wait(&kv_full[j % L::STAGES], (j / L::STAGES) & 1, err);
@@ -228,6 +234,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok) {
       tc_fence_after();
       issue_s(0, 0);
+      ok = mbar_wait_warp(q1_full, 0, err);
+    }
+    if (ok) {
+      tc_fence_after();
       issue_s(1, 0);
       commit(&kv_empty[1]);  // K_0 read: slot 1 (V_1, K_2) may load
     }
