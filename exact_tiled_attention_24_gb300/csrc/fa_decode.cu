@@ -110,7 +110,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
 //           the box reads zeros and the entry is never dereferenced.
 //   gather  any other block size: the producer warp's lanes look up each
 //           token's block and copy its row in 16-byte pieces to the
-//           swizzled position (zero fill for the same two cases).
+//           swizzled position (zero fill for the same two cases). Each lane
+//           arrives on the tile's barrier when its copies land, and the
+//           issuer fences them for the tensor core after its wait. Below 8
+//           tokens per block the lookups are loaded two tiles ahead.
 // The softmax keeps one exponent reference per head, raised (and Oᵀ's column
 // rescaled) when a key outgrows it by more than 2^8, as in the forward.
 // Roles (224 threads): warp 0 loads K tiles, warp 1 V tiles (lane 0 for
@@ -160,11 +163,16 @@ struct Smem {
   static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
 };
 
-// GATHER: the cache's block size does not tile a 128-key tile into whole
-// 8-row swizzle groups (a multiple of 8 dividing 128), so K and V arrive by
-// per-token 16-byte copies instead of one TMA box per cache block; tk and tv
-// are then unused and kc, vc are read directly.
-template <int D, int GM, bool GATHER>
+// How K and V tiles reach shared memory. BOXES: one TMA box per cache block
+// (a block size that is a multiple of 8 dividing 128, so boxes land on whole
+// 8-row swizzle groups). Otherwise per-token 16-byte copies, with tk and tv
+// unused and kc, vc read directly: GATHER looks up a tile's block-table
+// entries after issuing the previous tile's copies; GATHER_AHEAD (block
+// sizes below 8, where a tile needs 16 or more distinct entries) loads them
+// two tiles ahead and the first ones before the CTA's setup.
+enum TileLoad : int { BOXES = 0, GATHER = 1, GATHER_AHEAD = 2 };
+
+template <int D, int GM, int LOAD>
 __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __nv_bfloat16* __restrict__ kc,
@@ -172,6 +180,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B, int H,
     int Hkv, int num_blocks, int bs, int max_blocks, float scale_log2) {
   constexpr int KST = Cfg<GM>::KST, VST = Cfg<GM>::VST, PB = Cfg<GM>::PB;
+  constexpr bool GATHERED = LOAD != BOXES, AHEAD = LOAD == GATHER_AHEAD;
   using L = Smem<D, KST, VST, PB>;
   static_assert(Cfg<GM>::CTAS * (L::ALLOC + 1024) <= 233472, "the CTAs must fit an SM");
   extern __shared__ uint8_t smem_raw[];
@@ -204,6 +213,29 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   const int n_t = tile1 - tile0;
   const int t_end = min(Lb, tile1 * TK);  // keys at or past t_end are masked
 
+  // GATHER_AHEAD: fetch() loads the block-table entries of rows lane,
+  // lane + 32, lane + 64 and lane + 96 of a tile (0 past the context, -1 for
+  // an index outside the table) into registers; the producer lanes use them
+  // two tiles later. The first two tiles' loads are issued here, before the
+  // CTA's setup.
+  auto fetch = [&](int tile, int (&raw)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = tile * TK + lane + 32 * u;
+      int e = 0;
+      if (t < Lb) {
+        const long long ti = static_cast<long long>(b) * max_blocks + t / bs;
+        e = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
+      }
+      raw[u] = e;
+    }
+  };
+  int raw_a[4] = {0, 0, 0, 0}, raw_b[4] = {0, 0, 0, 0};
+  if (AHEAD && warp <= 1) {
+    fetch(tile0, raw_a);
+    if (n_t > 1) fetch(tile0 + 1, raw_b);
+  }
+
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
   uint8_t* sQ = smem + L::Q_OFF;
@@ -226,11 +258,11 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     mbar_init(q_full, 1);
     // Gathered tiles: one arrival per producer lane once its copies landed.
     for (int i = 0; i < KST; ++i) {
-      mbar_init(&k_full[i], GATHER ? 32 : 1);
+      mbar_init(&k_full[i], GATHERED ? 32 : 1);
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < VST; ++i) {
-      mbar_init(&v_full[i], GATHER ? 32 : 1);
+      mbar_init(&v_full[i], GATHERED ? 32 : 1);
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
@@ -268,14 +300,33 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     }
   };
 
-  // The same tile by per-token copies, run by a whole warp. resolve() looks
-  // up where rows lane, lane + 32, lane + 64 and lane + 96 of a tile live
-  // (element offset, or -1: past the context or a bad block index, zero
+  // The same tile by per-token copies, run by a whole warp. resolve() turns
+  // fetched table entries of rows lane, lane + 32, lane + 64 and lane + 96
+  // into element offsets (-1: past the context or a bad block index, zero
   // fill); copy_tile() then moves chunk c (16 bytes) of row r into the
   // 128-byte-swizzled K-major layout the products read: panel c / 8, at
   // 128 r + 16 ((c mod 8) xor (r mod 8)).
   const long long cache_elems = static_cast<long long>(num_blocks) * Hkv * bs * D;
-  auto resolve = [&](int tile, long long (&row_off)[4]) {
+  auto resolve = [&](int tile, const int (&raw)[4], long long (&row_off)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = tile * TK + lane + 32 * u;
+      long long off = -1;
+      if (t < Lb) {
+        const int blk = raw[u], bi = t / bs;
+        if (blk >= 0 && blk < num_blocks)
+          off = ((static_cast<long long>(blk) * Hkv + hk) * bs + (t - bi * bs)) * D;
+        else
+          atomicExch(err, DEV_BAD_INDEX);
+      }
+      row_off[u] = off;
+    }
+  };
+  // GATHER: the same offsets with the entries loaded on the spot. (The two
+  // forms stay apart: GATHER written as fetch() + resolve() measured 5%
+  // slower at block sizes 12 to 48; its producer's instructions per tile
+  // count there.)
+  auto lookup = [&](int tile, long long (&row_off)[4]) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int t = tile * TK + lane + 32 * u;
@@ -308,39 +359,37 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
       }
     }
   };
-  // Producer loop of the gathered path (NST stages; the whole warp). The
-  // next tile's rows are looked up while this tile's copies are in flight.
-  // A tile's full barrier gets each lane's arrival once that lane's copies
-  // completed and were fenced for the tensor core; with two stages the
-  // wait trails the issue by one tile, so two tiles' copies overlap.
+  // Producer loop of the gathered path (NST stages; the whole warp). Each
+  // lane's copies arrive on the tile's full barrier when they land (32
+  // arrivals), so the lanes go straight on to the next tile's lookups; the
+  // issuer fences the async proxy after its wait.
   auto gather_loop = [&](const __nv_bfloat16* cache, uint8_t* base, int stage_bytes, uint64_t* full,
                          uint64_t* empty, auto nst_c) {
     constexpr int NST = decltype(nst_c)::value;
     long long cur[4], nxt[4] = {-1, -1, -1, -1};
-    resolve(tile0, cur);
-    int j = 0;
-    for (; j < n_t; ++j) {
+    if (AHEAD)
+      resolve(tile0, raw_a, cur);
+    else
+      lookup(tile0, cur);
+    for (int j = 0; j < n_t; ++j) {
       const int st = j % NST;
       if (!mbar_wait_warp(&empty[st], ((j / NST) & 1) ^ 1, err)) break;
       copy_tile(cache, base + st * stage_bytes, cur);
-      cp_async_commit();
-      if (j + 1 < n_t) resolve(tile0 + j + 1, nxt);
-      if (NST == 1 || j >= 1) {
-        cp_async_wait<NST - 1>();
-        fence_async_smem();
-        mbar_arrive(&full[(j - (NST - 1)) % NST]);
-      }
+      cp_async_arrive_noinc(&full[st]);
+      if (AHEAD) {
+        if (j + 1 < n_t) resolve(tile0 + j + 1, raw_b, cur);
+        if (j + 2 < n_t) fetch(tile0 + j + 2, raw_b);
+      } else {
+        if (j + 1 < n_t) lookup(tile0 + j + 1, nxt);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+        for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+      }
     }
+    cp_async_commit();
     cp_async_wait<0>();  // nothing may land after the CTA exits
-    if (NST > 1 && j == n_t && n_t >= 1) {
-      fence_async_smem();
-      mbar_arrive(&full[(n_t - 1) % NST]);
-    }
   };
 
-  if (GATHER && warp <= 1) {
+  if (GATHERED && warp <= 1) {
     // ------------------------------------ K (warp 0) and V (warp 1) producers
     if (warp == 0 && lane == 0) {
       prefetch_tmap(&tq);
@@ -397,6 +446,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
       const int st = j % KST;
       if (!mbar_wait_warp(&k_full[st], (j / KST) & 1, err)) return false;
       tc_fence_after();
+      if (GATHERED) fence_async_smem();  // the lanes' copies, for the tensor core
       const uint64_t dk = sdesc_kmajor(smem_u32(sK + st * L::K_TILE), 0);
       if (elect_one()) {
 #pragma unroll
@@ -420,6 +470,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
       ok = mbar_wait_warp(&v_full[vs], (j / VST) & 1, err) && mbar_wait_warp(&p_full[pb], (j / PB) & 1, err);
       if (!ok) break;
       tc_fence_after();
+      if (GATHERED) fence_async_smem();
       const uint64_t dv = sdesc_mnmajor(smem_u32(sV + vs * L::V_TILE), 0, L::PANEL);
       const uint64_t dp = sdesc_kmajor(smem_u32(sP + pb * 2 * L::QPANEL), 0);
       if (elect_one()) {
@@ -574,14 +625,14 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
 // lands on whole 1024-byte swizzle groups); other sizes gather per token.
 inline bool boxes(int bs) { return bs % 8 == 0 && TK % bs == 0; }
 
-template <int D, int GM, bool GATHER>
+template <int D, int GM, int LOAD>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const void* kc,
                             const void* vc, const int* table, const int* seq_lens, float* o_part, float* lse_part,
                             int B, int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
                             cudaStream_t stream) {
   using C = Cfg<GM>;
   const int smem = Smem<D, C::KST, C::VST, C::PB>::ALLOC;
-  auto kern = decode_mma_kernel<D, GM, GATHER>;
+  auto kern = decode_mma_kernel<D, GM, LOAD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_chunk = (H / Hkv + NH - 1) / NH;
@@ -598,10 +649,13 @@ static cudaError_t launch_g(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             int B, int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
                             cudaStream_t stream) {
   if (boxes(bs))
-    return launch_t<D, GM, false>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+    return launch_t<D, GM, BOXES>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
                                   max_blocks, scale, S, stream);
-  return launch_t<D, GM, true>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                               max_blocks, scale, S, stream);
+  if (bs < 8)
+    return launch_t<D, GM, GATHER_AHEAD>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv,
+                                         num_blocks, bs, max_blocks, scale, S, stream);
+  return launch_t<D, GM, GATHER>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
+                                 max_blocks, scale, S, stream);
 }
 
 template <int D>

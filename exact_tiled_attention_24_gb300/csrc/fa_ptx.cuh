@@ -149,12 +149,19 @@ __device__ __forceinline__ void tma_store_wait_all() {
 
 // 16-byte asynchronous copy global -> shared through L2 only. src_bytes < 16
 // zero-fills the rest of the 16 bytes; 0 reads nothing. The copy writes
-// shared memory through the generic proxy: wait for it (cp_async_wait) and
-// fence_async_smem() before a tensor-core product reads the bytes.
+// shared memory through the generic proxy: once it is known complete (by
+// cp_async_wait, or by the barrier of cp_async_arrive_noinc), fence_async_smem()
+// must run before a tensor-core product reads the bytes.
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
                "l"(__cvta_generic_to_global(src)), "r"(src_bytes)
                : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued before has landed.
+// The arrival is one of the barrier's expected count (noinc: the count is
+// not raised for it), so the thread goes on without waiting for its copies.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's committed copy groups are pending.

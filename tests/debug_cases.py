@@ -58,8 +58,9 @@ def run_cases():
     mo, ml = fa.attn_merge(o_parts, lse_parts)
     check("merge")
     out["merge_o"], out["merge_lse"] = mo.cpu(), ml.cpu()
-    # paged decode: TMA boxes (16-token blocks) and per-token gathering (3)
-    for bs in (16, 3):
+    # paged decode: TMA boxes (16-token blocks) and per-token gathering
+    # (3: table entries loaded ahead; 24: looked up per tile)
+    for bs in (16, 3, 24):
         B, H, Hkv, d = 3, 8, 2, 128
         lens = [37, 1, 160]
         nb = [(L + bs - 1) // bs for L in lens]

@@ -87,11 +87,15 @@ def test_decode_split_count_does_not_change_the_result(fa):
         assert (lse - outs[0][1]).abs().max() <= 1e-4
 
 
-@pytest.mark.parametrize("d,bs", [(64, 16), (128, 16), (128, 3)])
-def test_decode_bad_block_index_is_reported_not_read(fa, d, bs):
-    # TMA boxes (16-token blocks) and per-token gathering (3-token blocks)
-    q, kc, vc, table, lens = paged_case(2, 4, 2, d, bs, [40, 40], seed=9)
-    table[1, 1] = kc.shape[0] + 5  # outside the cache
+@pytest.mark.parametrize("d,bs,L,bad", [
+    (64, 16, 40, 1), (128, 16, 40, 1),  # TMA boxes
+    (128, 3, 40, 1),                    # gathered, entries loaded before the CTA's setup
+    (128, 1, 800, 300),                 # gathered, an entry loaded two tiles ahead (tile 2 of 4)
+    (128, 24, 400, 11),                 # gathered, entries looked up per tile
+])
+def test_decode_bad_block_index_is_reported_not_read(fa, d, bs, L, bad):
+    q, kc, vc, table, lens = paged_case(2, 4, 2, d, bs, [L, L], seed=9)
+    table[1, bad] = kc.shape[0] + 5  # outside the cache
     fa.decode_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), lens.cuda(), n_splits=2)
     assert fa.last_device_error() == 7  # FA_ERR_BAD_INDEX
     assert fa.last_device_error() == 0  # read and cleared
