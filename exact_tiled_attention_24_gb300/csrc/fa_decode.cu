@@ -107,7 +107,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
 //           num_blocks·Hkv)) at row offset block·block_size of the tile; a
 //           block past the context or with a table entry outside
 //           [0, num_blocks) is requested at an out-of-range coordinate, so
-//           the box reads zeros and the entry is never dereferenced.
+//           the box reads zeros and the entry is never dereferenced. Lane i
+//           of the producer warp issues block i's box; the table entries
+//           are loaded two tiles ahead, the first ones before the setup.
 //   gather  any other block size: the producer warp's lanes look up each
 //           token's block and copy its row in 16-byte pieces to the
 //           swizzled position (zero fill for the same two cases). Each lane
@@ -116,10 +118,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
 //           tokens per block the lookups are loaded two tiles ahead.
 // The softmax keeps one exponent reference per head, raised (and Oᵀ's column
 // rescaled) when a key outgrows it by more than 2^8, as in the forward.
-// Roles (224 threads): warp 0 loads K tiles, warp 1 V tiles (lane 0 for
-// boxes, the whole warp to gather), warp 2 owns TMEM and issues the
-// products, warps 3..6 run the softmax and the epilogue. Two or three CTAs
-// share an SM.
+// Roles (224 threads): warp 0 loads K tiles, warp 1 V tiles (the whole
+// warp: a lane per box, or four rows per lane to gather), warp 2 owns TMEM
+// and issues the products, warps 3..6 run the softmax and the epilogue. Two
+// or three CTAs share an SM.
 namespace decmma {
 
 constexpr int TK = 128;       // keys per tile (M of the score product)
@@ -235,6 +237,23 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     fetch(tile0, raw_a);
     if (n_t > 1) fetch(tile0 + 1, raw_b);
   }
+  // BOXES: lane i of a producer warp holds the table entry of block i of a
+  // tile (at most 16 blocks per tile), loaded two tiles ahead.
+  const int bpt = TK / bs;  // blocks per tile
+  auto fetch_box = [&](int tile) -> int {
+    const int bi = tile * bpt + lane;
+    int e = 0;
+    if (lane < bpt && bi * bs < Lb) {
+      const long long ti = static_cast<long long>(b) * max_blocks + bi;
+      e = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
+    }
+    return e;
+  };
+  int box_a = 0, box_b = 0;
+  if (LOAD == BOXES && warp <= 1) {
+    box_a = fetch_box(tile0);
+    if (n_t > 1) box_b = fetch_box(tile0 + 1);
+  }
 
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
@@ -283,21 +302,20 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Loads of one 128-key tile of the cache: one box per cache block.
-  const int bpt = TK / bs;  // blocks per tile
-  auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile) {  // D / 64 panels
-    const int blk_first = tile * bpt;
-    for (int i = 0; i < bpt; ++i) {
-      const int bi = blk_first + i;
-      int z = num_blocks * Hkv;  // out of range: the box reads zeros
-      if (bi * bs < Lb) {
-        const long long ti = static_cast<long long>(b) * max_blocks + bi;
-        const int blk = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
-        if (blk >= 0 && blk < num_blocks) z = blk * Hkv + hk;
-        else atomicExch(err, DEV_BAD_INDEX);
-      }
-      for (int p = 0; p < L::KPANELS; ++p) tma_load_3d(dst + p * L::PANEL + i * bs * 128, map, bar, p * 64, 0, z);
+  // Loads of one 128-key tile of the cache: one box per cache block, lane i
+  // of the producer warp issuing block i's box from its table entry `e`
+  // (after lane 0 set the barrier's byte count).
+  auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile, int e, int bytes) {
+    const int bi = tile * bpt + lane;
+    int z = num_blocks * Hkv;  // out of range: the box reads zeros
+    if (lane < bpt && bi * bs < Lb) {
+      if (e >= 0 && e < num_blocks) z = e * Hkv + hk;
+      else atomicExch(err, DEV_BAD_INDEX);
     }
+    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+    __syncwarp();
+    if (lane < bpt)
+      for (int p = 0; p < L::KPANELS; ++p) tma_load_3d(dst + p * L::PANEL + lane * bs * 128, map, bar, p * 64, 0, z);
   };
 
   // The same tile by per-token copies, run by a whole warp. resolve() turns
@@ -409,31 +427,36 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
       prefetch_tmap(&tk);
       mbar_arrive_expect_tx(q_full, L::KPANELS * L::QPANEL);
       for (int p = 0; p < L::KPANELS; ++p) tma_load_3d(sQ + p * L::QPANEL, &tq, q_full, p * 64, head0, 0);
-      int issued = 0;
-      for (int j = 0; j < n_t; ++j) {
-        const int st = j % KST;
-        if (!mbar_wait(&k_empty[st], ((j / KST) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::K_TILE);
-        load_tile(&tk, sK + st * L::K_TILE, &k_full[st], tile0 + j);
-        issued = j + 1;
-      }
+    }
+    __syncwarp();
+    int issued = 0, cur = box_a;
+    for (int j = 0; j < n_t; ++j) {
+      const int st = j % KST;
+      if (!mbar_wait_warp(&k_empty[st], ((j / KST) & 1) ^ 1, err)) break;
+      load_tile(&tk, sK + st * L::K_TILE, &k_full[st], tile0 + j, cur, L::K_TILE);
+      issued = j + 1;
+      cur = box_b;
+      if (j + 2 < n_t) box_b = fetch_box(tile0 + j + 2);
+    }
+    if (lane == 0) {
       mbar_wait(q_full, 0, err);
       for (int j = max(0, issued - KST); j < issued; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, err);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- V producer
-    if (lane == 0) {
-      prefetch_tmap(&tv);
-      int issued = 0;
-      for (int j = 0; j < n_t; ++j) {
-        const int st = j % VST;
-        if (!mbar_wait(&v_empty[st], ((j / VST) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::K_TILE);  // the real panels of the V tile
-        load_tile(&tv, sV + st * L::V_TILE, &v_full[st], tile0 + j);
-        issued = j + 1;
-      }
-      for (int j = max(0, issued - VST); j < issued; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, err);
+    if (lane == 0) prefetch_tmap(&tv);
+    __syncwarp();
+    int issued = 0, cur = box_a;
+    for (int j = 0; j < n_t; ++j) {
+      const int st = j % VST;
+      if (!mbar_wait_warp(&v_empty[st], ((j / VST) & 1) ^ 1, err)) break;
+      load_tile(&tv, sV + st * L::V_TILE, &v_full[st], tile0 + j, cur, L::K_TILE);  // the real panels of the V tile
+      issued = j + 1;
+      cur = box_b;
+      if (j + 2 < n_t) box_b = fetch_box(tile0 + j + 2);
     }
+    if (lane == 0)
+      for (int j = max(0, issued - VST); j < issued; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, err);
   } else if (warp == 2) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16(TK, NH, false, false);  // A = K (K-major), B = Q (K-major)
