@@ -845,7 +845,7 @@ def run_decode(args, dw, rank, world, dist):
         "clocks": clk.summary(),
         "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (2 if dw.n_splits > 1 else 1) * args.steps,  # kernel (+ merge)
     }
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import decode_paged

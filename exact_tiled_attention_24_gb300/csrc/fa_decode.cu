@@ -47,12 +47,18 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // One warp per output row: o = Σ_s e^(lse_s − lse) o_s, lse = ln Σ_s e^(lse_s).
+// Lane i computes the weight of part i (of each group of 32), and the parts'
+// output slices are loaded several at a time before any is used, so a row
+// takes a few round trips to memory, not one per part. The sums run over the
+// parts in order, the same arithmetic as one part after another.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_parts,
                                                     const float* __restrict__ lse_parts, int S,
                                                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                                     long long rows) {
-  constexpr int CPL = D / 32;  // columns per lane
+  constexpr int CPL = D / 32;  // columns per lane: 4 (d = 128) or 2 (d = 64)
+  constexpr int U = 16 / CPL;  // part slices in flight per lane (16 floats: the merge fits one wave)
+  using Vec = typename std::conditional<CPL == 4, float4, float2>::type;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -67,13 +73,30 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
 #pragma unroll
   for (int j = 0; j < CPL; ++j) acc[j] = 0.f;
   if (m != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      if (!in_range((s * rows + row) * D + lane * CPL, CPL, prt * D, err)) continue;
-      const float w = ex2((lse_parts[s * rows + row] - m) * LOG2E);
-      l += w;
-      const float* src = o_parts + (s * rows + row) * D + lane * CPL;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int sl = s0 + lane;
+      float wl = 0.f;  // weight of part sl (0 for a part that is not there)
+      if (sl < S && in_range(sl * rows + row, 1, prt, err)) wl = ex2((lse_parts[sl * rows + row] - m) * LOG2E);
+      const int n = min(32, S - s0);
+      for (int s1 = 0; s1 < n; s1 += U) {
+        Vec v[U];
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) acc[j] = fmaf(w, src[j], acc[j]);
+        for (int u = 0; u < U; ++u) {
+          const long long off = ((s0 + s1 + u) * rows + row) * D + lane * CPL;
+          if (s1 + u < n && in_range(off, CPL, prt * D, err)) v[u] = *reinterpret_cast<const Vec*>(o_parts + off);
+          else v[u] = Vec{};
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, s1 + u);
+          if (s1 + u < n) {
+            l += w;
+            const float* x = reinterpret_cast<const float*>(&v[u]);
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) acc[j] = fmaf(w, x[j], acc[j]);
+          }
+        }
+      }
     }
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -179,7 +202,8 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table,
-    const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part, int B, int H,
+    const int* __restrict__ seq_lens, float* __restrict__ o_part, float* __restrict__ lse_part,
+    __nv_bfloat16* __restrict__ o_out, float* __restrict__ lse_out, int B, int H,
     int Hkv, int num_blocks, int bs, int max_blocks, float scale_log2) {
   constexpr int KST = Cfg<GM>::KST, VST = Cfg<GM>::VST, PB = Cfg<GM>::PB;
   constexpr bool GATHERED = LOAD != BOXES, AHEAD = LOAD == GATHER_AHEAD;
@@ -207,9 +231,15 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   const long long prow = static_cast<long long>(s) * B * H + head0;  // its partial row
   const long long part_rows = static_cast<long long>(S) * B * H;
   if (tile0 >= tile1) {  // no key in this split: o_s = 0, lse_s = -inf (weight 0 in the merge)
-    for (int i = threadIdx.x; i < G * D; i += THREADS)
-      if (in_range(prow * D + i, 1, part_rows * D, err)) o_part[prow * D + i] = 0.f;
-    if (threadIdx.x < G && in_range(prow + threadIdx.x, 1, part_rows, err)) lse_part[prow + threadIdx.x] = -INFINITY;
+    for (int i = threadIdx.x; i < G * D; i += THREADS) {
+      if (S == 1) {
+        if (in_range(prow * D + i, 1, part_rows * D, err)) o_out[prow * D + i] = __float2bfloat16_rn(0.f);
+      } else if (in_range(prow * D + i, 1, part_rows * D, err)) {
+        o_part[prow * D + i] = 0.f;
+      }
+    }
+    if (threadIdx.x < G && in_range(prow + threadIdx.x, 1, part_rows, err))
+      (S == 1 ? lse_out : lse_part)[prow + threadIdx.x] = -INFINITY;
     return;
   }
   const int n_t = tile1 - tile0;
@@ -631,8 +661,13 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
         if (h >= G) break;
         const float lh = (red[h] + red[NH + h]) + (red[2 * NH + h] + red[3 * NH + h]);
         const long long orow = prow + h;
-        if (r < D && in_range(orow * D + r, 1, part_rows * D, err)) o_part[orow * D + r] = __uint_as_float(o[h]) / lh;
-        if (r == 0 && in_range(orow, 1, part_rows, err)) lse_part[orow] = (m[h] + __log2f(lh)) * dec::LN2;
+        // One split: this is the final row (o in bf16), and no merge runs.
+        const float ov = __uint_as_float(o[h]) / lh, lv = (m[h] + __log2f(lh)) * dec::LN2;
+        if (r < D && in_range(orow * D + r, 1, part_rows * D, err)) {
+          if (S == 1) o_out[orow * D + r] = __float2bfloat16_rn(ov);
+          else o_part[orow * D + r] = ov;
+        }
+        if (r == 0 && in_range(orow, 1, part_rows, err)) (S == 1 ? lse_out : lse_part)[orow] = lv;
       }
     }
   }
@@ -648,11 +683,19 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
 // lands on whole 1024-byte swizzle groups); other sizes gather per token.
 inline bool boxes(int bs) { return bs % 8 == 0 && TK % bs == 0; }
 
+// Output pointers of every launcher: o_part, lse_part take the split results
+// (S > 1, merged afterwards); o_out, lse_out the final rows (S = 1).
+struct Out {
+  float* o_part;
+  float* lse_part;
+  __nv_bfloat16* o;
+  float* lse;
+};
+
 template <int D, int GM, int LOAD>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const void* kc,
-                            const void* vc, const int* table, const int* seq_lens, float* o_part, float* lse_part,
-                            int B, int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
-                            cudaStream_t stream) {
+                            const void* vc, const int* table, const int* seq_lens, const Out& out, int B, int H,
+                            int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S, cudaStream_t stream) {
   using C = Cfg<GM>;
   const int smem = Smem<D, C::KST, C::VST, C::PB>::ALLOC;
   auto kern = decode_mma_kernel<D, GM, LOAD>;
@@ -661,30 +704,30 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
   const int n_chunk = (H / Hkv + NH - 1) / NH;
   const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(Hkv * n_chunk), static_cast<unsigned>(B));
   kern<<<grid, THREADS, smem, stream>>>(tq, tk, tv, static_cast<const __nv_bfloat16*>(kc),
-                                        static_cast<const __nv_bfloat16*>(vc), table, seq_lens, o_part, lse_part, B, H,
-                                        Hkv, num_blocks, bs, max_blocks, scale * dec::LOG2E);
+                                        static_cast<const __nv_bfloat16*>(vc), table, seq_lens, out.o_part,
+                                        out.lse_part, out.o, out.lse, B, H, Hkv, num_blocks, bs, max_blocks,
+                                        scale * dec::LOG2E);
   return cudaGetLastError();
 }
 
 template <int D, int GM>
 static cudaError_t launch_g(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const void* kc,
-                            const void* vc, const int* table, const int* seq_lens, float* o_part, float* lse_part,
-                            int B, int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S,
-                            cudaStream_t stream) {
+                            const void* vc, const int* table, const int* seq_lens, const Out& out, int B, int H,
+                            int Hkv, int num_blocks, int bs, int max_blocks, float scale, int S, cudaStream_t stream) {
   if (boxes(bs))
-    return launch_t<D, GM, BOXES>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                                  max_blocks, scale, S, stream);
+    return launch_t<D, GM, BOXES>(tq, tk, tv, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs, max_blocks,
+                                  scale, S, stream);
   if (bs < 8)
-    return launch_t<D, GM, GATHER_AHEAD>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv,
-                                         num_blocks, bs, max_blocks, scale, S, stream);
-  return launch_t<D, GM, GATHER>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                                 max_blocks, scale, S, stream);
+    return launch_t<D, GM, GATHER_AHEAD>(tq, tk, tv, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs,
+                                         max_blocks, scale, S, stream);
+  return launch_t<D, GM, GATHER>(tq, tk, tv, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs, max_blocks,
+                                 scale, S, stream);
 }
 
 template <int D>
 static cudaError_t launch_d(const void* q, const void* kc, const void* vc, const int* table, const int* seq_lens,
-                            float* o_part, float* lse_part, int B, int H, int Hkv, int num_blocks, int bs,
-                            int max_blocks, float scale, int S, cudaStream_t stream) {
+                            const Out& out, int B, int H, int Hkv, int num_blocks, int bs, int max_blocks, float scale,
+                            int S, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16(&tq, q, 1, B * H, D, NH)) return cudaErrorInvalidValue;
   if (boxes(bs)) {
@@ -696,22 +739,22 @@ static cudaError_t launch_d(const void* q, const void* kc, const void* vc, const
   }
   const int G = H / Hkv;  // query heads per K/V head; CTAs take them 16 at a time
   if (G <= 4)
-    return launch_g<D, 4>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                          max_blocks, scale, S, stream);
+    return launch_g<D, 4>(tq, tk, tv, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs, max_blocks, scale, S,
+                          stream);
   if (G <= 8)
-    return launch_g<D, 8>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                          max_blocks, scale, S, stream);
-  return launch_g<D, 16>(tq, tk, tv, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                         max_blocks, scale, S, stream);
+    return launch_g<D, 8>(tq, tk, tv, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs, max_blocks, scale, S,
+                          stream);
+  return launch_g<D, 16>(tq, tk, tv, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs, max_blocks, scale, S,
+                         stream);
 }
 
 static cudaError_t launch(const void* q, const void* kc, const void* vc, const int* table, const int* seq_lens,
-                          float* o_part, float* lse_part, int B, int H, int Hkv, int d, int num_blocks, int bs,
-                          int max_blocks, float scale, int S, cudaStream_t stream) {
-  return d == 64 ? launch_d<64>(q, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                                max_blocks, scale, S, stream)
-                 : launch_d<128>(q, kc, vc, table, seq_lens, o_part, lse_part, B, H, Hkv, num_blocks, bs,
-                                 max_blocks, scale, S, stream);
+                          const Out& out, int B, int H, int Hkv, int d, int num_blocks, int bs, int max_blocks,
+                          float scale, int S, cudaStream_t stream) {
+  return d == 64 ? launch_d<64>(q, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs, max_blocks, scale, S,
+                                stream)
+                 : launch_d<128>(q, kc, vc, table, seq_lens, out, B, H, Hkv, num_blocks, bs, max_blocks, scale, S,
+                                 stream);
 }
 
 // Shapes this kernel serves (any block size).
@@ -737,9 +780,10 @@ cudaError_t launch_decode_paged(const void* q, const void* k_cache, const void* 
                                 int num_blocks, int block_size, int max_blocks, float scale, int S,
                                 cudaStream_t stream) {
   if (!decmma::serves(d, block_size)) return cudaErrorInvalidValue;
-  cudaError_t e = decmma::launch(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, B, H, Hkv, d,
-                                 num_blocks, block_size, max_blocks, scale, S, stream);
-  if (e != cudaSuccess) return e;
+  const decmma::Out out{o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse};
+  cudaError_t e = decmma::launch(q, k_cache, v_cache, block_table, seq_lens, out, B, H, Hkv, d, num_blocks,
+                                 block_size, max_blocks, scale, S, stream);
+  if (e != cudaSuccess || S == 1) return e;  // one split: the kernel wrote o and lse
   return launch_attn_merge(o_part, lse_part, S, o, lse, static_cast<long long>(B) * H, d, stream);
 }
 

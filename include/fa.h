@@ -339,13 +339,15 @@ int fa_attn_merge(const float* o_parts, const float* lse_parts, int n_parts, voi
  *                query row over its request's tokens (no mask beyond the
  *                context length); query head h reads K/V head h / (H/Hkv).
  *   workspace    device buffer of fa_decode_workspace_bytes(B, H, d,
- *                n_splits) bytes (16-byte aligned), for the partial results.
+ *                n_splits) bytes (16-byte aligned), for the partial results
+ *                (required always; not touched when n_splits = 1).
  *   block_size   any size >= 1. Sizes that are a multiple of 8 dividing 128
  *                load each cache block as one TMA box; others are gathered
  *                token by token (fewer bytes per second).
  *   n_splits     the context of every request is cut into n_splits parts of
  *                whole 128-token tiles, processed in parallel and combined
- *                as in fa_attn_merge (two kernels on `stream`).
+ *                as in fa_attn_merge (two kernels on `stream`). With
+ *                n_splits = 1 one kernel writes o and lse directly.
  * Errors: null pointer, sizes < 1, Hkv not dividing H, bad scale ->
  * FA_ERR_INVALID_ARG; d not 64/128, B > 65535, Hkv·ceil(H/Hkv / 16) > 65535 ->
  * FA_ERR_UNSUPPORTED; short workspace -> FA_ERR_WORKSPACE; misaligned ->

@@ -53,6 +53,8 @@ def run_case(fa, q, kc, vc, table, lens, n_splits, scale):
     (2, 32, 8, 128, 128, [4097, 256], 3),
     (1, 16, 1, 128, 16, [777], 5),           # 16 query heads on one K/V head
     (3, 4, 2, 128, 16, [0, 1, 129], 2),      # an empty context
+    (3, 8, 2, 128, 16, [0, 300, 5], 1),      # one split (no merge): an empty context too
+    (2, 8, 2, 64, 3, [0, 1000], 1),          # one split, gathered
     (1, 2, 1, 64, 48, [2000], 7),            # block size not a power of two
     (2, 32, 1, 128, 16, [300, 1500], 3),     # 32 query heads on one K/V head: two CTAs of 16
     (1, 24, 1, 64, 32, [777], 2),            # 24 = 16 + 8
