@@ -23,7 +23,6 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <mutex>
 
 #include "../../include/fa.h"
 #include "fa_common.h"
@@ -32,22 +31,14 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
 // Device address of the scratch array on the current device (host code
-// cannot use the array's name as an address). Returns nullptr on failure.
+// cannot use the array's name as an address), looked up on every call: a
+// device reset reloads the module, and the array may then sit elsewhere.
+// Returns nullptr on failure.
 void* scratch_on_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
-  }
-  return g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -40,10 +40,10 @@
  *             limit) are reported by fa_last_device_error.
  *   Threads   entry points may be called from several host threads; each
  *             call works on its own descriptors.
- *   Devices   per-device state the library keeps (its side streams, the
- *             scratch address of fa_bwd_noalloc) lives as long as the
- *             process; after cudaDeviceReset on a device, do not call into
- *             the library on that device again in the same process.
+ *   Devices   per-device state the library keeps (its side streams) lives
+ *             as long as the process; after cudaDeviceReset on a device, do
+ *             not call into the library on that device again in the same
+ *             process.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -244,13 +244,11 @@ int fa_fwd_bwd_host(const fa_tensors* host, const fa_tensors* dev, void* workspa
  *   - Problems whose scratch need exceeds FA_BWD_NOALLOC_SCRATCH_BYTES are
  *     rejected with FA_ERR_WORKSPACE before anything is launched
  *     (B*H*N*4 bytes: up to 8,388,608 query rows over all heads).
- *   - The first call on a device looks up the array's device address with
- *     that device current (a one-time set-up per device); make that first
- *     call before any stream capture. The address is kept for the life of
- *     the process: after cudaDeviceReset (or any teardown of the device's
- *     primary context) the library's per-device state, this address
- *     included, is stale, so do not call into the library on that device
- *     again in the same process.
+ *   - Every call looks up the array's device address on the current
+ *     device (a runtime query, nothing launched), so the address stays
+ *     right after a device reset. The first call on a device may load the
+ *     library's device code; make it before any stream capture. Later
+ *     calls can be captured into a CUDA graph.
  *   - Every call on a device shares the one array. Calls whose kernels
  *     overlap on the GPU (different streams or host threads without
  *     ordering between them) race on it and give undefined results; order

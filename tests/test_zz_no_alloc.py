@@ -68,3 +68,32 @@ def test_noalloc_matches_fa_bwd_two_calls_in_a_row(L):
         # the backward uses no atomics: identical to the workspace path
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+
+
+@pytest.mark.gpu
+def test_noalloc_call_captures_into_a_graph(L):
+    # after an eager first call, a captured call (the scratch address looked up
+    # inside the capture) replays to the same bits as fa_bwd
+    dev = torch.device("cuda")
+    q, k, v, do = (t.to(dev) for t in make_inputs(1, 4, 300, 128, seed=43))
+    o, lse = fa.fwd(q, k, v, causal=True)
+    ref = fa.bwd(q, k, v, o, lse, do, causal=True)
+    _call_noalloc(L, q, k, v, o, lse, do, True)
+    torch.cuda.synchronize()
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            st = L.fa_bwd_noalloc(p(q), p(k), p(v), p(o), p(do), p(lse), p(dq), p(dk), p(dv),
+                                  1, 4, 300, 128, 1.0 / 128 ** 0.5, 1,
+                                  ctypes.c_void_p(s.cuda_stream))
+    assert st == 0
+    for t in (dq, dk, dv):
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    for a, b in zip((dq, dk, dv), ref):
+        assert torch.equal(a, b)
