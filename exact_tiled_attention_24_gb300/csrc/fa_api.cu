@@ -247,7 +247,9 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
   if (B > 65535 || static_cast<long long>(Hkv) * ((H / Hkv + 15) / 16) > 65535 || n_splits > 4096)
     return FA_ERR_UNSUPPORTED;
   const long long ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
-  if (ctx > INT_MAX / 2 || static_cast<long long>(num_blocks) * Hkv * block_size * d > (1ll << 40))
+  // The cache's token rows (num_blocks * Hkv * block_size) are indexed in
+  // 32 bits on the device: fewer than 2^32 - 1 (512 GB of cache at d = 64).
+  if (ctx > INT_MAX / 2 || static_cast<long long>(num_blocks) * Hkv * block_size >= 0xffffffffll)
     return FA_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < fa_decode_workspace_bytes(B, H, d, n_splits)) return FA_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||

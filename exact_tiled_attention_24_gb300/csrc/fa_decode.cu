@@ -350,60 +350,78 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
 
   // The same tile by per-token copies, run by a whole warp. resolve() turns
   // fetched table entries of rows lane, lane + 32, lane + 64 and lane + 96
-  // into element offsets (-1: past the context or a bad block index, zero
-  // fill); copy_tile() then moves chunk c (16 bytes) of row r into the
-  // 128-byte-swizzled K-major layout the products read: panel c / 8, at
-  // 128 r + 16 ((c mod 8) xor (r mod 8)).
+  // into cache row indices (token rows of d elements; NO_ROW past the
+  // context or for a bad block index, zero fill); copy_tile() then moves
+  // chunk c (16 bytes) of row r into the 128-byte-swizzled K-major layout
+  // the products read: panel c / 8, at 128 r + 16 ((c mod 8) xor (r mod 8)).
+  constexpr uint32_t NO_ROW = 0xffffffffu;  // the host keeps the cache below 2^32 - 1 rows
   const long long cache_elems = static_cast<long long>(num_blocks) * Hkv * bs * D;
-  auto resolve = [&](int tile, const int (&raw)[4], long long (&row_off)[4]) {
+  auto row_of = [&](int blk, int t, int bi) -> uint32_t {
+    return (static_cast<uint32_t>(blk) * static_cast<uint32_t>(Hkv) + static_cast<uint32_t>(hk)) *
+               static_cast<uint32_t>(bs) + static_cast<uint32_t>(t - bi * bs);
+  };
+  auto resolve = [&](int tile, const int (&raw)[4], uint32_t (&rows)[4]) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int t = tile * TK + lane + 32 * u;
-      long long off = -1;
+      uint32_t row = NO_ROW;
       if (t < Lb) {
         const int blk = raw[u], bi = t / bs;
         if (blk >= 0 && blk < num_blocks)
-          off = ((static_cast<long long>(blk) * Hkv + hk) * bs + (t - bi * bs)) * D;
+          row = row_of(blk, t, bi);
         else
           atomicExch(err, DEV_BAD_INDEX);
       }
-      row_off[u] = off;
+      rows[u] = row;
     }
   };
-  // GATHER: the same offsets with the entries loaded on the spot. (The two
+  // GATHER: the same rows with the entries loaded on the spot. (The two
   // forms stay apart: GATHER written as fetch() + resolve() measured 5%
   // slower at block sizes 12 to 48; its producer's instructions per tile
   // count there.)
-  auto lookup = [&](int tile, long long (&row_off)[4]) {
+  auto lookup = [&](int tile, uint32_t (&rows)[4]) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int t = tile * TK + lane + 32 * u;
-      long long off = -1;
+      uint32_t row = NO_ROW;
       if (t < Lb) {
         const int bi = t / bs;
         const long long ti = static_cast<long long>(b) * max_blocks + bi;
         const int blk = in_range(ti, 1, static_cast<long long>(B) * max_blocks, err) ? block_table[ti] : -1;
         if (blk >= 0 && blk < num_blocks)
-          off = ((static_cast<long long>(blk) * Hkv + hk) * bs + (t - bi * bs)) * D;
+          row = row_of(blk, t, bi);
         else
           atomicExch(err, DEV_BAD_INDEX);
       }
-      row_off[u] = off;
+      rows[u] = row;
     }
   };
-  auto copy_tile = [&](const __nv_bfloat16* cache, uint8_t* dst, const long long (&row_off)[4]) {
+  // Lane (c, rsub) copies chunk c of rows r = 32 u + r0 + RPI k + rsub. The
+  // chunk's swizzled slot depends on r mod 8 = (RPI k + rsub) mod 8 only, so
+  // the NX slots are computed once, and a copy costs a shuffle of the row
+  // index, one multiply-add for the address and the copy itself.
+  auto copy_tile = [&](const __nv_bfloat16* cache, uint8_t* dst, const uint32_t (&rows)[4]) {
     constexpr int CH = D / 8;     // 16-byte chunks per row
     constexpr int RPI = 32 / CH;  // rows per warp instruction
+    constexpr int NX = 8 / RPI;   // rows per swizzle period and warp instruction
     const int c = lane % CH, rsub = lane / CH;
+    const char* src_lane = reinterpret_cast<const char*>(cache) + c * 16;
+    uint8_t* dst_lane = dst + (c >> 3) * L::PANEL + rsub * 128;
+    uint32_t slot[NX];
+#pragma unroll
+    for (int k = 0; k < NX; ++k) slot[k] = static_cast<uint32_t>(((c & 7) ^ ((k * RPI + rsub) & 7)) << 4);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-#pragma unroll 4
-      for (int r1 = 0; r1 < 32; r1 += RPI) {
-        const int r = 32 * u + r1 + rsub;
-        const long long off = __shfl_sync(0xffffffffu, row_off[u], r1 + rsub);
-        const bool live = off >= 0 && in_range(off + c * 8, 8, cache_elems, err);
-        cp_async_16(dst + (c >> 3) * L::PANEL + r * 128 + (((c & 7) ^ (r & 7)) << 4),
-                    live ? cache + off + c * 8 : cache, live ? 16u : 0u);
+#pragma unroll 2
+      for (int r0 = 0; r0 < 32; r0 += 8) {
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+          const int r1 = r0 + k * RPI;
+          const uint32_t row = __shfl_sync(0xffffffffu, rows[u], r1 + rsub);
+          const bool live = row != NO_ROW && in_range(static_cast<long long>(row) * D + c * 8, 8, cache_elems, err);
+          const char* src = src_lane + static_cast<size_t>(live ? row : 0u) * (D * 2);
+          cp_async_16(dst_lane + (32 * u + r1) * 128 + slot[k], src, live ? 16u : 0u);
+        }
       }
     }
   };
@@ -414,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   auto gather_loop = [&](const __nv_bfloat16* cache, uint8_t* base, int stage_bytes, uint64_t* full,
                          uint64_t* empty, auto nst_c) {
     constexpr int NST = decltype(nst_c)::value;
-    long long cur[4], nxt[4] = {-1, -1, -1, -1};
+    uint32_t cur[4], nxt[4] = {NO_ROW, NO_ROW, NO_ROW, NO_ROW};
     if (AHEAD)
       resolve(tile0, raw_a, cur);
     else

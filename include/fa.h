@@ -347,8 +347,10 @@ int fa_attn_merge(const float* o_parts, const float* lse_parts, int n_parts, voi
  *                as in fa_attn_merge (two kernels on `stream`). With
  *                n_splits = 1 one kernel writes o and lse directly.
  * Errors: null pointer, sizes < 1, Hkv not dividing H, bad scale ->
- * FA_ERR_INVALID_ARG; d not 64/128, B > 65535, Hkv·ceil(H/Hkv / 16) > 65535 ->
- * FA_ERR_UNSUPPORTED; short workspace -> FA_ERR_WORKSPACE; misaligned ->
+ * FA_ERR_INVALID_ARG; d not 64/128, B > 65535, Hkv·ceil(H/Hkv / 16) > 65535,
+ * n_splits > 4096, num_blocks·Hkv·block_size >= 2^32 - 1 (token rows of the
+ * cache, indexed in 32 bits) -> FA_ERR_UNSUPPORTED; short workspace ->
+ * FA_ERR_WORKSPACE; misaligned ->
  * FA_ERR_MISALIGNED. A block-table entry outside [0, num_blocks) is never
  * dereferenced: the tokens it maps are skipped (the results are then
  * undefined) and fa_last_device_error reports FA_ERR_BAD_INDEX.

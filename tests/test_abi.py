@@ -172,6 +172,8 @@ def test_decode_and_merge_argument_errors(L):
     assert dec(d=96) == 2
     assert dec(B=70000) == 2                  # more requests than one grid dimension holds
     assert dec(max_blocks=1 << 27, bs=16) == 2   # a context of 2^31 tokens: past the int range
+    assert dec(num_blocks=1 << 28, Hkv=2, bs=8) == 2     # 2^32 token rows in the cache: past 32-bit row indices
+    assert dec(num_blocks=(1 << 28) - 1, Hkv=2, bs=8, ws_ptr=NUL) == 6  # just below: checks go on
     assert dec(ws_ptr=NUL) == 6
     assert dec(ws_bytes=ws - 1) == 6
     assert dec(q=MIS) == 3
