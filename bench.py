@@ -605,8 +605,8 @@ def run_ours(args, w, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline:
         heads = [(0, 0)]
         dt, fl, first = oracle_sample(w, q, k, v, do, heads, keep_first=True)
-        reps = 1
-        while dt * reps < 10.0 and reps < 8:
+        reps = 1  # heads timed: at least ~10 s of oracle work in all, at most 16 heads
+        while dt < 10.0 and reps < 16:
             dt2, _ = oracle_sample(w, q, k, v, do, [(0, reps % w.H)])
             dt += dt2
             reps += 1
@@ -713,7 +713,7 @@ def run_softmax(args, rw, rank, world, dist):
         k = 16
         xs = x_host[:k].to(torch.float64).numpy()
         reps, t0 = 0, time.perf_counter()
-        while reps < 1000 and (reps == 0 or time.perf_counter() - t0 < 5.0):
+        while reps < 2000 and (reps == 0 or time.perf_counter() - t0 < 10.0):
             softmax_safe(xs)
             reps += 1
         dt = time.perf_counter() - t0
@@ -883,7 +883,7 @@ def run_decode(args, dw, rank, world, dist):
         from oracle import decode_paged
         qs, kcs, vcs, tab, ln, sample_bytes, k = decode_oracle_sample(dw)
         reps, t0 = 0, time.perf_counter()
-        while reps < 200 and (reps == 0 or time.perf_counter() - t0 < 5.0):
+        while reps < 400 and (reps == 0 or time.perf_counter() - t0 < 10.0):
             decode_paged(qs, kcs, vcs, tab, ln, dw.d ** -0.5)
             reps += 1
         dt = time.perf_counter() - t0
