@@ -135,3 +135,33 @@ def test_fwd_bwd_host_with_pageable_memory(fa):
     torch.cuda.synchronize()
     for name, ref in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
         assert torch.equal(host[name], ref.cpu()), name
+
+
+def test_two_host_calls_in_flight_on_two_streams(fa):
+    # double buffering: calls on two streams, each with its own inputs and
+    # buffers, share the library's copy streams; each must give its own
+    # device calls' bits (B=2 H=8 over 2 K/V heads, N=700, causal, d=128)
+    B, H, Hkv, N, d = 2, 8, 2, 700, 128
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    calls = []
+    for i, s in enumerate(streams):
+        q, k, v, do = make_inputs(B, H, N, d, seed=900 + i, Hkv=Hkv)
+        host = {"q": q.pin_memory(), "k": k.pin_memory(), "v": v.pin_memory(), "dO": do.pin_memory()}
+        host.update(host_bufs(q, k, True))
+        dev = dev_bufs(q, k, True)
+        ws = torch.empty(fa.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+        calls.append((q, k, v, do, host, dev, ws, s))
+    torch.cuda.synchronize()
+    for rnd in range(3):  # several rounds, so calls of one stream meet the other's in flight
+        for q, k, v, do, host, dev, ws, s in calls:
+            with torch.cuda.stream(s):
+                fa.fwd_bwd_host(host, dev, ws, causal=True, n_chunks=3)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    for q, k, v, do, host, dev, ws, s in calls:
+        qg, kg, vg, dog = (t.cuda() for t in (q, k, v, do))
+        o, lse = fa.fwd(qg, kg, vg, causal=True)
+        dq, dk, dv = fa.bwd(qg, kg, vg, o, lse, dog, causal=True)
+        torch.cuda.synchronize()
+        for name, ref in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            assert torch.equal(host[name], ref.cpu()), name
