@@ -515,7 +515,7 @@ def run_ours(args, w, rank, world, dist):
     # run it), so one step's result copies overlap the next step's input
     # copies; every step still copies all of its inputs in and its results
     # out inside the timed region.
-    e2e_steps = max(3, args.steps // 4)
+    e2e_steps = max(12, args.steps // 4)  # enough that the in-flight pipeline's start weighs little
     inflight = max(1, args.e2e_inflight)
 
     def host_out(t):
