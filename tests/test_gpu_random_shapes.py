@@ -41,7 +41,7 @@ def fa():
     return m
 
 
-@pytest.mark.parametrize("B,H,Hkv,N,d,causal,scale,seed", draw_cases(32, seed=2026))
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,scale,seed", draw_cases(64, seed=2026))
 def test_random_shape_vs_oracle(fa, B, H, Hkv, N, d, causal, scale, seed):
     q, k, v, do = make_inputs(B, H, N, d, seed=seed, Hkv=Hkv)
     dev = torch.device("cuda")
@@ -87,7 +87,7 @@ def draw_decode_cases(n, seed):
     return cases
 
 
-@pytest.mark.parametrize("B,H,Hkv,d,bs,lens,splits,seed", draw_decode_cases(24, seed=2027))
+@pytest.mark.parametrize("B,H,Hkv,d,bs,lens,splits,seed", draw_decode_cases(48, seed=2027))
 def test_random_decode_vs_oracle(fa, B, H, Hkv, d, bs, lens, splits, seed):
     from oracle import decode_paged
     g = torch.Generator().manual_seed(seed)
