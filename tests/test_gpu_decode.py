@@ -146,3 +146,27 @@ def test_decode_peaked_scores_raise_the_reference(fa, d):
         ro, rlse = decode_paged(qd, kd, to_f64(vc), table.numpy(), lens.numpy(), scale)
         assert_o(o, ro)
         assert_lse(lse, rlse)
+
+
+@pytest.mark.parametrize("name", ["d1", "d2"])
+def test_decode_workload_full_size_sampled_requests(fa, name):
+    # the decode workloads at full size, in the launch configuration the bench
+    # times (8 context splits), against the oracle on sampled requests: each
+    # one's blocks are gathered in table order into a small cache of its own
+    from exact_tiled_attention_24_gb300.workloads import DECODE_WORKLOADS, make_decode
+    w = DECODE_WORKLOADS[name]
+    q, kc, vc, table, lens = make_decode(w, torch.device("cuda"))
+    o, lse = fa.decode_paged(q, kc, vc, table, lens, n_splits=w.n_splits)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    scale = w.d ** -0.5
+    for b in sorted({0, int(lens.argmax()), w.B - 1}):  # first, longest, last request
+        L = int(lens[b])
+        nb = (L + w.block_size - 1) // w.block_size
+        blocks = table[b, :nb].long()
+        kc_b, vc_b = kc[blocks].cpu(), vc[blocks].cpu()
+        tab_b = np.arange(nb, dtype=np.int32)[None, :]
+        ro, rlse = decode_paged(to_f64(q[b:b + 1]), to_f64(kc_b), to_f64(vc_b), tab_b,
+                                np.array([L], dtype=np.int32), scale)
+        assert_o(o[b:b + 1], ro)
+        assert_lse(lse[b:b + 1], rlse)
