@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, Cfg<GM>::CTAS) decode_mma_kernel(
   auto copy_tile = [&](const __nv_bfloat16* cache, uint8_t* dst, const uint32_t (&rows)[4]) {
     constexpr int CH = D / 8;     // 16-byte chunks per row
     constexpr int RPI = 32 / CH;  // rows per warp instruction
-    constexpr int NX = 8 / RPI;   // rows per swizzle period and warp instruction
+    constexpr int NX = 8 / RPI;   // warp instructions per 8-row swizzle period
     const int c = lane % CH, rsub = lane / CH;
     const char* src_lane = reinterpret_cast<const char*>(cache) + c * 16;
     uint8_t* dst_lane = dst + (c >> 3) * L::PANEL + rsub * 128;
