@@ -5,7 +5,9 @@ combinations no hand-picked case names are exercised too:
   kernel order fa_bwd takes) and the dQ-sweep-with-D stage order;
 - paged decode: batch, query heads per K/V head (up to 20, so beyond one
   CTA's 16), block size (TMA boxes and per-token gathering), context
-  lengths (empty and single-token ones included), splits and head size."""
+  lengths (empty and single-token ones included), splits and head size.
+Each sweep has a second, larger draw: attention lengths 700 to 4000, decode
+contexts up to 20,000 tokens over up to 32 splits."""
 import random
 
 import pytest
@@ -18,15 +20,18 @@ from gpu_helpers import assert_grad_scaled, assert_lse, assert_o
 pytestmark = pytest.mark.gpu
 
 
-def draw_cases(n, seed):
+def draw_cases(n, seed, large=False):
     rng = random.Random(seed)
     cases = []
     for i in range(n):
         d = rng.choice((64, 128))
         Hkv = rng.randint(1, 3)
         G = rng.choice((1, 1, 2, 3, 4))
-        B = rng.randint(1, 3)
-        N = rng.choice((1, 2, 63, 127, 128, 129)) if i % 4 == 0 else rng.randint(1, 700)
+        B = rng.randint(1, 2 if large else 3)
+        if large:  # several hundred tiles per head, tile-boundary lengths among them
+            N = rng.choice((1023, 1024, 1025, 2047, 2049, 4000)) if i % 4 == 0 else rng.randint(700, 4000)
+        else:
+            N = rng.choice((1, 2, 63, 127, 128, 129)) if i % 4 == 0 else rng.randint(1, 700)
         causal = rng.random() < 0.5
         scale = rng.uniform(0.5, 1.5) / d ** 0.5
         cases.append((B, Hkv * G, Hkv, N, d, causal, round(scale, 5), 9000 + i))
@@ -41,7 +46,8 @@ def fa():
     return m
 
 
-@pytest.mark.parametrize("B,H,Hkv,N,d,causal,scale,seed", draw_cases(64, seed=2026))
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,scale,seed",
+                         draw_cases(64, seed=2026) + draw_cases(20, seed=4041, large=True))
 def test_random_shape_vs_oracle(fa, B, H, Hkv, N, d, causal, scale, seed):
     q, k, v, do = make_inputs(B, H, N, d, seed=seed, Hkv=Hkv)
     dev = torch.device("cuda")
@@ -69,7 +75,7 @@ def test_random_shape_vs_oracle(fa, B, H, Hkv, N, d, causal, scale, seed):
     assert torch.allclose(Dvec.double(), ref_D, atol=1e-4, rtol=1e-5)
 
 
-def draw_decode_cases(n, seed):
+def draw_decode_cases(n, seed, large=False):
     rng = random.Random(seed)
     cases = []
     for i in range(n):
@@ -81,13 +87,17 @@ def draw_decode_cases(n, seed):
         lens = []
         for _ in range(B):
             r = rng.random()
-            lens.append(0 if r < 0.1 else (1 if r < 0.2 else rng.randint(2, 3000)))
-        splits = rng.randint(1, 6)
+            if large:  # long contexts, many splits
+                lens.append(0 if r < 0.05 else (1 if r < 0.1 else rng.randint(2, 20000)))
+            else:
+                lens.append(0 if r < 0.1 else (1 if r < 0.2 else rng.randint(2, 3000)))
+        splits = rng.choice((1, 2, 5, 8, 16, 32)) if large else rng.randint(1, 6)
         cases.append((B, Hkv * G, Hkv, d, bs, tuple(lens), splits, 7000 + i))
     return cases
 
 
-@pytest.mark.parametrize("B,H,Hkv,d,bs,lens,splits,seed", draw_decode_cases(48, seed=2027))
+@pytest.mark.parametrize("B,H,Hkv,d,bs,lens,splits,seed",
+                         draw_decode_cases(48, seed=2027) + draw_decode_cases(20, seed=4042, large=True))
 def test_random_decode_vs_oracle(fa, B, H, Hkv, d, bs, lens, splits, seed):
     from oracle import decode_paged
     g = torch.Generator().manual_seed(seed)
