@@ -165,3 +165,40 @@ def test_two_host_calls_in_flight_on_two_streams(fa):
         torch.cuda.synchronize()
         for name, ref in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
             assert torch.equal(host[name], ref.cpu()), name
+
+
+def _draw_host_cases(n, seed):
+    import random
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        d = rng.choice((64, 128))
+        Hkv = rng.randint(1, 4)
+        G = rng.choice((1, 1, 2, 4))
+        B = rng.randint(1, 3)
+        N = rng.randint(1, 900)
+        chunks = rng.choice((0, 1, 2, 3, 5, 64))
+        cases.append((B, Hkv * G, Hkv, N, d, rng.random() < 0.5, chunks, 600 + i))
+    return cases
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,chunks,seed", _draw_host_cases(12, seed=2028))
+def test_random_host_pipeline_matches_device_calls(fa, B, H, Hkv, N, d, causal, chunks, seed):
+    # seeded shapes and slice counts: the pipelined call gives the device calls'
+    # bits (B*H <= 48 and N <= 900 keep every slice and the whole problem below
+    # the dK/dV grid at which fa_bwd switches to forming D in the dQ sweep, so
+    # all take one kernel order)
+    q, k, v, do = make_inputs(B, H, N, d, seed=seed, Hkv=Hkv)
+    host = {"q": q.pin_memory(), "k": k.pin_memory(), "v": v.pin_memory(), "dO": do.pin_memory()}
+    host.update(host_bufs(q, k, True))
+    dev = dev_bufs(q, k, True)
+    ws = torch.empty(fa.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    fa.fwd_bwd_host(host, dev, ws, causal=causal, n_chunks=chunks)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    qg, kg, vg, dog = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qg, kg, vg, causal=causal)
+    dq, dk, dv = fa.bwd(qg, kg, vg, o, lse, dog, causal=causal)
+    torch.cuda.synchronize()
+    for name, ref in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.equal(host[name], ref.cpu()), name
